@@ -1,0 +1,228 @@
+/*
+ * dec.h -- C ABI of the GB300 persistent MoE decode engine.
+ *
+ * One call of dec_step runs a whole decode step (every layer, the LM head and the greedy
+ * argmax) as ONE launch of one persistent, warp-specialised kernel, instead of a chain of
+ * per-operator kernels. This is the execution model described on the page "Ultra-High
+ * Interactivity on NVIDIA GPUs? TileRT on InferenceX", section "But What Exactly is TileRT?"
+ * (the host launches once, warp groups specialise on data movement and compute, stages overlap
+ * at tile granularity and intermediates stay in registers, shared memory and L2), applied to the
+ * per-layer decode recipe of "vLLM's Kimi K3 Backend Hits 842 Tokens per Second", section "Four
+ * changes drive the gains" (shape-aware small-N GEMV, split-K at larger batches, the shared
+ * expert overlapped with routing, weight prefetch ahead of use).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are CUDA device pointers; "host" pointers are CPU memory.
+ *  - bf16 tensors are passed as 16-bit bit patterns (any type with that layout).
+ *  - FP8 matrices are OCP E4M3 codes, row-major [rows][cols], with fp32 block scales
+ *    [ceil(rows/128)][ceil(cols/128)]; element (r, c) means scale[r/128][c/128] * e4m3(W[r][c]).
+ *  - A `stream` argument is a cudaStream_t; NULL means the engine's own (non-blocking) stream,
+ *    so the legacy default stream must be passed as cudaStreamLegacy.
+ *  - Every call returns a dec_status. Errors found on the device (a wait that ran out of time,
+ *    a failed bounds check) are reported by the next call that synchronises (dec_sync,
+ *    dec_generate, dec_prefill_kv, dec_export_kv) and POISON the engine: later calls return
+ *    DEC_ERR_POISONED. dec_last_error() gives a human-readable reason.
+ *  - No call falls back to a CPU path: shapes the kernel does not handle give
+ *    DEC_ERR_UNSUPPORTED.
+ *  - The engine is not thread-safe; use one engine per host thread.
+ */
+#ifndef DEC_H
+#define DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dec_engine dec_engine; /* opaque, owned by the library */
+
+typedef enum {
+  DEC_OK = 0,
+  DEC_ERR_ARG = -1,         /* bad argument (NULL, out of range, batch > max_batch, ...) */
+  DEC_ERR_CUDA = -2,        /* a CUDA runtime call failed */
+  DEC_ERR_OOM = -3,         /* device allocation failed */
+  DEC_ERR_TIMEOUT = -4,     /* a device-side wait ran out of time; engine poisoned */
+  DEC_ERR_UNSUPPORTED = -5, /* model shape or batch the kernel does not implement */
+  DEC_ERR_POISONED = -6,    /* an earlier device error made the engine unusable */
+  DEC_ERR_DEVICE = -7,      /* a device-side consistency check failed; engine poisoned */
+  DEC_ERR_CAPACITY = -8     /* a sequence would exceed max_ctx */
+} dec_status;
+
+/* Model shape. The layer is a pre-norm decoder: RMSNorm -> q/k/v projection -> RoPE (half-split
+   pairing) -> GQA attention over a bf16 KV cache -> output projection + residual -> RMSNorm ->
+   FFN + residual. The FFN is either a dense SwiGLU of width dense_ffn (n_experts == 0), or a
+   sigmoid-routed MoE: top_k of n_experts SwiGLU experts of width moe_inter with gates normalised
+   over the selected scores, plus n_shared (0 or 1) always-on experts of the same width.
+   ("Kimi K3: The Manos, The Mythos, The Legendos": GQA; the expert as SwiGLU; top-k over router
+   scores; the residual x_{l+1} = x_l + f(x_l).) vocab == 0 builds a headless stack that maps a
+   bf16 hidden state to a bf16 hidden state (no embedding, LM head or argmax). */
+typedef struct {
+  int32_t n_layers;   /* >= 1 */
+  int32_t hidden;     /* multiple of 128 */
+  int32_t n_heads;    /* query heads */
+  int32_t n_kv_heads; /* KV heads; n_heads / n_kv_heads must be 2 or 4 */
+  int32_t head_dim;   /* 64 or 128 */
+  int32_t n_experts;  /* 0 for a dense FFN, else <= 128 */
+  int32_t top_k;      /* 1..16, <= n_experts */
+  int32_t moe_inter;  /* expert SwiGLU width, multiple of 128 */
+  int32_t n_shared;   /* 0 or 1 */
+  int32_t dense_ffn;  /* dense SwiGLU width (multiple of 128) when n_experts == 0, else 0 */
+  int32_t vocab;      /* 0: headless stack */
+  int32_t max_ctx;    /* KV positions per sequence */
+  int32_t max_batch;  /* sequences decoded together, 1..8 */
+  float rms_eps;
+  float rope_theta;
+} dec_model_cfg;
+
+/* An FP8-E4M3 matrix with its fp32 block scales (both device pointers, borrowed). */
+typedef struct {
+  const void* w;
+  const float* scale;
+} dec_fp8_mat;
+
+/* One layer's weights. Matrix shapes (rows x cols): wq [n_heads*head_dim x hidden],
+   wk/wv [n_kv_heads*head_dim x hidden], wo [hidden x n_heads*head_dim],
+   router [n_experts x hidden], gate/up [inter x hidden], down [hidden x inter].
+   The expert and shared arrays are HOST arrays of device matrices. */
+typedef struct {
+  const void* attn_norm; /* device bf16 [hidden] */
+  dec_fp8_mat wq, wk, wv, wo;
+  const void* ffn_norm; /* device bf16 [hidden] */
+  dec_fp8_mat router;
+  const dec_fp8_mat* expert_gate; /* host array [n_experts] */
+  const dec_fp8_mat* expert_up;
+  const dec_fp8_mat* expert_down;
+  const dec_fp8_mat* shared_gate; /* host array [n_shared] */
+  const dec_fp8_mat* shared_up;
+  const dec_fp8_mat* shared_down;
+  dec_fp8_mat ffn_gate, ffn_up, ffn_down; /* dense FFN */
+} dec_layer_weights;
+
+typedef struct {
+  const void* embed;      /* device bf16 [vocab][hidden] (vocab > 0) */
+  const void* final_norm; /* device bf16 [hidden] (vocab > 0) */
+  dec_fp8_mat lm_head;    /* [vocab x hidden] (vocab > 0) */
+  const dec_layer_weights* layers; /* host array [n_layers] */
+} dec_weights;
+
+/* Host-only check of a model shape (no CUDA needed). DEC_OK, DEC_ERR_ARG (inconsistent) or
+   DEC_ERR_UNSUPPORTED (consistent but not implemented by the kernel). */
+dec_status dec_validate_cfg(const dec_model_cfg* cfg);
+
+/* Build an engine on the current CUDA device: validates the shape, copies every weight into
+   library-owned memory (repacked into the kernel's tile order; the caller may free its buffers
+   once the call returns), builds the RoPE table (angles in double on the host), allocates the
+   KV cache [n_layers][max_batch][n_kv_heads][max_ctx][head_dim] bf16 x2 and the workspace, and
+   checks that one CTA per SM can be co-resident. All sequence lengths start at 0. Work is
+   queued on `stream` and synchronised before return. *out receives the engine (NULL on
+   failure). */
+dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* weights, void* stream,
+                    dec_engine** out);
+
+/* Fill the KV cache of sequence slots [seq, seq + n_seq).
+   Token mode (k_import == NULL): token_ids is device int32 [n_seq][n_tokens]; the engine runs
+   n_tokens batched decode steps (slots decoded together), appending to each slot's current
+   length, and discards the logits. This is decode-engine prefill as on the pages' prefill/decode
+   split; it is not a fast prefill path.
+   Import mode (k_import != NULL): copies an external KV state, device bf16
+   [n_layers][n_kv_heads][n_tokens][head_dim] for K (post-RoPE) and V, into positions
+   0..n_tokens of every slot in the range and sets their length to n_tokens (the handoff of a KV
+   cache produced elsewhere, as in the TileRT page's section "PD Disaggregated Engine with vLLM
+   and TileRT"). n_tokens == 0 is a no-op in both modes. Synchronises. */
+typedef struct {
+  int32_t seq;
+  int32_t n_seq;
+  const int32_t* token_ids; /* device, token mode */
+  int32_t n_tokens;
+  const void* k_import; /* device, import mode */
+  const void* v_import;
+} dec_ctx;
+dec_status dec_prefill_kv(dec_engine* eng, const dec_ctx* ctx);
+
+/* One decode step of `batch` sequences in slots [seq0, seq0 + batch). Token b is written at
+   position length[seq0 + b] and attends over positions 0..length (inclusive); the lengths grow
+   by one. Exactly one kernel launch on `stream`; nothing is synchronised.
+     tokens      device int32 [batch]         input ids (vocab > 0)
+     hidden_in   device bf16 [batch][hidden]  input hidden states (vocab == 0; also accepted
+                                              with vocab > 0 in place of tokens)
+     logits      device fp32 [batch][vocab]   caller-owned output, may be NULL
+     next_tokens device int32 [batch]         greedy argmax (lowest id on ties), may be NULL
+     hidden_out  device bf16 [batch][hidden]  final residual stream (before the final norm),
+                                              may be NULL
+   batch == 0 is a no-op. Errors: DEC_ERR_ARG, DEC_ERR_CAPACITY (a length would pass max_ctx),
+   DEC_ERR_POISONED, DEC_ERR_CUDA (launch failure). */
+typedef struct {
+  const int32_t* tokens;
+  const void* hidden_in;
+  int32_t batch;
+  int32_t seq0;
+  float* logits;
+  int32_t* next_tokens;
+  void* hidden_out;
+  void* stream;
+} dec_step_args;
+dec_status dec_step_ex(dec_engine* eng, const dec_step_args* args);
+
+/* The plain form: slots [0, batch), token input, logits/next_tokens outputs (may be NULL). */
+dec_status dec_step(dec_engine* eng, const int32_t* token_ids, int32_t batch, float* logits,
+                    int32_t* next_tokens, void* stream);
+
+/* Greedy generation from HOST buffers: copies first_tokens (host int32 [batch]) to the device,
+   runs n_steps device-chained decode steps of slots [0, batch) (step i's argmax is step i+1's
+   input, with no host round trip), copies the generated tokens back to out_tokens (host int32
+   [n_steps][batch]) and synchronises. Requires vocab > 0. */
+dec_status dec_generate(dec_engine* eng, const int32_t* first_tokens, int32_t batch,
+                        int32_t n_steps, int32_t* out_tokens, void* stream);
+
+/* Sequence lengths (positions already in the cache). Setting a length rewinds or advances a
+   slot without touching the cache contents. */
+dec_status dec_set_length(dec_engine* eng, int32_t seq, int32_t length);
+dec_status dec_get_length(dec_engine* eng, int32_t seq, int32_t* length);
+
+/* Copy positions [pos0, pos0 + n) of one slot and layer out of the KV cache into device bf16
+   buffers k_out/v_out [n_kv_heads][n][head_dim]. Synchronises. */
+dec_status dec_export_kv(dec_engine* eng, int32_t seq, int32_t layer, int32_t pos0, int32_t n,
+                         void* k_out, void* v_out);
+
+/* Wait for all queued engine work and read the device status word. */
+dec_status dec_sync(dec_engine* eng);
+
+/* Engine facts for tools and benchmarks. */
+typedef struct {
+  int32_t grid;           /* persistent CTAs (one per SM) */
+  int32_t threads;        /* threads per CTA */
+  int32_t smem_bytes;     /* dynamic shared memory per CTA */
+  int32_t ring_slots;     /* stages of the shared-memory weight ring */
+  int32_t stages_per_layer;
+  int64_t weight_bytes;   /* repacked weight bytes held by the engine */
+  int64_t kv_bytes;       /* KV cache bytes */
+  int64_t workspace_bytes;
+  int64_t launches;       /* kernel launches issued by this engine so far */
+} dec_info;
+dec_status dec_get_info(dec_engine* eng, dec_info* out);
+
+/* Routing of the most recent step at one layer (MoE models): copies the selected experts
+   (score-descending) into host idx [max_batch][top_k] and their normalised gates into host
+   gates [max_batch][top_k]; rows >= the step's batch are stale. Synchronises. */
+dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* gates);
+
+/* Per-step device timestamps (%globaltimer, ns) written by CTA 0 at the start of the step, at
+   every grid-wide stage boundary and at the end: copies the most recent step's stamps into
+   host_buf[0..n) and returns how many were written in *n_written. Synchronises. */
+dec_status dec_get_trace(dec_engine* eng, uint64_t* host_buf, int32_t n, int32_t* n_written);
+
+/* Reason for the last failing call on this engine ("" if none). Valid until the next call. */
+const char* dec_last_error(const dec_engine* eng);
+
+/* Fixed string naming a status code. */
+const char* dec_status_string(dec_status s);
+
+/* Release every device buffer of the engine (synchronises first). NULL is a no-op. */
+void dec_destroy(dec_engine* eng);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DEC_H */

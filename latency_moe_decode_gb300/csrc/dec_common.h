@@ -1,0 +1,99 @@
+// Internal layout shared by the engine's host code and its persistent kernel.
+#pragma once
+#include <cstdint>
+
+namespace dec {
+
+// Tiles: 128 weight rows x 128 columns of E4M3 codes (one 128x128 scale block), stored in the
+// order the consumer warps read them, followed by a 16-byte header {scale of rows 0..63, scale
+// of rows 64..127, 0, 0}. Two 64-row halves may come from different matrices (q/k/v heads, or
+// an expert's gate and up rows interleaved so one tile yields both SwiGLU operands).
+constexpr int kTileRows = 128;
+constexpr int kTileK = 128;
+constexpr int kTileData = kTileRows * kTileK;  // 16384
+constexpr int kTileBytes = kTileData + 16;     // 16400
+constexpr int kSlotBytes = kTileBytes;         // one ring slot holds one weight tile or one KV tile
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kKvTilePos = 32;                       // KV positions per ring slot
+constexpr int kMaxBatch = 8;
+constexpr int kTraceSlots = 512;                     // stamps kept per step
+
+// Device error codes (low byte) -- the upper bytes carry where it happened.
+enum : int {
+  kDevOk = 0,
+  kDevTimeout = 1,
+  kDevBadArg = 2,
+};
+
+struct LayerDev {
+  const uint8_t* qkv;     // tiles, q/k/v rows, [n_rb_qkv][kb_d]
+  const uint8_t* o;       // [n_rb_d][kb_o]
+  const uint8_t* router;  // [n_rb_router][kb_d]
+  const uint8_t* sh_gu;   // shared (or dense FFN) gate/up, [n_rb_gu][kb_d]
+  const uint8_t* sh_d;    // shared (or dense FFN) down, [n_rb_d][kb_i]
+  const uint8_t* e_gu;    // routed experts gate/up, expert e at e_gu + e * e_gu_stride
+  const uint8_t* e_d;     // routed experts down
+  const uint16_t* attn_norm;
+  const uint16_t* ffn_norm;
+};
+
+// Everything the kernel reads, passed by value at launch.
+struct KParams {
+  // model shape
+  int L, d, hq, hkv, hd, E, topk, inter, nsh, dense, V, max_ctx, MB;
+  float eps;
+  // tile geometry
+  int kb_d, kb_o, kb_i;
+  int n_rb_qkv, n_rb_d, n_rb_gu, n_rb_router, n_rb_lm;
+  long long e_gu_stride, e_d_stride;
+  int umax;       // most distinct routed experts one step can select
+  int nch;        // attention chunks per (sequence, KV head)
+  int ring;       // ring slots
+  int xmax;       // elements per token of the shared-memory activation buffer
+  // weights and tables
+  const LayerDev* layers;
+  const uint16_t* embed;
+  const uint16_t* final_norm;
+  const uint8_t* lm;
+  const float2* rope;  // [max_ctx][hd/2] (cos, sin)
+  uint16_t* kc;        // [L][MB][hkv][max_ctx][hd]
+  uint16_t* vc;
+  int32_t* lengths;    // [MB]
+  // activations
+  uint16_t* xbuf;   // [2][MB][d]
+  uint16_t* xmid;   // [MB][d]
+  uint16_t* qbuf;   // [MB][hq*hd]
+  uint16_t* obuf;   // [MB][hq*hd]
+  uint16_t* hsh;    // [MB][inter_sh]
+  uint16_t* hrt;    // [umax][MB][inter]
+  // split-K partial sums: [segment][slot][MB][128] fp32, and per-output arrival counters
+  float *part_qkv, *part_o, *part_router, *part_shgu, *part_rtgu, *part_d, *part_lm;
+  int *cnt_qkv, *cnt_o, *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
+  // attention split-KV partials: [MB][hkv][nch][group][hd + 2], counters [MB][hkv]
+  float* attn_part;
+  int* attn_cnt;
+  // routing result of the current layer
+  int* rt_u;          // [1] number of distinct experts
+  int* rt_elist;      // [E] distinct experts, ascending
+  float* rt_gate;     // [MB][E] gate of token b for distinct expert u (0 if not selected)
+  int* rt_idx;        // [L][MB][topk] selections (score-descending) for inspection
+  float* rt_topk_gate;// [L][MB][topk]
+  unsigned* rt_flag;  // [L] = epoch once the layer's routing is published
+  unsigned long long* amax;  // [MB] packed (ordered logit, ~id) maxima
+  unsigned* gbar;     // [0] arrivals, [32] generation (separate lines)
+  int* err;           // device status word
+  float* logits_ws;   // [MB][V] when the caller gives no logits buffer
+  unsigned long long* trace;  // [kTraceSlots]
+  // this step
+  const int32_t* tokens;
+  const uint16_t* hidden_in;
+  int B, seq0;
+  float* logits;
+  int32_t* next_tokens;
+  uint16_t* hidden_out;
+  unsigned epoch;
+  unsigned long long timeout_ns;
+};
+
+}  // namespace dec

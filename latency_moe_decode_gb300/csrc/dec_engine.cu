@@ -1,0 +1,765 @@
+// Host side of the decode engine: validation, weight repacking into kernel tiles, KV cache and
+// workspace allocation, the per-step cooperative launch and status readback. Implements dec.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "dec.h"
+#include "dec_kernel.cuh"
+
+using namespace dec;
+
+namespace {
+
+// ---------------------------------------------------------------------------------------------
+// repacking: a tile is two 64-row halves; each half comes from one source matrix.
+
+struct RepackDesc {
+  const uint8_t* w[3];
+  const float* s[3];
+  int n[3];       // rows of each source
+  int halves[3];  // 64-row halves taken from each source (stacked mode)
+  int nsrc;
+  int interleave; // 1: half h comes from source h % 2, rows 64 * (h / 2)
+  int K;          // columns (multiple of 128)
+};
+
+__global__ void repack_kernel(const RepackDesc d, uint8_t* dst) {
+  const int kbn = d.K / kTileK;
+  const int tile = blockIdx.x;  // rb * kbn + kb
+  const int rb = tile / kbn, kb = tile % kbn;
+  uint8_t* out = dst + (size_t)tile * kTileBytes;
+  for (int q = threadIdx.x; q < kTileData / 16; q += blockDim.x) {
+    const int l = q & 31, w = (q >> 5) & 7, i = q >> 8;
+    const int row = i * 32 + l;  // row inside the tile
+    const int h = rb * 2 + row / 64;
+    int src = -1, srow = 0;
+    if (d.interleave) {
+      src = h & 1;
+      srow = (h >> 1) * 64 + (row & 63);
+    } else {
+      int hh = h;
+      for (int s = 0; s < d.nsrc; ++s) {
+        if (hh < d.halves[s]) {
+          src = s;
+          srow = hh * 64 + (row & 63);
+          break;
+        }
+        hh -= d.halves[s];
+      }
+    }
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (src >= 0 && srow < d.n[src]) {
+      const uint8_t* p = d.w[src] + (size_t)srow * d.K + kb * kTileK + w * 16;
+      v = *reinterpret_cast<const uint4*>(p);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)q * 16) = v;
+  }
+  if (threadIdx.x < 2) {
+    const int h = rb * 2 + threadIdx.x;
+    int src = -1, srow = 0;
+    if (d.interleave) {
+      src = h & 1;
+      srow = (h >> 1) * 64;
+    } else {
+      int hh = h;
+      for (int s = 0; s < d.nsrc; ++s) {
+        if (hh < d.halves[s]) {
+          src = s;
+          srow = hh * 64;
+          break;
+        }
+        hh -= d.halves[s];
+      }
+    }
+    float sc = 0.f;
+    if (src >= 0 && srow < d.n[src]) sc = d.s[src][(size_t)(srow / 128) * kbn + kb];
+    reinterpret_cast<float*>(out + kTileData)[threadIdx.x] = sc;
+    if (threadIdx.x == 0) reinterpret_cast<float*>(out + kTileData)[2] = 0.f;
+    if (threadIdx.x == 1) reinterpret_cast<float*>(out + kTileData)[3] = 0.f;
+  }
+}
+
+__global__ void transpose_tokens_kernel(const int32_t* src, int n_seq, int n_tok, int32_t* dst) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_seq * n_tok) {
+    int s = i / n_tok, t = i % n_tok;
+    dst[(size_t)t * n_seq + s] = src[i];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+
+using KernelFn = void (*)(const KParams);
+
+template <int BM, int HD, int G>
+KernelFn pick_kernel() {
+  return decode_step_kernel<BM, HD, G>;
+}
+
+KernelFn kernel_for(int bm, int hd, int group) {
+#define DEC_K(B, H, GR) \
+  if (bm == B && hd == H && group == GR) return pick_kernel<B, H, GR>();
+  DEC_K(1, 64, 2) DEC_K(2, 64, 2) DEC_K(4, 64, 2) DEC_K(8, 64, 2)
+  DEC_K(1, 128, 4) DEC_K(2, 128, 4) DEC_K(4, 128, 4) DEC_K(8, 128, 4)
+#undef DEC_K
+  return nullptr;
+}
+
+const int kBmChoices[4] = {1, 2, 4, 8};
+
+}  // namespace
+
+struct dec_engine {
+  dec_model_cfg cfg{};
+  int device = 0, sms = 0, grid = 0;
+  cudaStream_t stream = nullptr;
+  KParams base{};
+  std::vector<void*> allocs;
+  LayerDev* d_layers = nullptr;
+  int hd = 0, group = 0;
+  KernelFn kern[4] = {nullptr, nullptr, nullptr, nullptr};
+  int smem[4] = {0, 0, 0, 0};
+  int ring[4] = {0, 0, 0, 0};
+  int nch_max = 1;
+  std::vector<int32_t> lengths;
+  unsigned epoch = 0;
+  bool poisoned = false;
+  std::string err;
+  int32_t* d_hist = nullptr;
+  int64_t launches = 0, weight_bytes = 0, kv_bytes = 0, ws_bytes = 0;
+};
+
+namespace {
+
+dec_status fail(dec_engine* e, dec_status s, const std::string& msg) {
+  if (e) e->err = msg;
+  return s;
+}
+
+dec_status cuda_fail(dec_engine* e, cudaError_t c, const char* what) {
+  return fail(e, c == cudaErrorMemoryAllocation ? DEC_ERR_OOM : DEC_ERR_CUDA,
+              std::string(what) + ": " + cudaGetErrorString(c));
+}
+
+#define DEC_CUDA(call)                                   \
+  do {                                                   \
+    cudaError_t _c = (call);                             \
+    if (_c != cudaSuccess) return cuda_fail(e, _c, #call); \
+  } while (0)
+
+template <typename T>
+dec_status dalloc(dec_engine* e, T** p, size_t bytes, int64_t* account) {
+  void* v = nullptr;
+  cudaError_t c = cudaMalloc(&v, bytes ? bytes : 16);
+  if (c != cudaSuccess) return cuda_fail(e, c, "cudaMalloc");
+  e->allocs.push_back(v);
+  if (account) *account += (int64_t)bytes;
+  *p = reinterpret_cast<T*>(v);
+  return DEC_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dec_status repack(dec_engine* e, const RepackDesc& d, int n_rb, uint8_t** out) {
+  for (int s = 0; s < d.nsrc; ++s)
+    if (d.w[s] && (!aligned16(d.w[s]) || !d.s[s])) return fail(e, DEC_ERR_ARG, "weight not 16-byte aligned or scale missing");
+  const int kbn = d.K / kTileK;
+  size_t bytes = (size_t)n_rb * kbn * kTileBytes;
+  dec_status st = dalloc(e, out, bytes, &e->weight_bytes);
+  if (st != DEC_OK) return st;
+  repack_kernel<<<n_rb * kbn, 256, 0, e->stream>>>(d, *out);
+  DEC_CUDA(cudaGetLastError());
+  return DEC_OK;
+}
+
+RepackDesc plain_desc(const dec_fp8_mat& m, int n, int K) {
+  RepackDesc d{};
+  d.w[0] = static_cast<const uint8_t*>(m.w);
+  d.s[0] = m.scale;
+  d.n[0] = n;
+  d.halves[0] = (n + 63) / 64;
+  d.nsrc = 1;
+  d.K = K;
+  return d;
+}
+
+RepackDesc gu_desc(const dec_fp8_mat& g, const dec_fp8_mat& u, int inter, int K) {
+  RepackDesc d{};
+  d.w[0] = static_cast<const uint8_t*>(g.w);
+  d.s[0] = g.scale;
+  d.n[0] = inter;
+  d.w[1] = static_cast<const uint8_t*>(u.w);
+  d.s[1] = u.scale;
+  d.n[1] = inter;
+  d.nsrc = 2;
+  d.interleave = 1;
+  d.K = K;
+  return d;
+}
+
+dec_status copy_bf16(dec_engine* e, const void* src, size_t n, uint16_t** out) {
+  dec_status st = dalloc(e, out, n * 2, &e->weight_bytes);
+  if (st != DEC_OK) return st;
+  if (!src) return fail(e, DEC_ERR_ARG, "missing bf16 tensor");
+  DEC_CUDA(cudaMemcpyAsync(*out, src, n * 2, cudaMemcpyDeviceToDevice, e->stream));
+  return DEC_OK;
+}
+
+int range_lo_h(int T, int c, int G) { return (int)((long long)T * c / G); }
+
+dec_status check_device_status(dec_engine* e) {
+  int code = 0;
+  DEC_CUDA(cudaMemcpy(&code, e->base.err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (code == 0) return DEC_OK;
+  e->poisoned = true;
+  char buf[160];
+  const int kind = code & 0xFF, where = code >> 8;
+  if (kind == kDevTimeout) {
+    snprintf(buf, sizeof buf, "device wait timed out (site %d); engine poisoned", where);
+    return fail(e, DEC_ERR_TIMEOUT, buf);
+  }
+  snprintf(buf, sizeof buf, "device check failed (code %d, site %d); engine poisoned", kind, where);
+  return fail(e, DEC_ERR_DEVICE, buf);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dec_status_string(dec_status s) {
+  switch (s) {
+    case DEC_OK: return "ok";
+    case DEC_ERR_ARG: return "bad argument";
+    case DEC_ERR_CUDA: return "CUDA error";
+    case DEC_ERR_OOM: return "out of device memory";
+    case DEC_ERR_TIMEOUT: return "device wait timed out";
+    case DEC_ERR_UNSUPPORTED: return "unsupported shape";
+    case DEC_ERR_POISONED: return "engine poisoned by an earlier device error";
+    case DEC_ERR_DEVICE: return "device-side check failed";
+    case DEC_ERR_CAPACITY: return "sequence would exceed max_ctx";
+  }
+  return "unknown status";
+}
+
+dec_status dec_validate_cfg(const dec_model_cfg* c) {
+  if (!c) return DEC_ERR_ARG;
+  if (c->n_layers < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
+      c->max_ctx < 1 || c->max_batch < 1 || c->vocab < 0 || c->n_experts < 0 || c->dense_ffn < 0 ||
+      c->n_shared < 0 || !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
+    return DEC_ERR_ARG;
+  if (c->n_heads % c->n_kv_heads != 0) return DEC_ERR_ARG;
+  if ((c->n_experts > 0) == (c->dense_ffn > 0)) return DEC_ERR_ARG;  // exactly one FFN kind
+  if (c->n_experts > 0 && (c->top_k < 1 || c->top_k > c->n_experts || c->moe_inter < 1)) return DEC_ERR_ARG;
+  if (c->head_dim % 2 != 0) return DEC_ERR_ARG;
+  // implemented subset
+  const int group = c->n_heads / c->n_kv_heads;
+  if (!((c->head_dim == 64 && group == 2) || (c->head_dim == 128 && group == 4))) return DEC_ERR_UNSUPPORTED;
+  if (c->hidden % 128 != 0 || (c->n_heads * c->head_dim) % 128 != 0) return DEC_ERR_UNSUPPORTED;
+  if (c->n_experts > 0) {
+    if (c->n_experts > kMaxExperts || c->top_k > 16 || c->moe_inter % 128 != 0 || c->n_shared > 1)
+      return DEC_ERR_UNSUPPORTED;
+  } else if (c->dense_ffn % 128 != 0) {
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c->max_batch > kMaxBatch) return DEC_ERR_UNSUPPORTED;
+  return DEC_OK;
+}
+
+dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream, dec_engine** out) {
+  if (!out) return DEC_ERR_ARG;
+  *out = nullptr;
+  dec_status vs = dec_validate_cfg(cfg);
+  if (vs != DEC_OK) return vs;
+  if (!W || !W->layers) return DEC_ERR_ARG;
+  if (cfg->vocab > 0 && (!W->embed || !W->final_norm || !W->lm_head.w)) return DEC_ERR_ARG;
+
+  dec_engine* e = new dec_engine();
+  e->cfg = *cfg;
+  const dec_model_cfg& c = *cfg;
+  dec_status st = DEC_OK;
+  auto bail = [&](dec_status s) {
+    dec_destroy(e);
+    return s;
+  };
+
+  cudaError_t ce = cudaGetDevice(&e->device);
+  if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaGetDevice"));
+  cudaDeviceProp prop;
+  ce = cudaGetDeviceProperties(&prop, e->device);
+  if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaGetDeviceProperties"));
+  e->sms = prop.multiProcessorCount;
+  if (!prop.cooperativeLaunch) return bail(DEC_ERR_UNSUPPORTED);
+  ce = cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking);
+  if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaStreamCreate"));
+  cudaStream_t user = stream ? static_cast<cudaStream_t>(stream) : e->stream;
+  // weights are read on the engine's stream: order after the caller's pending work
+  {
+    cudaEvent_t ev;
+    cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    cudaEventRecord(ev, user);
+    cudaStreamWaitEvent(e->stream, ev, 0);
+    cudaEventDestroy(ev);
+  }
+
+  KParams& p = e->base;
+  const bool dense = c.dense_ffn > 0;
+  e->hd = c.head_dim;
+  e->group = c.n_heads / c.n_kv_heads;
+  p.L = c.n_layers;
+  p.d = c.hidden;
+  p.hq = c.n_heads;
+  p.hkv = c.n_kv_heads;
+  p.hd = c.head_dim;
+  p.E = dense ? 0 : c.n_experts;
+  p.topk = dense ? 0 : c.top_k;
+  p.inter = dense ? c.dense_ffn : c.moe_inter;
+  p.nsh = dense ? 1 : c.n_shared;
+  p.dense = dense ? 1 : 0;
+  p.V = c.vocab;
+  p.max_ctx = c.max_ctx;
+  p.MB = c.max_batch;
+  p.eps = c.rms_eps;
+  p.kb_d = c.hidden / kTileK;
+  p.kb_o = c.n_heads * c.head_dim / kTileK;
+  p.kb_i = p.inter / kTileK;
+  p.n_rb_qkv = ((c.n_heads + 2 * c.n_kv_heads) * c.head_dim + kTileRows - 1) / kTileRows;
+  p.n_rb_d = c.hidden / kTileRows;
+  p.n_rb_gu = p.inter / 64;
+  p.n_rb_router = dense ? 0 : (c.n_experts + kTileRows - 1) / kTileRows;
+  p.n_rb_lm = (c.vocab + kTileRows - 1) / kTileRows;
+  p.e_gu_stride = (long long)p.n_rb_gu * p.kb_d * kTileBytes;
+  p.e_d_stride = (long long)p.n_rb_d * p.kb_i * kTileBytes;
+  p.umax = dense ? 0 : std::min(c.n_experts, c.max_batch * c.top_k);
+  e->grid = e->sms;
+  const int G = e->grid;
+
+  // ---- weights
+  std::vector<LayerDev> layers(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dec_layer_weights& Lw = W->layers[l];
+    LayerDev& Ld = layers[l];
+    RepackDesc q{};
+    q.w[0] = static_cast<const uint8_t*>(Lw.wq.w);
+    q.s[0] = Lw.wq.scale;
+    q.n[0] = c.n_heads * c.head_dim;
+    q.halves[0] = q.n[0] / 64;
+    q.w[1] = static_cast<const uint8_t*>(Lw.wk.w);
+    q.s[1] = Lw.wk.scale;
+    q.n[1] = c.n_kv_heads * c.head_dim;
+    q.halves[1] = q.n[1] / 64;
+    q.w[2] = static_cast<const uint8_t*>(Lw.wv.w);
+    q.s[2] = Lw.wv.scale;
+    q.n[2] = c.n_kv_heads * c.head_dim;
+    q.halves[2] = q.n[2] / 64;
+    q.nsrc = 3;
+    q.K = c.hidden;
+    if (!q.w[0] || !q.w[1] || !q.w[2] || !Lw.wo.w || !Lw.attn_norm || !Lw.ffn_norm)
+      return bail(fail(e, DEC_ERR_ARG, "missing attention weights"));
+    uint8_t* t = nullptr;
+    if ((st = repack(e, q, p.n_rb_qkv, &t)) != DEC_OK) return bail(st);
+    Ld.qkv = t;
+    if ((st = repack(e, plain_desc(Lw.wo, c.hidden, c.n_heads * c.head_dim), p.n_rb_d, &t)) != DEC_OK) return bail(st);
+    Ld.o = t;
+    uint16_t* nb = nullptr;
+    if ((st = copy_bf16(e, Lw.attn_norm, c.hidden, &nb)) != DEC_OK) return bail(st);
+    Ld.attn_norm = nb;
+    if ((st = copy_bf16(e, Lw.ffn_norm, c.hidden, &nb)) != DEC_OK) return bail(st);
+    Ld.ffn_norm = nb;
+    if (dense) {
+      if (!Lw.ffn_gate.w || !Lw.ffn_up.w || !Lw.ffn_down.w) return bail(fail(e, DEC_ERR_ARG, "missing FFN weights"));
+      if ((st = repack(e, gu_desc(Lw.ffn_gate, Lw.ffn_up, p.inter, c.hidden), p.n_rb_gu, &t)) != DEC_OK) return bail(st);
+      Ld.sh_gu = t;
+      if ((st = repack(e, plain_desc(Lw.ffn_down, c.hidden, p.inter), p.n_rb_d, &t)) != DEC_OK) return bail(st);
+      Ld.sh_d = t;
+    } else {
+      if (!Lw.router.w || !Lw.expert_gate || !Lw.expert_up || !Lw.expert_down ||
+          (c.n_shared > 0 && (!Lw.shared_gate || !Lw.shared_up || !Lw.shared_down)))
+        return bail(fail(e, DEC_ERR_ARG, "missing MoE weights"));
+      if ((st = repack(e, plain_desc(Lw.router, c.n_experts, c.hidden), p.n_rb_router, &t)) != DEC_OK) return bail(st);
+      Ld.router = t;
+      if (c.n_shared > 0) {
+        if ((st = repack(e, gu_desc(Lw.shared_gate[0], Lw.shared_up[0], p.inter, c.hidden), p.n_rb_gu, &t)) != DEC_OK)
+          return bail(st);
+        Ld.sh_gu = t;
+        if ((st = repack(e, plain_desc(Lw.shared_down[0], c.hidden, p.inter), p.n_rb_d, &t)) != DEC_OK) return bail(st);
+        Ld.sh_d = t;
+      }
+      uint8_t* egu = nullptr;
+      uint8_t* ed = nullptr;
+      if ((st = dalloc(e, &egu, (size_t)c.n_experts * p.e_gu_stride, &e->weight_bytes)) != DEC_OK) return bail(st);
+      if ((st = dalloc(e, &ed, (size_t)c.n_experts * p.e_d_stride, &e->weight_bytes)) != DEC_OK) return bail(st);
+      for (int x = 0; x < c.n_experts; ++x) {
+        RepackDesc gd = gu_desc(Lw.expert_gate[x], Lw.expert_up[x], p.inter, c.hidden);
+        RepackDesc dd = plain_desc(Lw.expert_down[x], c.hidden, p.inter);
+        for (int s = 0; s < 2; ++s)
+          if (!gd.w[s] || !aligned16(gd.w[s]) || !gd.s[s]) return bail(fail(e, DEC_ERR_ARG, "bad expert weight"));
+        if (!dd.w[0] || !aligned16(dd.w[0]) || !dd.s[0]) return bail(fail(e, DEC_ERR_ARG, "bad expert weight"));
+        repack_kernel<<<p.n_rb_gu * p.kb_d, 256, 0, e->stream>>>(gd, egu + (size_t)x * p.e_gu_stride);
+        repack_kernel<<<p.n_rb_d * p.kb_i, 256, 0, e->stream>>>(dd, ed + (size_t)x * p.e_d_stride);
+      }
+      ce = cudaGetLastError();
+      if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "repack"));
+      Ld.e_gu = egu;
+      Ld.e_d = ed;
+    }
+  }
+  if ((st = dalloc(e, &e->d_layers, sizeof(LayerDev) * c.n_layers, nullptr)) != DEC_OK) return bail(st);
+  ce = cudaMemcpyAsync(e->d_layers, layers.data(), sizeof(LayerDev) * c.n_layers, cudaMemcpyHostToDevice, e->stream);
+  if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "copy layers"));
+  p.layers = e->d_layers;
+  if (c.vocab > 0) {
+    uint16_t* emb = nullptr;
+    if ((st = copy_bf16(e, W->embed, (size_t)c.vocab * c.hidden, &emb)) != DEC_OK) return bail(st);
+    p.embed = emb;
+    uint16_t* fn = nullptr;
+    if ((st = copy_bf16(e, W->final_norm, c.hidden, &fn)) != DEC_OK) return bail(st);
+    p.final_norm = fn;
+    uint8_t* t = nullptr;
+    if ((st = repack(e, plain_desc(W->lm_head, c.vocab, c.hidden), p.n_rb_lm, &t)) != DEC_OK) return bail(st);
+    p.lm = t;
+  }
+
+  // ---- RoPE table: angles pos * theta^(-2i/hd) in double, stored as fp32 (cos, sin)
+  {
+    const int half = c.head_dim / 2;
+    std::vector<float2> tab((size_t)c.max_ctx * half);
+    for (int pos = 0; pos < c.max_ctx; ++pos)
+      for (int i = 0; i < half; ++i) {
+        double inv = std::pow((double)c.rope_theta, -2.0 * i / (double)c.head_dim);
+        double a = (double)pos * inv;
+        tab[(size_t)pos * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    float2* d = nullptr;
+    if ((st = dalloc(e, &d, tab.size() * sizeof(float2), &e->ws_bytes)) != DEC_OK) return bail(st);
+    ce = cudaMemcpy(d, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "copy rope"));
+    p.rope = d;
+  }
+
+  // ---- KV cache
+  {
+    size_t n = (size_t)c.n_layers * c.max_batch * c.n_kv_heads * c.max_ctx * c.head_dim;
+    if ((st = dalloc(e, &p.kc, n * 2, &e->kv_bytes)) != DEC_OK) return bail(st);
+    if ((st = dalloc(e, &p.vc, n * 2, &e->kv_bytes)) != DEC_OK) return bail(st);
+    cudaMemsetAsync(p.kc, 0, n * 2, e->stream);
+    cudaMemsetAsync(p.vc, 0, n * 2, e->stream);
+  }
+
+  // ---- workspace
+  {
+    const int MB = c.max_batch, d = c.hidden, qd = c.n_heads * c.head_dim;
+    const size_t rows = kTileRows;
+    auto zalloc = [&](auto** ptr, size_t bytes) -> dec_status {
+      dec_status s2 = dalloc(e, ptr, bytes, &e->ws_bytes);
+      if (s2 == DEC_OK && cudaMemsetAsync(*ptr, 0, bytes ? bytes : 16, e->stream) != cudaSuccess) s2 = DEC_ERR_CUDA;
+      return s2;
+    };
+#define Z(ptr, bytes) \
+  if ((st = zalloc(&(ptr), (bytes))) != DEC_OK) return bail(st);
+    Z(p.lengths, sizeof(int32_t) * MB);
+    Z(p.xbuf, 2ull * MB * d * 2);
+    Z(p.xmid, (size_t)MB * d * 2);
+    Z(p.qbuf, (size_t)MB * qd * 2);
+    Z(p.obuf, (size_t)MB * qd * 2);
+    Z(p.hsh, (size_t)MB * p.inter * 2);
+    Z(p.hrt, (size_t)std::max(1, p.umax) * MB * p.inter * 2);
+    const size_t fb = sizeof(float) * MB * rows;
+    Z(p.part_qkv, fb * p.n_rb_qkv * p.kb_d);
+    Z(p.part_o, fb * p.n_rb_d * p.kb_o);
+    Z(p.part_router, fb * std::max(1, p.n_rb_router) * p.kb_d);
+    Z(p.part_shgu, fb * p.n_rb_gu * p.kb_d);
+    Z(p.part_rtgu, fb * std::max(1, p.umax) * p.n_rb_gu * p.kb_d);
+    Z(p.part_d, fb * (size_t)(p.umax + p.nsh) * p.n_rb_d * p.kb_i);
+    Z(p.part_lm, fb * std::max(1, p.n_rb_lm) * p.kb_d);
+    Z(p.cnt_qkv, sizeof(int) * p.n_rb_qkv);
+    Z(p.cnt_o, sizeof(int) * p.n_rb_d);
+    Z(p.cnt_router, sizeof(int) * std::max(1, p.n_rb_router));
+    Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
+    Z(p.cnt_rtgu, sizeof(int) * std::max(1, p.umax) * p.n_rb_gu);
+    Z(p.cnt_d, sizeof(int) * p.n_rb_d);
+    Z(p.cnt_lm, sizeof(int) * std::max(1, p.n_rb_lm));
+    Z(p.cnt_lm_done, sizeof(int) * 32);
+    e->nch_max = std::max(1, G / c.n_kv_heads);
+    Z(p.attn_part, sizeof(float) * MB * c.n_kv_heads * e->nch_max * e->group * (c.head_dim + 2));
+    Z(p.attn_cnt, sizeof(int) * MB * c.n_kv_heads);
+    Z(p.rt_u, sizeof(int) * 32);
+    Z(p.rt_elist, sizeof(int) * kMaxExperts);
+    Z(p.rt_gate, sizeof(float) * MB * kMaxExperts);
+    Z(p.rt_idx, sizeof(int) * c.n_layers * MB * std::max(1, c.top_k));
+    Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
+    Z(p.rt_flag, sizeof(unsigned) * c.n_layers);
+    Z(p.amax, sizeof(unsigned long long) * MB);
+    Z(p.gbar, sizeof(unsigned) * 64);
+    Z(p.err, sizeof(int) * 32);
+    Z(p.logits_ws, sizeof(float) * MB * std::max(1, c.vocab));
+    Z(p.trace, sizeof(unsigned long long) * kTraceSlots);
+    Z(e->d_hist, sizeof(int32_t) * (size_t)(c.max_ctx + 1) * MB);
+#undef Z
+  }
+
+  // ---- activation buffer width: d, n_heads*head_dim, or the experts a CTA's down range spans
+  {
+    int xmax = std::max(c.hidden, c.n_heads * c.head_dim);
+    const int tpe = p.n_rb_d * p.kb_i;
+    int span = 1;
+    for (int U = 0; U <= p.umax; ++U) {
+      const int T = (U + p.nsh) * tpe;
+      for (int cta = 0; cta < G; ++cta) {
+        int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
+        if (t1 > t0) span = std::max(span, (t1 - 1) / tpe - t0 / tpe + 1);
+      }
+    }
+    xmax = std::max(xmax, span * p.inter);
+    p.xmax = xmax;
+  }
+
+  // ---- kernels: one per batch bucket; ring depth from the shared memory left over
+  int max_optin = 0;
+  cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, e->device);
+  for (int i = 0; i < 4; ++i) {
+    const int bm = kBmChoices[i];
+    if (bm > std::max(1, c.max_batch) && i > 0 && kBmChoices[i - 1] >= c.max_batch) continue;
+    KernelFn k = kernel_for(bm, e->hd, e->group);
+    if (!k) return bail(DEC_ERR_UNSUPPORTED);
+    int ring = 16;
+    while (ring >= 4 && smem_layout(ring, bm, p.xmax, e->hd, e->group).total > max_optin) --ring;
+    if (ring < 4) return bail(fail(e, DEC_ERR_UNSUPPORTED, "shared memory too small for the ring"));
+    const int smem = smem_layout(ring, bm, p.xmax, e->hd, e->group).total;
+    ce = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaFuncSetAttribute"));
+    int nb = 0;
+    ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, (const void*)k, kThreads, smem);
+    if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "occupancy"));
+    if (nb < 1) return bail(fail(e, DEC_ERR_UNSUPPORTED, "persistent CTA does not fit on an SM"));
+    e->kern[i] = k;
+    e->smem[i] = smem;
+    e->ring[i] = ring;
+  }
+  {
+    const char* tm = getenv("DEC_TIMEOUT_MS");
+    double ms = tm ? atof(tm) : 1000.0;
+    if (!(ms > 0)) ms = 1000.0;
+    p.timeout_ns = (unsigned long long)(ms * 1e6);
+  }
+  e->lengths.assign(c.max_batch, 0);
+  ce = cudaStreamSynchronize(e->stream);
+  if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "init synchronize"));
+  *out = e;
+  return DEC_OK;
+}
+
+dec_status dec_step_ex(dec_engine* e, const dec_step_args* a) {
+  if (!e || !a) return DEC_ERR_ARG;
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  const dec_model_cfg& c = e->cfg;
+  if (a->batch == 0) return DEC_OK;
+  if (a->batch < 0 || a->seq0 < 0 || a->seq0 + a->batch > c.max_batch) return fail(e, DEC_ERR_ARG, "batch/seq0 out of range");
+  const bool use_tokens = a->tokens != nullptr;
+  if (!use_tokens && !a->hidden_in) return fail(e, DEC_ERR_ARG, "need tokens or hidden_in");
+  if (use_tokens && c.vocab == 0) return fail(e, DEC_ERR_ARG, "tokens given to a headless stack");
+  if ((a->logits || a->next_tokens) && c.vocab == 0) return fail(e, DEC_ERR_ARG, "no LM head");
+  if (a->hidden_in && !aligned16(a->hidden_in)) return fail(e, DEC_ERR_ARG, "hidden_in must be 16-byte aligned");
+  for (int b = 0; b < a->batch; ++b)
+    if (e->lengths[a->seq0 + b] + 1 > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "sequence full");
+  int bi = 0;
+  while (kBmChoices[bi] < a->batch) ++bi;
+  KParams p = e->base;
+  p.B = a->batch;
+  p.seq0 = a->seq0;
+  p.tokens = a->tokens;
+  p.hidden_in = static_cast<const uint16_t*>(a->hidden_in);
+  p.logits = a->logits;
+  p.next_tokens = a->next_tokens;
+  p.hidden_out = static_cast<uint16_t*>(a->hidden_out);
+  p.epoch = ++e->epoch;
+  p.ring = e->ring[bi];
+  p.nch = std::max(1, std::min(e->nch_max, e->grid / (a->batch * c.n_kv_heads)));
+  cudaStream_t s = a->stream ? static_cast<cudaStream_t>(a->stream) : e->stream;
+  void* args[] = {&p};
+  cudaError_t ce = cudaLaunchCooperativeKernel((const void*)e->kern[bi], dim3(e->grid), dim3(kThreads), args,
+                                               (size_t)e->smem[bi], s);
+  if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaLaunchCooperativeKernel");
+  for (int b = 0; b < a->batch; ++b) e->lengths[a->seq0 + b] += 1;
+  e->launches += 1;
+  return DEC_OK;
+}
+
+dec_status dec_step(dec_engine* e, const int32_t* token_ids, int32_t batch, float* logits, int32_t* next_tokens,
+                    void* stream) {
+  dec_step_args a{};
+  a.tokens = token_ids;
+  a.batch = batch;
+  a.logits = logits;
+  a.next_tokens = next_tokens;
+  a.stream = stream;
+  return dec_step_ex(e, &a);
+}
+
+dec_status dec_sync(dec_engine* e) {
+  if (!e) return DEC_ERR_ARG;
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
+  DEC_CUDA(cudaDeviceSynchronize());
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, e->err.empty() ? "engine poisoned" : e->err);
+  return check_device_status(e);
+}
+
+dec_status dec_prefill_kv(dec_engine* e, const dec_ctx* x) {
+  if (!e || !x) return DEC_ERR_ARG;
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  const dec_model_cfg& c = e->cfg;
+  if (x->n_seq < 1 || x->seq < 0 || x->seq + x->n_seq > c.max_batch || x->n_tokens < 0)
+    return fail(e, DEC_ERR_ARG, "bad slot range");
+  if (x->n_tokens == 0) return DEC_OK;
+  DEC_CUDA(cudaDeviceSynchronize());  // earlier steps may be queued on a caller stream
+  if (x->k_import) {
+    if (!x->v_import) return fail(e, DEC_ERR_ARG, "v_import missing");
+    if (x->n_tokens > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "import longer than max_ctx");
+    const size_t row = (size_t)c.head_dim * 2;
+    for (int s = x->seq; s < x->seq + x->n_seq; ++s)
+      for (int l = 0; l < c.n_layers; ++l)
+        for (int g = 0; g < c.n_kv_heads; ++g) {
+          size_t src = (((size_t)l * c.n_kv_heads + g) * x->n_tokens) * row;
+          size_t dst = ((((size_t)l * c.max_batch + s) * c.n_kv_heads + g) * c.max_ctx) * row;
+          DEC_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(e->base.kc) + dst,
+                                   static_cast<const uint8_t*>(x->k_import) + src, x->n_tokens * row,
+                                   cudaMemcpyDeviceToDevice, e->stream));
+          DEC_CUDA(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(e->base.vc) + dst,
+                                   static_cast<const uint8_t*>(x->v_import) + src, x->n_tokens * row,
+                                   cudaMemcpyDeviceToDevice, e->stream));
+        }
+    for (int s = x->seq; s < x->seq + x->n_seq; ++s) {
+      e->lengths[s] = x->n_tokens;
+      DEC_CUDA(cudaMemcpyAsync(e->base.lengths + s, &e->lengths[s], sizeof(int32_t), cudaMemcpyHostToDevice, e->stream));
+    }
+    DEC_CUDA(cudaStreamSynchronize(e->stream));
+    return DEC_OK;
+  }
+  if (!x->token_ids) return fail(e, DEC_ERR_ARG, "token_ids missing");
+  if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "token prefill needs an embedding");
+  for (int s = x->seq; s < x->seq + x->n_seq; ++s)
+    if (e->lengths[s] + x->n_tokens > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "prefill exceeds max_ctx");
+  int32_t* tt = nullptr;
+  DEC_CUDA(cudaMalloc(&tt, sizeof(int32_t) * (size_t)x->n_seq * x->n_tokens));
+  const int n = x->n_seq * x->n_tokens;
+  transpose_tokens_kernel<<<(n + 255) / 256, 256, 0, e->stream>>>(x->token_ids, x->n_seq, x->n_tokens, tt);
+  dec_status st = DEC_OK;
+  for (int t = 0; t < x->n_tokens && st == DEC_OK; ++t) {
+    dec_step_args a{};
+    a.tokens = tt + (size_t)t * x->n_seq;
+    a.batch = x->n_seq;
+    a.seq0 = x->seq;
+    st = dec_step_ex(e, &a);
+  }
+  cudaError_t ce = cudaStreamSynchronize(e->stream);
+  cudaFree(tt);
+  if (st != DEC_OK) return st;
+  if (ce != cudaSuccess) return cuda_fail(e, ce, "prefill synchronize");
+  return check_device_status(e);
+}
+
+dec_status dec_generate(dec_engine* e, const int32_t* first, int32_t batch, int32_t n_steps, int32_t* out,
+                        void* stream) {
+  if (!e || !first || !out || batch < 1 || n_steps < 0) return DEC_ERR_ARG;
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  const dec_model_cfg& c = e->cfg;
+  if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "generate needs an LM head");
+  if (batch > c.max_batch || n_steps > c.max_ctx) return fail(e, DEC_ERR_ARG, "batch or n_steps too large");
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
+  const int MB = c.max_batch;
+  DEC_CUDA(cudaMemcpyAsync(e->d_hist, first, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s));
+  for (int i = 0; i < n_steps; ++i) {
+    dec_status st = dec_step(e, e->d_hist + (size_t)i * MB, batch, nullptr, e->d_hist + (size_t)(i + 1) * MB, s);
+    if (st != DEC_OK) return st;
+  }
+  if (n_steps > 0)
+    DEC_CUDA(cudaMemcpy2DAsync(out, sizeof(int32_t) * batch, e->d_hist + MB, sizeof(int32_t) * MB,
+                               sizeof(int32_t) * batch, n_steps, cudaMemcpyDeviceToHost, s));
+  DEC_CUDA(cudaStreamSynchronize(s));
+  return check_device_status(e);
+}
+
+dec_status dec_set_length(dec_engine* e, int32_t seq, int32_t length) {
+  if (!e) return DEC_ERR_ARG;
+  if (seq < 0 || seq >= e->cfg.max_batch || length < 0 || length > e->cfg.max_ctx) return fail(e, DEC_ERR_ARG, "bad length");
+  DEC_CUDA(cudaDeviceSynchronize());  // steps may be queued on any stream
+  e->lengths[seq] = length;
+  DEC_CUDA(cudaMemcpyAsync(e->base.lengths + seq, &e->lengths[seq], sizeof(int32_t), cudaMemcpyHostToDevice, e->stream));
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
+  return DEC_OK;
+}
+
+dec_status dec_get_length(dec_engine* e, int32_t seq, int32_t* length) {
+  if (!e || !length || seq < 0 || seq >= e->cfg.max_batch) return DEC_ERR_ARG;
+  *length = e->lengths[seq];
+  return DEC_OK;
+}
+
+dec_status dec_export_kv(dec_engine* e, int32_t seq, int32_t layer, int32_t pos0, int32_t n, void* k_out, void* v_out) {
+  if (!e || !k_out || !v_out) return DEC_ERR_ARG;
+  const dec_model_cfg& c = e->cfg;
+  if (seq < 0 || seq >= c.max_batch || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > c.max_ctx)
+    return fail(e, DEC_ERR_ARG, "export range");
+  DEC_CUDA(cudaDeviceSynchronize());
+  const size_t row = (size_t)c.head_dim * 2;
+  for (int g = 0; g < c.n_kv_heads; ++g) {
+    size_t src = ((((size_t)layer * c.max_batch + seq) * c.n_kv_heads + g) * c.max_ctx + pos0) * row;
+    DEC_CUDA(cudaMemcpy(static_cast<uint8_t*>(k_out) + (size_t)g * n * row,
+                        reinterpret_cast<const uint8_t*>(e->base.kc) + src, n * row, cudaMemcpyDeviceToDevice));
+    DEC_CUDA(cudaMemcpy(static_cast<uint8_t*>(v_out) + (size_t)g * n * row,
+                        reinterpret_cast<const uint8_t*>(e->base.vc) + src, n * row, cudaMemcpyDeviceToDevice));
+  }
+  return DEC_OK;
+}
+
+dec_status dec_get_info(dec_engine* e, dec_info* o) {
+  if (!e || !o) return DEC_ERR_ARG;
+  o->grid = e->grid;
+  o->threads = kThreads;
+  o->smem_bytes = e->smem[0];
+  o->ring_slots = e->ring[0];
+  o->stages_per_layer = 5;
+  o->weight_bytes = e->weight_bytes;
+  o->kv_bytes = e->kv_bytes;
+  o->workspace_bytes = e->ws_bytes;
+  o->launches = e->launches;
+  return DEC_OK;
+}
+
+dec_status dec_get_routing(dec_engine* e, int32_t layer, int32_t* idx, float* gates) {
+  if (!e || !idx || !gates) return DEC_ERR_ARG;
+  const dec_model_cfg& c = e->cfg;
+  if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
+  DEC_CUDA(cudaDeviceSynchronize());
+  const size_t n = (size_t)c.max_batch * c.top_k, off = (size_t)layer * n;
+  DEC_CUDA(cudaMemcpy(idx, e->base.rt_idx + off, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
+  DEC_CUDA(cudaMemcpy(gates, e->base.rt_topk_gate + off, sizeof(float) * n, cudaMemcpyDeviceToHost));
+  return DEC_OK;
+}
+
+dec_status dec_get_trace(dec_engine* e, uint64_t* host_buf, int32_t n, int32_t* n_written) {
+  if (!e || !host_buf || n < 0) return DEC_ERR_ARG;
+  DEC_CUDA(cudaDeviceSynchronize());
+  const int m = std::min(n, kTraceSlots);
+  DEC_CUDA(cudaMemcpy(host_buf, e->base.trace, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost));
+  if (n_written) *n_written = m;
+  return DEC_OK;
+}
+
+const char* dec_last_error(const dec_engine* e) { return e ? e->err.c_str() : "no engine"; }
+
+void dec_destroy(dec_engine* e) {
+  if (!e) return;
+  if (e->stream) cudaStreamSynchronize(e->stream);
+  for (void* p : e->allocs) cudaFree(p);
+  if (e->stream) cudaStreamDestroy(e->stream);
+  delete e;
+}
+
+}  // extern "C"

@@ -1,0 +1,194 @@
+// Device primitives of the persistent decode kernel: mbarrier rings fed by bulk (TMA) copies,
+// L2 prefetch, acquire/release flags, a grid barrier, and FP8/bf16 conversions. Every wait is
+// bounded by %globaltimer: on expiry it records an error code in the device status word and
+// returns false, and every caller unwinds without touching the GPU further.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <cstdint>
+
+#include "dec_common.h"
+
+namespace dec {
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------------------------
+// status word
+
+__device__ __forceinline__ bool aborted(const KParams& p) {
+  return *reinterpret_cast<volatile int*>(p.err) != 0;
+}
+
+__device__ __noinline__ void raise_err(const KParams& p, int code, int where) {
+  atomicCAS(p.err, 0, code | (where << 8));
+}
+
+// ---------------------------------------------------------------------------------------------
+// mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const KParams& p, int where) {
+  if (mbar_try_wait(b, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  while (true) {
+    if (mbar_try_wait(b, parity)) return true;
+    if (aborted(p)) return false;
+    if (gtimer() - t0 > p.timeout_ns) {
+      raise_err(p, kDevTimeout, where);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// bulk copies (TMA, non-tensor): global -> this CTA's shared memory, completing on an mbarrier.
+// Addresses 16-byte aligned, size a multiple of 16.
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// cross-CTA memory
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int atom_add_acqrel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// L2-coherent loads for data written by other CTAs during this launch (never served from a
+// possibly stale L1 line).
+__device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ uint4 ldcg4(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ uint16_t ldcg_u16(const uint16_t* p) { return __ldcg(p); }
+
+// Consumer warps only (named barrier 1, 256 threads).
+__device__ __forceinline__ void cons_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Grid barrier among the consumer warps of all CTAs (sense by generation count). Called by all
+// consumer threads; returns false if the kernel is aborting.
+__device__ __noinline__ bool grid_sync(const KParams& p, int* s_flag, int where) {
+  cons_sync();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    __threadfence();
+    unsigned* cnt = p.gbar;
+    unsigned* gen = p.gbar + 32;
+    const unsigned g0 = ld_acquire(gen);
+    const unsigned old = atomicAdd(cnt, 1u);
+    if (old == gridDim.x - 1) {
+      atomicExch(cnt, 0u);
+      __threadfence();
+      st_release(gen, g0 + 1);
+    } else {
+      const unsigned long long t0 = gtimer();
+      while (ld_acquire(gen) == g0) {
+        if (aborted(p)) { ok = 0; break; }
+        if (gtimer() - t0 > p.timeout_ns) {
+          raise_err(p, kDevTimeout, where);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    *s_flag = ok && !aborted(p);
+  }
+  cons_sync();
+  return *reinterpret_cast<volatile int*>(s_flag) != 0;
+}
+
+// Wait until a published flag reaches `want` (acquire); one thread polls.
+__device__ __forceinline__ bool wait_flag(const KParams& p, const unsigned* f, unsigned want, int where) {
+  if (ld_acquire(f) == want) return true;
+  const unsigned long long t0 = gtimer();
+  while (ld_acquire(f) != want) {
+    if (aborted(p)) return false;
+    if (gtimer() - t0 > p.timeout_ns) {
+      raise_err(p, kDevTimeout, where);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------------------------
+// conversions (CUDA's own FP8 conversion instruction; bf16 -> fp32 is a shift)
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t u) { return __uint_as_float(static_cast<uint32_t>(u) << 16); }
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Order-preserving map float -> uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace dec

@@ -1,0 +1,79 @@
+"""Shared helpers of the GPU parity tests: run the engine and the oracle on the same seeded
+inputs and compare with the tolerances of the decode step:
+  * top-k expert indices identical, except where the oracle's k-th/(k+1)-th score gap < 1e-5;
+  * final hidden state relative L2 error <= 1e-2;
+  * logits max abs error <= 5e-2;
+  * greedy tokens agree (teacher-forced) on >= 99% of steps, near-ties (top-2 gap < 1e-3) counted.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+HIDDEN_REL_L2 = 1e-2
+LOGIT_MAX_ABS = 5e-2
+TOPK_GAP = 1e-5
+NEAR_TIE = 1e-3
+# Gates are not given a tolerance of their own: they follow the router logits, whose error is that
+# of a K=hidden GEMV over a bf16 input that may differ from the oracle's by bf16 rounding flips
+# (~1e-3 absolute in the logits); d gate / d logit <= 1/4, so 2e-3 bounds the gate error.
+GATE_ABS = 2e-3
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    b = np.asarray(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def t_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def rel_l2(a, b) -> float:
+    a, b = np.asarray(a, np.float64).ravel(), np.asarray(b, np.float64).ravel()
+    assert a.shape == b.shape, (a.shape, b.shape)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def topk_ok(gpu_idx, orc_idx, orc_scores, k: int) -> bool:
+    """Same selected set, unless the oracle's k-th and (k+1)-th scores are within TOPK_GAP."""
+    if set(int(x) for x in gpu_idx[:k]) == set(int(x) for x in orc_idx[:k]):
+        return True
+    s = np.sort(np.asarray(orc_scores, np.float64))[::-1]
+    return len(s) > k and (s[k - 1] - s[k]) < TOPK_GAP
+
+
+def near_tie(logits) -> bool:
+    s = np.sort(np.asarray(logits, np.float64))[::-1]
+    return len(s) > 1 and (s[0] - s[1]) < NEAR_TIE
+
+
+class StepCheck:
+    """Accumulates per-step comparisons of logits / argmax / hidden state."""
+
+    def __init__(self):
+        self.steps = 0
+        self.agree = 0
+        self.near_ties = 0
+        self.max_logit_err = 0.0
+        self.max_hidden_rel = 0.0
+
+    def add(self, gpu_logits=None, orc_logits=None, gpu_tok=None, orc_tok=None, gpu_hidden=None, orc_hidden=None):
+        self.steps += 1
+        if gpu_logits is not None:
+            err = float(np.max(np.abs(np.asarray(gpu_logits, np.float64) - orc_logits)))
+            self.max_logit_err = max(self.max_logit_err, err)
+        if gpu_tok is not None:
+            if int(gpu_tok) == int(orc_tok):
+                self.agree += 1
+            elif orc_logits is not None and near_tie(orc_logits):
+                self.near_ties += 1
+        if gpu_hidden is not None:
+            self.max_hidden_rel = max(self.max_hidden_rel, rel_l2(bf16_to_f64(gpu_hidden), bf16_to_f64(orc_hidden)))
+
+    def assert_ok(self, check_tokens=True):
+        assert self.max_logit_err <= LOGIT_MAX_ABS, f"logits max abs err {self.max_logit_err}"
+        assert self.max_hidden_rel <= HIDDEN_REL_L2, f"hidden rel L2 {self.max_hidden_rel}"
+        if check_tokens and self.steps:
+            rate = (self.agree + self.near_ties) / self.steps
+            assert rate >= 0.99, f"greedy agreement {self.agree}/{self.steps} (+{self.near_ties} near ties)"

@@ -1,0 +1,264 @@
+"""GPU parity: the persistent decode kernel (through the C ABI) against the CPU oracle on the same
+seeded inputs. Sizes: the tiny dense decoder and a small MoE run whole workloads; the full-size
+MoE stack is checked on sampled decode steps the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from latency_moe_decode_gb300 import synth
+from tests.parity import GATE_ABS, StepCheck, bf16_to_f64, rel_l2, t_bits, topk_ok
+
+pytestmark = pytest.mark.gpu
+
+# A small MoE with the full-size head geometry (head_dim 128, 4 query heads per KV head) so that
+# batch and ragged-length cases run in seconds on the oracle.
+MOE_SMALL = synth.ModelCfg(n_layers=2, hidden=512, n_heads=8, n_kv_heads=2, head_dim=128, n_experts=16,
+                           top_k=4, moe_inter=256, n_shared=1, vocab=2048, max_ctx=512, max_batch=8,
+                           rms_eps=1e-6, rope_theta=1e6)
+TINY_MOE = synth.ModelCfg(n_layers=2, hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, n_experts=8, top_k=2,
+                          moe_inter=128, n_shared=1, vocab=512, max_ctx=128, max_batch=4)
+
+
+def _engine(m_gpu, **kw):
+    from latency_moe_decode_gb300.engine import Engine
+    return Engine(m_gpu, **kw)
+
+
+def _models(cfg, seed):
+    m_cpu = synth.gen_model(cfg, seed=seed, device="cpu")
+    return m_cpu, synth.model_to(m_cpu, "cuda")
+
+
+def _gpu_step(eng, tok=None, hidden=None, batch=1, seq0=0):
+    c = eng.cfg
+    logits = torch.empty(batch, max(1, c.vocab), device="cuda") if c.vocab else None
+    nxt = torch.empty(batch, dtype=torch.int32, device="cuda") if c.vocab else None
+    hout = torch.empty(batch, c.hidden, dtype=torch.bfloat16, device="cuda")
+    t = torch.tensor(tok, dtype=torch.int32, device="cuda").reshape(batch) if tok is not None else None
+    eng.step(tokens=t, hidden=hidden, batch=batch, seq0=seq0, logits=logits, next_tokens=nxt, hidden_out=hout)
+    eng.sync()
+    return (logits.cpu().numpy().astype(np.float64) if logits is not None else None,
+            nxt.cpu().numpy() if nxt is not None else None, t_bits(hout))
+
+
+# ------------------------------------------------------------------------------------------------
+# tiny dense decoder: KV prefilled from 128 random tokens (seed 0), then 16 greedy steps
+
+
+def test_tiny_dense_prefill_and_16_greedy_steps():
+    cfg = synth.TINY
+    m_cpu, m_gpu = _models(cfg, 0)
+    prompt = synth.gen_tokens(128, cfg.vocab, seed=0)
+    orc = oracle.Oracle(m_cpu)
+    kv = orc.new_kv(cfg.max_ctx)
+    first = orc.prefill(kv, prompt)
+    eng = _engine(m_gpu)
+    eng.prefill_tokens(prompt.cuda())
+    assert eng.get_length(0) == 128
+    # KV cache after prefill, every layer and position
+    for l in range(cfg.n_layers):
+        k, v = eng.export_kv(0, l, 0, 128)
+        ko = bf16_to_f64(kv["k"][l, :, :128])
+        vo = bf16_to_f64(kv["v"][l, :, :128])
+        assert rel_l2(bf16_to_f64(t_bits(k)), ko) < 1e-2
+        assert rel_l2(bf16_to_f64(t_bits(v)), vo) < 1e-2
+    chk = StepCheck()
+    tok = first["token"]
+    for i in range(16):
+        o = orc.decode_step(kv, 128 + i, token=tok)
+        g_logits, g_next, g_hidden = _gpu_step(eng, tok=[tok])
+        chk.add(g_logits[0], o["logits"], g_next[0], o["token"], g_hidden[0], o["hidden"])
+        tok = o["token"]
+    chk.assert_ok()
+    assert eng.get_length(0) == 144
+
+
+def test_tiny_moe_generate_matches_oracle_greedy():
+    cfg = TINY_MOE
+    m_cpu, m_gpu = _models(cfg, 1)
+    prompt = synth.gen_tokens(24, cfg.vocab, seed=1)
+    orc = oracle.Oracle(m_cpu)
+    kv = orc.new_kv(cfg.max_ctx)
+    first = orc.prefill(kv, prompt)
+    eng = _engine(m_gpu)
+    eng.prefill_tokens(prompt.cuda())
+    toks = [first["token"]]
+    for i in range(12):
+        toks.append(orc.decode_step(kv, 24 + i, token=toks[-1])["token"])
+    gen = eng.generate([first["token"]], 12)[:, 0]
+    agree = np.mean(gen == np.array(toks[1:]))
+    assert agree >= 0.99 or np.sum(gen != np.array(toks[1:])) <= 1
+
+
+# ------------------------------------------------------------------------------------------------
+# small MoE: batches, ragged lengths, slot offsets, routing
+
+
+@pytest.fixture(scope="module")
+def moe_small():
+    return _models(MOE_SMALL, 3)
+
+
+@pytest.mark.parametrize("batch", [1, 2, 3, 5, 8])
+def test_moe_small_batch_ragged(moe_small, batch):
+    m_cpu, m_gpu = moe_small
+    cfg = MOE_SMALL
+    orc = oracle.Oracle(m_cpu)
+    eng = _engine(m_gpu)
+    lens = [37 + 29 * b for b in range(batch)]  # ragged, crosses 32-position tiles
+    kvs = []
+    toks = synth.gen_tokens(batch, cfg.vocab, seed=5 + batch).tolist()
+    for b in range(batch):
+        k, v = synth.gen_kv(cfg, lens[b], seed=100 + b)
+        eng.prefill_import(k.cuda(), v.cuda(), seq=b)
+        kv = orc.new_kv(cfg.max_ctx)
+        orc.import_kv(kv, k, v, lens[b])
+        kvs.append(kv)
+    g_logits, g_next, g_hidden = _gpu_step(eng, tok=toks, batch=batch)
+    chk = StepCheck()
+    for b in range(batch):
+        o = orc.decode_step(kvs[b], lens[b], token=toks[b], want_trace=True)
+        chk.add(g_logits[b], o["logits"], g_next[b], o["token"], g_hidden[b], o["hidden"])
+        for l in range(cfg.n_layers):
+            gi, gg = eng.routing(l)
+            assert topk_ok(gi[b], o["trace"]["topk_idx"][l], o["trace"]["router_score"][l], cfg.top_k)
+            if set(gi[b]) == set(o["trace"]["topk_idx"][l]):
+                assert np.allclose(gg[b], o["trace"]["topk_gate"][l], atol=GATE_ABS)
+                assert abs(gg[b].sum() - 1) < 1e-5
+        assert eng.get_length(b) == lens[b] + 1
+    chk.assert_ok()
+
+
+def test_moe_small_slot_offset_and_batch_invariance(moe_small):
+    """Sequence results do not depend on which other sequences share the step."""
+    m_cpu, m_gpu = moe_small
+    cfg = MOE_SMALL
+    eng = _engine(m_gpu)
+    k, v = synth.gen_kv(cfg, 77, seed=9)
+    for s in range(4):
+        eng.prefill_import(k.cuda(), v.cuda(), seq=s)
+    toks = [11, 11, 11, 11]
+    lg4, nx4, h4 = _gpu_step(eng, tok=toks, batch=4)
+    for s in range(4):
+        eng.set_length(s, 77)
+    lg1, nx1, h1 = _gpu_step(eng, tok=[11], batch=1, seq0=2)
+    assert np.max(np.abs(lg4[0] - lg1[0])) < 1e-3 and nx4[0] == nx1[0]
+    assert np.allclose(lg4[0], lg4[3], atol=1e-3)
+
+
+def test_moe_small_deterministic_rerun(moe_small):
+    m_cpu, m_gpu = moe_small
+    eng = _engine(m_gpu)
+    k, v = synth.gen_kv(MOE_SMALL, 300, seed=10)
+    eng.prefill_import(k.cuda(), v.cuda(), seq=0)
+    a = _gpu_step(eng, tok=[5])
+    eng.set_length(0, 300)
+    b = _gpu_step(eng, tok=[5])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+
+
+def test_argument_errors(moe_small):
+    from latency_moe_decode_gb300.capi import DecError
+    m_cpu, m_gpu = moe_small
+    eng = _engine(m_gpu, max_batch=2, max_ctx=40)
+    t = torch.zeros(3, dtype=torch.int32, device="cuda")
+    with pytest.raises(DecError) as e:
+        eng.step(tokens=t, batch=3)
+    assert e.value.status == -1
+    eng.step(tokens=t, batch=0)  # no-op
+    k, v = synth.gen_kv(MOE_SMALL.replace(max_ctx=40), 40, seed=1)
+    eng.prefill_import(k.cuda(), v.cuda(), seq=0)
+    with pytest.raises(DecError) as e:
+        eng.step(tokens=t[:1], batch=1)
+    assert e.value.status == -8  # capacity
+    eng.sync()
+
+
+# ------------------------------------------------------------------------------------------------
+# full size: one MoE layer (hidden 4096, 64 experts, top-8, shared expert), KV 8192 ~N(0,1)
+
+
+@pytest.fixture(scope="module")
+def moe8():
+    m_gpu = synth.gen_model(synth.MOE8, seed=0, device="cuda")
+    m_cpu = synth.model_to(m_gpu, "cpu")
+    return m_cpu, m_gpu
+
+
+def _one_layer(m):
+    m1 = {"cfg": synth.MOE_LAYER, "layers": [m["layers"][0]]}
+    return m1
+
+
+def test_moe_layer_kv8192_hidden_input(moe8):
+    m_cpu, m_gpu = moe8
+    cfg = synth.MOE_LAYER
+    k, v = synth.gen_kv(cfg, 8192, seed=0, device="cuda")
+    x = synth.gen_hidden(1, cfg.hidden, seed=0, device="cuda")
+    orc = oracle.Oracle(_one_layer(m_cpu))
+    kv = orc.new_kv(8193)
+    orc.import_kv(kv, k.cpu(), v.cpu(), 8192)
+    o = orc.decode_step(kv, 8192, hidden=t_bits(x)[0], want_trace=True)
+    eng = _engine(_one_layer(m_gpu), max_ctx=8193)
+    eng.prefill_import(k, v, seq=0)
+    _, _, g_hidden = _gpu_step(eng, hidden=x, batch=1)
+    assert rel_l2(bf16_to_f64(g_hidden[0]), bf16_to_f64(o["hidden"])) <= 1e-2
+    gi, gg = eng.routing(0)
+    assert topk_ok(gi[0], o["trace"]["topk_idx"][0], o["trace"]["router_score"][0], 8)
+    assert abs(gg[0].sum() - 1) < 1e-5
+    # the new position's K/V landed in the cache
+    kg, vg = eng.export_kv(0, 0, 8192, 1)
+    assert rel_l2(bf16_to_f64(t_bits(kg)), bf16_to_f64(kv["k"][0, :, 8192])) < 1e-2
+    assert rel_l2(bf16_to_f64(t_bits(vg)), bf16_to_f64(kv["v"][0, :, 8192])) < 1e-2
+
+
+@pytest.mark.parametrize("ctx,steps", [(1024, 3), (8192, 1)], ids=["1k", "8k"])
+def test_moe8_decode_steps_teacher_forced(moe8, ctx, steps):
+    """8-layer stack, vocab 32000: KV state of `ctx` positions imported, then greedy steps."""
+    m_cpu, m_gpu = moe8
+    cfg = synth.MOE8.replace(max_ctx=ctx + 16)
+    k, v = synth.gen_kv(cfg, ctx, seed=1, device="cuda")
+    orc = oracle.Oracle(m_cpu)
+    kv = orc.new_kv(cfg.max_ctx)
+    orc.import_kv(kv, k.cpu(), v.cpu(), ctx)
+    eng = _engine(m_gpu, max_ctx=cfg.max_ctx)
+    eng.prefill_import(k, v, seq=0)
+    chk = StepCheck()
+    tok = 1234
+    for i in range(steps):
+        o = orc.decode_step(kv, ctx + i, token=tok, want_trace=True)
+        g_logits, g_next, g_hidden = _gpu_step(eng, tok=[tok])
+        chk.add(g_logits[0], o["logits"], g_next[0], o["token"], g_hidden[0], o["hidden"])
+        for l in range(cfg.n_layers):
+            gi, _ = eng.routing(l)
+            sc = o["trace"]["router_score"][l]
+            srt = np.sort(sc)[::-1]
+            assert topk_ok(gi[0], o["trace"]["topk_idx"][l], sc, 8), (
+                f"step {i} layer {l}: gpu {sorted(gi[0])} oracle {sorted(o['trace']['topk_idx'][l])} "
+                f"8th/9th oracle scores {srt[7]:.7f} {srt[8]:.7f} gpu-only {[round(sc[e], 7) for e in set(gi[0]) - set(o['trace']['topk_idx'][l])]}"
+                f" hidden-rel so far {chk.max_hidden_rel:.2e}")
+        tok = o["token"]
+    chk.assert_ok()
+
+
+def test_moe8_token_prefill(moe8):
+    """Token-mode prefill at full size: KV of every layer and the next step's logits."""
+    m_cpu, m_gpu = moe8
+    cfg = synth.MOE8.replace(max_ctx=64)
+    prompt = synth.gen_tokens(3, cfg.vocab, seed=7)
+    orc = oracle.Oracle(m_cpu)
+    kv = orc.new_kv(cfg.max_ctx)
+    first = orc.prefill(kv, prompt)
+    eng = _engine(m_gpu, max_ctx=cfg.max_ctx)
+    eng.prefill_tokens(prompt.cuda())
+    for l in range(cfg.n_layers):
+        kg, vg = eng.export_kv(0, l, 0, 3)
+        assert rel_l2(bf16_to_f64(t_bits(kg)), bf16_to_f64(kv["k"][l, :, :3])) < 1e-2
+        assert rel_l2(bf16_to_f64(t_bits(vg)), bf16_to_f64(kv["v"][l, :, :3])) < 1e-2
+    o = orc.decode_step(kv, 3, token=first["token"])
+    g_logits, g_next, g_hidden = _gpu_step(eng, tok=[first["token"]])
+    chk = StepCheck()
+    chk.add(g_logits[0], o["logits"], g_next[0], o["token"], g_hidden[0], o["hidden"])
+    chk.assert_ok()
