@@ -1,0 +1,372 @@
+"""Benchmark of the persistent MoE decode step on GB300.
+
+Default workload ("moe8_1k1k"): the 8-layer MoE stack (hidden 4096, 32/8 heads of 128, 64 routed
+SwiGLU experts of 1536 with top-8 sigmoid routing + 1 shared expert, vocab 32000, FP8-E4M3
+weights with 128x128 fp32 block scales, bf16 activations), batch 1: KV prefilled from 1024 seeded
+random token ids, then one timed step = 1024 greedy decode tokens, device-chained (each step's
+argmax feeds the next launch). Synthetic random-init weights (no trained weights exist here).
+
+value        tokens/s/user, device time: CUDA events on the launch stream around the step's 1024
+             launches, inputs resident in HBM. Each timed step restarts at position 1024.
+e2e          the same tokens through dec_generate() with pinned HOST buffers: the first token is
+             copied host->device and the 1024 generated tokens device->host inside the region.
+roofline     the decode kernel (the only kernel of a step): algorithmic bytes per launch (weights
+             of the attention, router, the selected + shared experts and the LM head, + KV read
+             over the context + KV write) / mean launch time, against the measured HBM copy peak.
+cpu_baseline the oracle (single-threaded C) decoding a few tokens of the same workload on the host.
+--impl reference runs that oracle as the reference arm.
+Multi-GPU: replicas only (one independent engine per rank); value sums the ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (model, prompt tokens (KV state), decode tokens per step, batch)
+    "moe8_1k1k": ("MOE8", 1024, 1024, 1),
+    "moe8_8k1k": ("MOE8", 8192, 1024, 1),
+    "moe_layer_8k": ("MOE_LAYER", 8192, 256, 1),
+    # small captures for ncu: two layers of the same stack + LM head
+    "moe2_1k_prof": ("MOE2", 1024, 8, 1),
+}
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "latency_moe_decode_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, only if it was taken on the
+    current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "decode_step_kernel_traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("csrc_hash") != csrc_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algorithmic_bytes(cfg, routed_distinct, ctx_lens, batch):
+    """Bytes one decode launch must move: every weight it reads once (attention, router, the
+    distinct selected experts + shared, LM head, block scales), the KV it attends over, and the
+    KV it writes."""
+    from latency_moe_decode_gb300 import synth
+    wb = synth.weight_bytes_per_token(cfg)
+    d = cfg.hidden
+
+    def mat(n, k):
+        return n * k + 4 * ((n + 127) // 128) * ((k + 127) // 128)
+
+    expert = 2 * mat(cfg.moe_inter, d) + mat(d, cfg.moe_inter)
+    weights = cfg.n_layers * (wb["attn"] + wb["router"]) + wb["lm_head"]
+    weights += sum(routed_distinct) * expert + cfg.n_layers * cfg.n_shared * expert
+    kv_row = cfg.n_kv_heads * cfg.head_dim * 2 * 2  # K and V, bf16
+    kv = cfg.n_layers * kv_row * sum(t + 1 for t in ctx_lens) + cfg.n_layers * kv_row * batch
+    return weights + kv
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from latency_moe_decode_gb300 import synth
+    from latency_moe_decode_gb300.engine import Engine
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    model_name, prompt_len, n_dec, batch = WORKLOADS[args.workload]
+    base = synth.MOE8.replace(n_layers=2) if model_name == "MOE2" else getattr(synth, model_name)
+    cfg = base.replace(max_ctx=prompt_len + n_dec + 16, max_batch=batch)
+    model = synth.gen_model(cfg, seed=0, device="cuda")
+    eng = Engine(model, max_ctx=cfg.max_ctx, max_batch=batch)
+    del model
+    torch.cuda.empty_cache()
+    headless = cfg.vocab == 0
+    if headless or args.kv == "import":
+        k, v = synth.gen_kv(cfg, prompt_len, seed=1, device="cuda")
+        eng.prefill_import(k, v, seq=0, n_seq=batch)
+        del k, v
+    else:
+        prompt = torch.stack([synth.gen_tokens(prompt_len, cfg.vocab, seed=s, device="cuda") for s in range(batch)])
+        eng.prefill_tokens(prompt, seq=0)
+    stream = torch.cuda.current_stream()
+    first = torch.arange(batch, dtype=torch.int32, device="cuda") + 17
+    toks = torch.zeros(n_dec + 1, batch, dtype=torch.int32, device="cuda")
+    hid = synth.gen_hidden(batch, cfg.hidden, seed=2, device="cuda") if headless else None
+    hout = torch.empty_like(hid) if headless else None
+
+    def one_step():
+        for s in range(batch):
+            eng.set_length(s, prompt_len)
+        toks[0] = first
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_dec):
+            if headless:
+                eng.step(hidden=hid, batch=batch, hidden_out=hout, stream=stream)
+            else:
+                eng.step(tokens=toks[i], batch=batch, next_tokens=toks[i + 1], stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    for _ in range(args.warmup):
+        one_step()
+    eng.sync()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    times = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            times.append(one_step())
+    torch.cuda.synchronize()
+    eng.sync()
+    total = sum(times)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    tokens = n_dec * batch * args.steps * world
+    value = tokens / total
+
+    # routing actually taken in the last step (distinct experts per layer) for the byte count
+    distinct = []
+    if cfg.n_experts:
+        for l in range(cfg.n_layers):
+            idx, _ = eng.routing(l)
+            distinct.append(len(set(idx[:batch].reshape(-1).tolist())))
+    ctx = [prompt_len + i for i in range(n_dec)]
+    bytes_per_step = sum(algorithmic_bytes(cfg, distinct, [c] * batch, batch) for c in ctx)
+    launches = n_dec * args.steps
+    per_launch_s = total / (args.steps * world) / n_dec
+    achieved = bytes_per_step / n_dec / per_launch_s / 1e9
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    traffic = profile_traffic(args.workload)
+
+    # e2e through the public API with host buffers
+    e2e = None
+    if not headless:
+        first_h = torch.full((batch,), 17, dtype=torch.int32).pin_memory()
+        out_h = torch.zeros(n_dec, batch, dtype=torch.int32).pin_memory()
+        e2e_t = []
+        for _ in range(max(1, args.steps)):
+            for s in range(batch):
+                eng.set_length(s, prompt_len)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            eng.generate_pinned(first_h, out_h)
+            e2e_t.append(time.perf_counter() - t0)
+        e2e = {"value": n_dec * batch * len(e2e_t) / sum(e2e_t), "unit": "tokens/s/user" if batch == 1 else "tokens/s",
+               "h2d_bytes_per_step": 4 * batch, "d2h_bytes_per_step": 4 * batch * n_dec}
+    trace = eng.trace(512)
+    per_layer_us = None
+    if len(trace) >= 4:
+        codes, ts = trace[0::2].astype(np.int64), trace[1::2].astype(np.int64)
+        bar5 = ts[codes == (8 << 4 | 5)]
+        start = ts[codes == (10 << 4)]
+        if len(bar5) and len(start):
+            edges = np.concatenate([start[:1], bar5])
+            per_layer_us = [round(float(x) / 1e3, 2) for x in np.diff(edges)]
+    info = eng.info()
+    eng.close()
+    if rank != 0:
+        return None
+    line = {
+        "metric": "batch-1 decode tokens/s/user" if batch == 1 else "decode tokens/s",
+        "value": round(value, 2),
+        "unit": "tokens/s/user" if batch == 1 and world == 1 else "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded random-init FP8 weights, random prompt ids)",
+        "config": {"workload": args.workload, "layers": cfg.n_layers, "hidden": cfg.hidden, "heads": cfg.n_heads,
+                   "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "experts": cfg.n_experts,
+                   "top_k": cfg.top_k, "moe_inter": cfg.moe_inter, "shared": cfg.n_shared, "vocab": cfg.vocab,
+                   "batch": batch, "prompt_tokens": prompt_len, "decode_tokens_per_step": n_dec,
+                   "weights": "fp8-e4m3 128x128 block scales", "activations": "bf16",
+                   "l2": "no flush: every decode token streams ~1.9 GB of weights, far above the 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "ms_per_token": round(per_launch_s * 1e3, 4),
+        "per_layer_us": per_layer_us,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_step_kernel", "bytes_per_launch": round(bytes_per_step / n_dec),
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks else "fallback 6.8 TB/s",
+                     "time": "mean launch-to-launch time over the timed region (includes launch gaps)"},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "engine": {"grid": info["grid"], "threads": info["threads"], "ring_slots": info["ring_slots"],
+                   "smem_bytes": info["smem_bytes"], "csrc_hash": csrc_hash()},
+    }
+    if args.cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args, cfg, prompt_len)
+    return line
+
+
+def cpu_baseline(args, cfg, prompt_len, budget_s=None):
+    """The oracle, as it stands, on a bounded sample of the same workload: decode tokens at the
+    workload's context from an imported synthetic KV state of that length (prefill not timed)."""
+    import oracle
+    from latency_moe_decode_gb300 import synth
+
+    budget_s = budget_s or args.cpu_seconds
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    model = synth.model_to(synth.gen_model(cfg, seed=0, device=dev), "cpu")
+    orc = oracle.Oracle(model)
+    kv = orc.new_kv(prompt_len + 64)
+    k, v = synth.gen_kv(cfg, prompt_len, seed=1)
+    orc.import_kv(kv, k, v, prompt_len)
+    hid = synth.gen_hidden(1, cfg.hidden, seed=2)
+    n, t0 = 0, time.perf_counter()
+    tok = 17
+    while True:
+        if cfg.vocab:
+            tok = orc.decode_step(kv, prompt_len + n, token=tok)["token"]
+        else:
+            orc.decode_step(kv, prompt_len + n, hidden=hid[0].view(torch.int16).numpy())
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 64:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 4), "unit": "tokens/s/user", "cores": 1, "kind": "oracle",
+            "sample": f"{n} decode tokens at context {prompt_len} from an imported synthetic KV state, batch 1"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    model_name, prompt_len, n_dec, batch = WORKLOADS[args.workload]
+    from latency_moe_decode_gb300 import synth
+    base = synth.MOE8.replace(n_layers=2) if model_name == "MOE2" else getattr(synth, model_name)
+    cfg = base.replace(max_ctx=prompt_len + 64)
+    times = []
+    cb = None
+    for _ in range(args.warmup + args.steps):
+        cb = cpu_baseline(args, cfg, prompt_len, budget_s=max(5.0, args.cpu_seconds / max(1, args.steps)))
+        times.append(cb)
+    val = statistics.mean(c["value"] for c in times[args.warmup:])
+    return {"impl": "reference", "metric": "batch-1 decode tokens/s/user", "value": round(val, 4),
+            "unit": "tokens/s/user", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "batch": batch, "prompt_tokens": prompt_len},
+            "cpu_baseline": {"value": round(val, 4), "unit": "tokens/s/user", "cores": 1, "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": round(val, 4), "unit": "tokens/s/user", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="moe8_1k1k", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--kv", default="prefill", choices=["prefill", "import"],
+                    help="prefill: KV from the seeded prompt (token mode); import: synthetic KV state")
+    args = ap.parse_args()
+    import __graft_entry__
+    __graft_entry__.build()
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

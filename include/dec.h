@@ -208,9 +208,14 @@ dec_status dec_get_info(dec_engine* eng, dec_info* out);
    gates [max_batch][top_k]; rows >= the step's batch are stale. Synchronises. */
 dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* gates);
 
-/* Per-step device timestamps (%globaltimer, ns) written by CTA 0 at the start of the step, at
-   every grid-wide stage boundary and at the end: copies the most recent step's stamps into
-   host_buf[0..n) and returns how many were written in *n_written. Synchronises. */
+/* Per-step trace written by CTA 0: (event code, %globaltimer ns) pairs in host_buf[2i], [2i+1].
+   code = what << 4 | event; what: 0 q/k/v GEMV, 1 output projection, 2 router, 3 shared-expert
+   (or dense FFN) gate/up, 4 routed gate/up, 5 down projections, 6 LM head, 7 attention, 8 grid
+   barrier, 9 routing wait, 10 step; event: 0 begin, 1 last tile consumed, 2 finalisers done
+   (barrier: its site). Words [512 - 128, 512) hold CTA 0's producer trace in the same format.
+   Words from 512 on hold, for each of the step's first 64 grid barriers, every CTA's arrival
+   time (barrier-major, grid words each). Copies up to n words and returns the count in
+   *n_written. Synchronises. */
 dec_status dec_get_trace(dec_engine* eng, uint64_t* host_buf, int32_t n, int32_t* n_written);
 
 /* Reason for the last failing call on this engine ("" if none). Valid until the next call. */

@@ -17,13 +17,15 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kKvTilePos = 32;                       // KV positions per ring slot
 constexpr int kMaxBatch = 8;
-constexpr int kTraceSlots = 512;                     // stamps kept per step
+constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
+constexpr int kBarTrace = 64;                        // grid barriers whose per-CTA arrival times are kept
 
 // Device error codes (low byte) -- the upper bytes carry where it happened.
 enum : int {
   kDevOk = 0,
   kDevTimeout = 1,
   kDevBadArg = 2,
+  kDevRange = 3,  // an activation outside the f16 range of the GEMV input staging
 };
 
 struct LayerDev {
@@ -56,6 +58,9 @@ struct KParams {
   const uint16_t* embed;
   const uint16_t* final_norm;
   const uint8_t* lm;
+  const uint8_t* warena;  // every repacked weight tile lives in [warena, warena + warena_bytes)
+  unsigned long long warena_bytes;
+  unsigned long long kv_bytes;  // bytes of each of kc / vc
   const float2* rope;  // [max_ctx][hd/2] (cos, sin)
   uint16_t* kc;        // [L][MB][hkv][max_ctx][hd]
   uint16_t* vc;
@@ -69,7 +74,14 @@ struct KParams {
   uint16_t* hrt;    // [umax][MB][inter]
   // split-K partial sums: [segment][slot][MB][128] fp32, and per-output arrival counters
   float *part_qkv, *part_o, *part_router, *part_shgu, *part_rtgu, *part_d, *part_lm;
-  int *cnt_qkv, *cnt_o, *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
+  // q/k/v and output-projection partials are read directly by the next stage: their counters
+  // only grow (one arrival per contributor per launch), [L][row blocks]
+  int *cnt_qkv, *cnt_o;
+  // finalised outputs (router, SwiGLU h, down projection + residual, logits): last-arriver counters
+  int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
+  unsigned* o_flag;  // [L][MB][hkv] = epoch once the attention output of (sequence, KV head) is merged
+  unsigned* h_flag;  // [L][umax + 1][n_rb_gu] = epoch once an expert's 64 SwiGLU rows are final
+                     // (slot umax: the shared / dense expert)
   // attention split-KV partials: [MB][hkv][nch][group][hd + 2], counters [MB][hkv]
   float* attn_part;
   int* attn_cnt;
@@ -81,10 +93,10 @@ struct KParams {
   float* rt_topk_gate;// [L][MB][topk]
   unsigned* rt_flag;  // [L] = epoch once the layer's routing is published
   unsigned long long* amax;  // [MB] packed (ordered logit, ~id) maxima
-  unsigned* gbar;     // [0] arrivals, [32] generation (separate lines)
+  unsigned* gbar;     // [grid] per-CTA grid-barrier sequence words
   int* err;           // device status word
   float* logits_ws;   // [MB][V] when the caller gives no logits buffer
-  unsigned long long* trace;  // [kTraceSlots]
+  unsigned long long* trace;  // [kTraceSlots + kBarTrace * grid]
   // this step
   const int32_t* tokens;
   const uint16_t* hidden_in;

@@ -36,8 +36,9 @@ __global__ void repack_kernel(const RepackDesc d, uint8_t* dst) {
   const int rb = tile / kbn, kb = tile % kbn;
   uint8_t* out = dst + (size_t)tile * kTileBytes;
   for (int q = threadIdx.x; q < kTileData / 16; q += blockDim.x) {
-    const int l = q & 31, w = (q >> 5) & 7, i = q >> 8;
-    const int row = i * 32 + l;  // row inside the tile
+    // consumer order: 16-byte chunk c of tile row 32r + l sits at unit (4c + r) * 32 + l
+    const int l = q & 31, r = (q >> 5) & 3, c = q >> 7;
+    const int row = r * 32 + l;  // row inside the tile
     const int h = rb * 2 + row / 64;
     int src = -1, srow = 0;
     if (d.interleave) {
@@ -56,7 +57,7 @@ __global__ void repack_kernel(const RepackDesc d, uint8_t* dst) {
     }
     uint4 v = make_uint4(0, 0, 0, 0);
     if (src >= 0 && srow < d.n[src]) {
-      const uint8_t* p = d.w[src] + (size_t)srow * d.K + kb * kTileK + w * 16;
+      const uint8_t* p = d.w[src] + (size_t)srow * d.K + kb * kTileK + c * 16;
       v = *reinterpret_cast<const uint4*>(p);
     }
     *reinterpret_cast<uint4*>(out + (size_t)q * 16) = v;
@@ -134,6 +135,8 @@ struct dec_engine {
   std::string err;
   int32_t* d_hist = nullptr;
   int64_t launches = 0, weight_bytes = 0, kv_bytes = 0, ws_bytes = 0;
+  uint8_t* arena = nullptr;  // all repacked weight tiles (one allocation the kernel bounds-checks)
+  size_t arena_size = 0, arena_used = 0;
 };
 
 namespace {
@@ -167,12 +170,21 @@ dec_status dalloc(dec_engine* e, T** p, size_t bytes, int64_t* account) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+dec_status carve(dec_engine* e, size_t bytes, uint8_t** out) {
+  const size_t at = (e->arena_used + 255) & ~(size_t)255;
+  if (at + bytes > e->arena_size) return fail(e, DEC_ERR_ARG, "weight arena overflow");
+  *out = e->arena + at;
+  e->arena_used = at + bytes;
+  e->weight_bytes += (int64_t)bytes;
+  return DEC_OK;
+}
+
 dec_status repack(dec_engine* e, const RepackDesc& d, int n_rb, uint8_t** out) {
   for (int s = 0; s < d.nsrc; ++s)
     if (d.w[s] && (!aligned16(d.w[s]) || !d.s[s])) return fail(e, DEC_ERR_ARG, "weight not 16-byte aligned or scale missing");
   const int kbn = d.K / kTileK;
   size_t bytes = (size_t)n_rb * kbn * kTileBytes;
-  dec_status st = dalloc(e, out, bytes, &e->weight_bytes);
+  dec_status st = carve(e, bytes, out);
   if (st != DEC_OK) return st;
   repack_kernel<<<n_rb * kbn, 256, 0, e->stream>>>(d, *out);
   DEC_CUDA(cudaGetLastError());
@@ -225,6 +237,10 @@ dec_status check_device_status(dec_engine* e) {
     snprintf(buf, sizeof buf, "device wait timed out (site %d); engine poisoned", where);
     return fail(e, DEC_ERR_TIMEOUT, buf);
   }
+  if (kind == kDevRange) {
+    snprintf(buf, sizeof buf, "an activation left the f16 staging range (site %d); engine poisoned", where);
+    return fail(e, DEC_ERR_DEVICE, buf);
+  }
   snprintf(buf, sizeof buf, "device check failed (code %d, site %d); engine poisoned", kind, where);
   return fail(e, DEC_ERR_DEVICE, buf);
 }
@@ -268,7 +284,7 @@ dec_status dec_validate_cfg(const dec_model_cfg* c) {
   } else if (c->dense_ffn % 128 != 0) {
     return DEC_ERR_UNSUPPORTED;
   }
-  if (c->max_batch > kMaxBatch) return DEC_ERR_UNSUPPORTED;
+  if (c->max_batch > kMaxBatch || c->n_kv_heads > 64 || c->hidden > 8192) return DEC_ERR_UNSUPPORTED;
   return DEC_OK;
 }
 
@@ -340,7 +356,21 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   e->grid = e->sms;
   const int G = e->grid;
 
-  // ---- weights
+  // ---- weights: one arena for every repacked tile
+  {
+    const size_t TB = kTileBytes;
+    size_t per_layer = (size_t)p.n_rb_qkv * p.kb_d + (size_t)p.n_rb_d * p.kb_o;
+    if (dense) {
+      per_layer += (size_t)p.n_rb_gu * p.kb_d + (size_t)p.n_rb_d * p.kb_i;
+    } else {
+      per_layer += (size_t)p.n_rb_router * p.kb_d;
+      per_layer += (size_t)(c.n_shared + c.n_experts) * ((size_t)p.n_rb_gu * p.kb_d + (size_t)p.n_rb_d * p.kb_i);
+    }
+    e->arena_size = per_layer * TB * c.n_layers + (size_t)p.n_rb_lm * p.kb_d * TB + 256 * (16 * (size_t)c.n_layers + 16);
+    if ((st = dalloc(e, &e->arena, e->arena_size, nullptr)) != DEC_OK) return bail(st);
+    p.warena = e->arena;
+    p.warena_bytes = e->arena_size;
+  }
   std::vector<LayerDev> layers(c.n_layers);
   for (int l = 0; l < c.n_layers; ++l) {
     const dec_layer_weights& Lw = W->layers[l];
@@ -393,8 +423,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
       }
       uint8_t* egu = nullptr;
       uint8_t* ed = nullptr;
-      if ((st = dalloc(e, &egu, (size_t)c.n_experts * p.e_gu_stride, &e->weight_bytes)) != DEC_OK) return bail(st);
-      if ((st = dalloc(e, &ed, (size_t)c.n_experts * p.e_d_stride, &e->weight_bytes)) != DEC_OK) return bail(st);
+      if ((st = carve(e, (size_t)c.n_experts * p.e_gu_stride, &egu)) != DEC_OK) return bail(st);
+      if ((st = carve(e, (size_t)c.n_experts * p.e_d_stride, &ed)) != DEC_OK) return bail(st);
       for (int x = 0; x < c.n_experts; ++x) {
         RepackDesc gd = gu_desc(Lw.expert_gate[x], Lw.expert_up[x], p.inter, c.hidden);
         RepackDesc dd = plain_desc(Lw.expert_down[x], c.hidden, p.inter);
@@ -446,6 +476,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   // ---- KV cache
   {
     size_t n = (size_t)c.n_layers * c.max_batch * c.n_kv_heads * c.max_ctx * c.head_dim;
+    p.kv_bytes = n * 2;
     if ((st = dalloc(e, &p.kc, n * 2, &e->kv_bytes)) != DEC_OK) return bail(st);
     if ((st = dalloc(e, &p.vc, n * 2, &e->kv_bytes)) != DEC_OK) return bail(st);
     cudaMemsetAsync(p.kc, 0, n * 2, e->stream);
@@ -478,8 +509,10 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.part_rtgu, fb * std::max(1, p.umax) * p.n_rb_gu * p.kb_d);
     Z(p.part_d, fb * (size_t)(p.umax + p.nsh) * p.n_rb_d * p.kb_i);
     Z(p.part_lm, fb * std::max(1, p.n_rb_lm) * p.kb_d);
-    Z(p.cnt_qkv, sizeof(int) * p.n_rb_qkv);
-    Z(p.cnt_o, sizeof(int) * p.n_rb_d);
+    Z(p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv);
+    Z(p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d);
+    Z(p.o_flag, sizeof(unsigned) * (size_t)c.n_layers * MB * c.n_kv_heads);
+    Z(p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu);
     Z(p.cnt_router, sizeof(int) * std::max(1, p.n_rb_router));
     Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
     Z(p.cnt_rtgu, sizeof(int) * std::max(1, p.umax) * p.n_rb_gu);
@@ -496,10 +529,10 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.rt_flag, sizeof(unsigned) * c.n_layers);
     Z(p.amax, sizeof(unsigned long long) * MB);
-    Z(p.gbar, sizeof(unsigned) * 64);
+    Z(p.gbar, sizeof(unsigned) * std::max(1024, G + 32));
     Z(p.err, sizeof(int) * 32);
     Z(p.logits_ws, sizeof(float) * MB * std::max(1, c.vocab));
-    Z(p.trace, sizeof(unsigned long long) * kTraceSlots);
+    Z(p.trace, sizeof(unsigned long long) * (kTraceSlots + (size_t)kBarTrace * G));
     Z(e->d_hist, sizeof(int32_t) * (size_t)(c.max_ctx + 1) * MB);
 #undef Z
   }
@@ -746,7 +779,7 @@ dec_status dec_get_routing(dec_engine* e, int32_t layer, int32_t* idx, float* ga
 dec_status dec_get_trace(dec_engine* e, uint64_t* host_buf, int32_t n, int32_t* n_written) {
   if (!e || !host_buf || n < 0) return DEC_ERR_ARG;
   DEC_CUDA(cudaDeviceSynchronize());
-  const int m = std::min(n, kTraceSlots);
+  const int m = std::min(n, kTraceSlots + kBarTrace * e->grid);
   DEC_CUDA(cudaMemcpy(host_buf, e->base.trace, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost));
   if (n_written) *n_written = m;
   return DEC_OK;

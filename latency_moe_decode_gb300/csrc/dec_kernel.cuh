@@ -16,8 +16,7 @@
 //               on mbarriers. Static weights never depend on activations, so the producer runs
 //               ahead across stage boundaries (the fix named on the vLLM page, section "Agent-
 //               written kernels face evidence gates": only static weights are loaded ahead of a
-//               synchronisation wait). While the routed experts are unknown it issues L2
-//               prefetches of its next-layer tiles, so HBM stays busy through the routing bubble.
+//               synchronisation wait).
 //   warps 0..7  consumers: dequantise E4M3 tiles (CUDA's cvt), multiply by the bf16 activations
 //               held in shared memory, accumulate in fp32, reduce across warps, and publish
 //               split-K partial sums. The last CTA to publish a partial of an output block
@@ -38,6 +37,9 @@ struct SmemLayout {
 };
 
 constexpr int kMaxExperts = 128;
+constexpr int kListCap = 1024;  // contributor slots one down-projection row block may gather
+constexpr int kMaxSegs = 64;    // split-K segments one CTA may flush in one stage
+constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
 struct Misc {
   int flag;
@@ -45,8 +47,8 @@ struct Misc {
   int U;
   int v_lo;
   int len[kMaxBatch];
-  int fin_group[64];
-  int fin_old[64];
+  int fin_group[kMaxSegs];
+  int fin_old[kMaxSegs];
   int elist[kMaxExperts];
   float gate[kMaxBatch][kMaxExperts + 1];
   float rsum[kConsumerWarps][kMaxBatch];
@@ -64,7 +66,9 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   s.red_off = align_up(s.xs_off + bm * xmax * 2, 128);
   int red_gemv = kConsumerWarps * kTileRows * bm * 4;
   int red_attn = kConsumerWarps * group * (hd + 2) * 4;
+  int red_fin = (bm * kTileRows + kListCap + 16) * 4;
   int red = red_gemv > red_attn ? red_gemv : red_attn;
+  red = red > red_fin ? red : red_fin;
   s.misc_off = align_up(s.red_off + red, 128);
   s.total = align_up(s.misc_off + (int)sizeof(Misc), 128);
   return s;
@@ -167,9 +171,29 @@ struct Producer {
   Misc* m;
   unsigned item = 0;
   bool dead = false;
+  int stamp = 0;
+
+  // CTA 0's producer records (code, %globaltimer) pairs in the last kProducerTrace words:
+  // code = what << 4 | event, event 0 = first copy of a stage issued, 1 = last copy issued
+  // (what: GEMV kind, 7 attention, 9 routing wait with 0 = begin, 1 = flag seen).
+  __device__ void trace(int code) {
+    if (blockIdx.x == 0 && stamp + 1 < kProducerTrace) {
+      p.trace[kTraceSlots - kProducerTrace + stamp] = (unsigned long long)code;
+      p.trace[kTraceSlots - kProducerTrace + stamp + 1] = gtimer();
+      stamp += 2;
+    }
+  }
 
   __device__ Producer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, Misc* m_)
       : p(p_), ring(r), full(f), empty(e), m(m_) {}
+
+  // every bulk copy source must lie inside its allocation (checked before the copy is issued)
+  __device__ bool in_range(const void* src, size_t bytes, const void* base, size_t extent, int where) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(base);
+    if (a >= b && a + bytes <= b + extent && (a & 15u) == 0 && (bytes & 15u) == 0) return true;
+    raise_err(p, kDevBadArg, where);
+    return false;
+  }
 
   // claim the next slot: wait until the consumers released it
   __device__ bool claim(int& slot) {
@@ -190,24 +214,22 @@ struct Producer {
     const int G_ = gridDim.x;
     const int t0 = range_lo(g.T, blockIdx.x, G_), t1 = range_lo(g.T, blockIdx.x + 1, G_);
     const LayerDev& Ld = p.layers[l < p.L ? l : 0];
+    if (t1 > t0) trace(kind << 4);
     for (int t = t0; t < t1; ++t) {
       int slot;
       if (!claim(slot)) return;
       const uint8_t* src = tile_addr(p, Ld, kind, t, g, U, elist);
       uint8_t* dst = ring + (size_t)slot * kSlotBytes;
+      if (!in_range(src, kTileBytes, p.warena, p.warena_bytes, 30)) {
+        mbar_arrive(&full[slot]);  // keep the ring consistent; the status word stops the step
+        ++item;
+        continue;
+      }
       mbar_arrive_expect_tx(&full[slot], kTileBytes);
       bulk_g2s(dst, src, kTileBytes, &full[slot]);
       ++item;
     }
-  }
-
-  __device__ void prefetch_gemv(int kind, int l) {
-    if (dead) return;
-    const StageGeo g = stage_geo(p, kind, 0);
-    const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
-    const LayerDev& Ld = p.layers[l < p.L ? l : 0];
-    const int tmax = t0 + 24;  // at most ~390 KB per stage and CTA
-    for (int t = t0; t < t1 && t < tmax; ++t) prefetch_l2(tile_addr(p, Ld, kind, t, g, 0, nullptr), kTileBytes);
+    if (t1 > t0) trace(kind << 4 | 1);
   }
 
   __device__ void issue_attn(int l) {
@@ -223,6 +245,12 @@ struct Producer {
         int n = min(kKvTilePos, a.T - p0);
         uint8_t* dst = ring + (size_t)slot * kSlotBytes;
         const size_t r0 = kv_row(p, l, a.b, a.g, p0);
+        if (n < 1 || n > kKvTilePos || !in_range(p.kc + r0, n * row_bytes, p.kc, p.kv_bytes, 31) ||
+            !in_range(p.vc + r0, n * row_bytes, p.vc, p.kv_bytes, 32)) {
+          mbar_arrive(&full[slot]);
+          ++item;
+          continue;
+        }
         mbar_arrive_expect_tx(&full[slot], 2u * n * row_bytes);
         bulk_g2s(dst, p.kc + r0, n * row_bytes, &full[slot]);
         bulk_g2s(dst + kKvTilePos * row_bytes, p.vc + r0, n * row_bytes, &full[slot]);
@@ -231,26 +259,15 @@ struct Producer {
     }
   }
 
-  __device__ void prefetch_attn(int l) {
-    if (dead) return;
-    const int NU = p.B * p.hkv * p.nch;
-    for (int u = blockIdx.x; u < NU; u += gridDim.x) {
-      AttnUnit a = attn_unit(p, m, u);
-      if (a.tile1 <= a.tile0) continue;
-      int n = min(a.T, a.tile1 * kKvTilePos) - a.tile0 * kKvTilePos;
-      const size_t r0 = kv_row(p, l, a.b, a.g, a.tile0 * kKvTilePos);
-      prefetch_l2(p.kc + r0, (unsigned)n * HD * 2);
-      prefetch_l2(p.vc + r0, (unsigned)n * HD * 2);
-    }
-  }
-
   // Routed experts are known only after the router: wait for this layer's routing flag.
   __device__ bool routing(int l, int& U, int* elist) {
     if (dead) return false;
+    trace(9 << 4);
     if (!wait_flag(p, p.rt_flag + l, p.epoch, 11)) {
       dead = true;
       return false;
     }
+    trace(9 << 4 | 1);
     U = min(max(__ldcg(p.rt_u), 0), p.umax);
     for (int i = 0; i < U; ++i) elist[i] = min(max(__ldcg(p.rt_elist + i), 0), p.E - 1);
     return true;
@@ -281,14 +298,6 @@ struct Producer {
       } else {
         issue_gemv(K_ROUTER, l, 0, nullptr);
         if (p.nsh) issue_gemv(K_SHGU, l, 0, nullptr);
-        // fill the routing bubble with L2 prefetches of what this CTA loads next
-        if (l + 1 < p.L) {
-          prefetch_gemv(K_QKV, l + 1);
-          prefetch_attn(l + 1);
-          prefetch_gemv(K_O, l + 1);
-        } else if (p.V > 0) {
-          prefetch_gemv(K_LM, 0);
-        }
         int U = 0;
         if (!routing(l, U, elist)) break;
         issue_gemv(K_RTGU, l, U, elist);
@@ -317,6 +326,9 @@ struct Consumer {
   bool dead = false;
   int warp, lane, tid;
   int stamp = 0;
+  int nflush = 0;   // segments flushed in the current stage
+  int pend = -1;    // pending counter arrival owned by this lane (warp 0 only)
+  unsigned nbar = 0;  // grid barriers passed in this step
 
   __device__ Consumer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint16_t* x, float* rd,
                       Misc* m_)
@@ -326,8 +338,15 @@ struct Consumer {
     lane = tid & 31;
   }
 
-  __device__ void trace() {
-    if (blockIdx.x == 0 && tid == 0 && stamp < kTraceSlots) p.trace[stamp++] = gtimer();
+  // CTA 0 records (event code, %globaltimer) pairs: code = what << 4 | event, where `what` is a
+  // GEMV kind (0..6), 7 attention, 8 grid barrier, 9 routing wait, 10 step start/end, and event
+  // 0 = begin, 1 = last tile consumed, 2 = finalisers done (barrier: its site number).
+  __device__ void trace(int code) {
+    if (blockIdx.x == 0 && tid == 0 && stamp + 1 < kTraceSlots - kProducerTrace) {
+      p.trace[stamp] = (unsigned long long)code;
+      p.trace[stamp + 1] = gtimer();
+      stamp += 2;
+    }
   }
 
   __device__ bool gsync(int where) {
@@ -337,12 +356,18 @@ struct Consumer {
       cons_sync();
       return false;
     }
-    bool ok = grid_sync(p, &m->flag, where);
+    const unsigned seq = p.epoch * 64u + (++nbar);
+    if (tid == 0 && nbar <= (unsigned)kBarTrace)  // every CTA's arrival time at this barrier
+      p.trace[kTraceSlots + (size_t)(nbar - 1) * gridDim.x + blockIdx.x] = gtimer();
+    bool ok = grid_sync(p, &m->flag, where, seq);
     if (!ok) dead = true;
-    trace();
+    trace(8 << 4 | where);
     return ok;
   }
 
+  // Every consumer warp walks the same item sequence; item i is consumed by warp i % 8 alone,
+  // so eight tiles are in flight across the warps of a CTA.
+  __device__ bool mine() const { return (item % kConsumerWarps) == (unsigned)warp; }
   __device__ const uint8_t* wait_item() {
     int slot = item % p.ring;
     if (!dead) {
@@ -350,10 +375,11 @@ struct Consumer {
     }
     return ring + (size_t)slot * kSlotBytes;
   }
-  __device__ void release_item() {
+  // A slot's "empty" barrier expects kConsumerWarps arrivals: a GEMV tile's owner arrives for all
+  // of them at once, a KV tile (shared by all warps) gets one arrival per warp.
+  __device__ void release_item(unsigned count = kConsumerWarps) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[item % p.ring]);
-    ++item;
+    if (lane == 0) mbar_arrive_cnt(&empty[item % p.ring], count);
   }
 
   // -------- activation staging --------
@@ -364,19 +390,63 @@ struct Consumer {
     return p.hidden_in + (size_t)b * p.d;
   }
 
-  // xs[b][0..d) = bf16(rmsnorm(src_b) * w); one pass for the sum of squares, one to write.
-  __device__ void stage_rmsnorm(int l_src, const uint16_t* direct, const uint16_t* w) {
+  // xs[b][0..d) = bf16(rmsnorm(src_b) * w). The activation is read once (all loads of all
+  // tokens issued together), parked in xs while the sums of squares are reduced, then scaled in
+  // place.
+  // With `from_o`, the input is x_mid = bf16(x_in + output projection), summed here from the
+  // projection's published split-K partials (after every contributor has arrived).
+  __device__ void stage_rmsnorm(int l_src, const uint16_t* direct, const uint16_t* w, bool from_o = false) {
+    constexpr int MAXV = 4;  // hidden <= 8192: four 8-element chunks per thread
+    const StageGeo go = stage_geo(p, K_O, 0);
+    if (from_o) {
+      if (tid == 0) {
+        bool ok = !dead;
+        for (int rb = 0; rb < p.n_rb_d && ok; ++rb)
+          ok = wait_at_least(p, p.cnt_o + (size_t)l_src * p.n_rb_d + rb,
+                             (int)p.epoch * n_contrib(rb * go.kbs, go.kbs, go.T, gridDim.x), 18);
+        m->flag = ok ? 1 : 0;
+      }
+      cons_sync();
+      if (!m->flag) dead = true;
+    }
     for (int b = 0; b < p.B; ++b) {
       const uint16_t* src = direct ? direct + (size_t)b * p.d : x_in(l_src, b);
-      float ss = 0.f;
-      for (int k = tid * 8; k < p.d; k += kConsumerWarps * 32 * 8) {
-        uint4 v = ldcg4(src + k);
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+      uint4 v[MAXV];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float a = bf16lo(u[j]), c = bf16hi(u[j]);
-          ss = fmaf(a, a, ss);
-          ss = fmaf(c, c, ss);
+      for (int j = 0; j < MAXV; ++j) {
+        const int k = (tid + j * kConsumerWarps * 32) * 8;
+        if (k < p.d) v[j] = ldcg4(src + k);
+      }
+      if (from_o) {
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+          const int k = (tid + j * kConsumerWarps * 32) * 8;
+          if (k < p.d) {
+            float o8[8];
+            seg_sum8(K_O, go, k / kTileRows, b, k % kTileRows, o8);
+            uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint16_t lo = f2bf(bf16lo(u[q]) + o8[2 * q]);
+              const uint16_t hi = f2bf(bf16hi(u[q]) + o8[2 * q + 1]);
+              u[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+          }
+        }
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int k = (tid + j * kConsumerWarps * 32) * 8;
+        if (k < p.d) {
+          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[j]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float a = bf16lo(u[q]), c = bf16hi(u[q]);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(c, c, ss);
+          }
+          *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) = v[j];
         }
       }
 #pragma unroll
@@ -389,19 +459,18 @@ struct Consumer {
 #pragma unroll
       for (int wi = 0; wi < kConsumerWarps; ++wi) ss += m->rsum[wi][b];
       const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
-      const uint16_t* src = direct ? direct + (size_t)b * p.d : x_in(l_src, b);
       for (int k = tid * 8; k < p.d; k += kConsumerWarps * 32 * 8) {
-        uint4 v = ldcg4(src + k);
-        uint4 wv = *reinterpret_cast<const uint4*>(w + k);
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)b * p.xmax + k);
+        const uint4 wv = *reinterpret_cast<const uint4*>(w + k);
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(&xv);
         const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv);
         uint4 o;
         uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint16_t lo = f2bf((bf16lo(u[j]) * inv) * bf16lo(wu[j]));
-          uint16_t hi = f2bf((bf16hi(u[j]) * inv) * bf16hi(wu[j]));
-          ou[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+        for (int q = 0; q < 4; ++q) {
+          const float lo = bf16f(f2bf((bf16lo(u[q]) * inv) * bf16lo(wu[q])));
+          const float hi = bf16f(f2bf((bf16hi(u[q]) * inv) * bf16hi(wu[q])));
+          ou[q] = pack_f16x2(lo, hi);
         }
         *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) = o;
       }
@@ -409,60 +478,77 @@ struct Consumer {
     cons_sync();
   }
 
-  // xs[b][0..n) = src[b][0..n) for a bf16 activation written by other CTAs
+  // The GEMV input is staged in shared memory as f16: every bf16 value with magnitude in
+  // [2^-17, 65504] converts exactly (8 significant bits fit in f16's 11); smaller ones round with
+  // an absolute error below 2^-25, far under the fp32 accumulation error of the sums they feed.
+  // A value beyond the f16 range would become infinite, so it is reported as a device error.
+  __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) raise_err(p, kDevRange, 5);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+
+  // xs[b][dst_off + 0..n) = f16(src[b][0..n)) for a bf16 activation written by other CTAs
   __device__ void stage_copy(const uint16_t* src, int n, size_t src_stride, int dst_off) {
     for (int b = 0; b < p.B; ++b)
-      for (int k = tid * 8; k < n; k += kConsumerWarps * 32 * 8)
-        *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k) = ldcg4(src + (size_t)b * src_stride + k);
+#pragma unroll 4
+      for (int k = tid * 8; k < n; k += kConsumerWarps * 32 * 8) {
+        const uint4 v = ldcg4(src + (size_t)b * src_stride + k);
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+        uint4 o;
+        uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ou[q] = pack_f16x2(bf16lo(u[q]), bf16hi(u[q]));
+        *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k) = o;
+      }
   }
 
   // -------- split-K GEMV over one stage --------
 
+  // One warp consumes a whole 128x128 tile: lane l owns rows l, l+32, l+64, l+96 and walks the
+  // 128 columns in eight 16-byte chunks (the repacked tile stores chunk c of row 32r + l at
+  // 16 * ((4c + r) * 32 + l), so every shared-memory load is conflict-free). The activation chunk
+  // is the same for all lanes (a broadcast load). E4M3 pairs become f16 pairs exactly (CUDA's
+  // cvt); each product is then formed and accumulated in fp32 by one mixed-precision FMA
+  // (f16 x f16 + f32, one rounding, as converting both operands to fp32 first would give).
+  // The tile's block scale (rows 0..63 / 64..127) multiplies the tile sum.
   __device__ __forceinline__ void tile_dot(const uint8_t* tile, int xoff, const float* gmul,
                                            float (&acc)[4][BM]) {
-    uint4 wv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      wv[i] = *reinterpret_cast<const uint4*>(tile + (((i * kConsumerWarps + warp) * 32 + lane) << 4));
     const float2 sc = *reinterpret_cast<const float2*>(tile + kTileData);
-    float wf[4][16];
+    float part[4][BM][2];  // two FMA chains per (row, token)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t* u = reinterpret_cast<const uint32_t*>(&wv[i]);
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float2 a = e4m3x2_to_float2(u[j]);
-        float2 c = e4m3x2_to_float2(u[j] >> 16);
-        wf[i][4 * j + 0] = a.x;
-        wf[i][4 * j + 1] = a.y;
-        wf[i][4 * j + 2] = c.x;
-        wf[i][4 * j + 3] = c.y;
+      for (int b = 0; b < BM; ++b) part[r][b][0] = part[r][b][1] = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint4 wv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) wv[r] = *reinterpret_cast<const uint4*>(tile + (((c * 4 + r) * 32 + lane) << 4));
+#pragma unroll
+      for (int b = 0; b < BM; ++b) {
+        if (b < p.B) {
+          const uint16_t* xp = xs + (size_t)b * p.xmax + xoff + c * 16;
+          const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 8);
+          const uint32_t xh[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const uint32_t* u = reinterpret_cast<const uint32_t*>(&wv[r]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              fma_f16x2_f32(e4m3x2_to_f16x2(u[j]), xh[2 * j], part[r][b][0], part[r][b][1]);
+              fma_f16x2_f32(e4m3x2_to_f16x2(u[j] >> 16), xh[2 * j + 1], part[r][b][0], part[r][b][1]);
+            }
+          }
+        }
       }
     }
 #pragma unroll
-    for (int b = 0; b < BM; ++b) {
-      if (b < p.B) {
-        const uint16_t* xp = xs + (size_t)b * p.xmax + xoff + warp * 16;
-        uint4 x0 = *reinterpret_cast<const uint4*>(xp);
-        uint4 x1 = *reinterpret_cast<const uint4*>(xp + 8);
-        const uint32_t* xu0 = reinterpret_cast<const uint32_t*>(&x0);
-        const uint32_t* xu1 = reinterpret_cast<const uint32_t*>(&x1);
-        float2 xf[8];
+    for (int r = 0; r < 4; ++r) {
+      const float s_r = r < 2 ? sc.x : sc.y;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xf[j] = make_float2(bf16lo(xu0[j]), bf16hi(xu0[j]));
-          xf[4 + j] = make_float2(bf16lo(xu1[j]), bf16hi(xu1[j]));
-        }
-        const float g = gmul[b];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) s2 = __ffma2_rn(make_float2(wf[i][2 * j], wf[i][2 * j + 1]), xf[j], s2);
-          const float sc_i = (i < 2 ? sc.x : sc.y) * g;
-          acc[i][b] = fmaf(sc_i, s2.x + s2.y, acc[i][b]);
-        }
-      }
+      for (int b = 0; b < BM; ++b) acc[r][b] = fmaf(s_r * gmul[b], part[r][b][0] + part[r][b][1], acc[r][b]);
     }
   }
 
@@ -495,7 +581,11 @@ struct Consumer {
 
   // Cross-warp reduction of one segment's accumulators, publication of the CTA's partial sums,
   // and the arrival on the output group's counter (result kept for the end of the stage).
-  __device__ void flush(int kind, const StageGeo& g, int seg, int first_tile, float (&acc)[4][BM]) {
+  __device__ int* pub_counter(int kind, int l) const {
+    return kind == K_QKV ? p.cnt_qkv + (size_t)l * p.n_rb_qkv : p.cnt_o + (size_t)l * p.n_rb_d;
+  }
+
+  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, float (&acc)[4][BM]) {
     // red[w][row][b]
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -514,14 +604,22 @@ struct Consumer {
     }
     __threadfence();
     cons_sync();
+    if (kind == K_QKV || kind == K_O) {
+      // published partials: the readers wait for every contributor of the row block
+      if (tid == 0 && !dead) atomicAdd(pub_counter(kind, l) + seg, 1);
+      return;
+    }
+    // Arrive on the output group's counter. The result is only needed at the end of the stage,
+    // so lane n of warp 0 keeps it in a register and the warp moves on to its next tile.
+    const int n = nflush++;
+    const int grp = seg_group(kind, seg);
+    if (warp == 0 && lane == (n & 31)) {
+      if (n >= 32) m->fin_old[n - 32] = pend;  // more than 32 segments: retire the older one
+      pend = dead ? -1 : atom_add_acqrel(cnt_base(kind) + grp, 1);
+    }
     if (tid == 0) {
-      const int grp = seg_group(kind, seg);
-      const int n = m->nfin;
-      if (n < 64) {
-        m->fin_group[n] = grp;
-        m->fin_old[n] = dead ? -1 : atom_add_acqrel(cnt_base(kind) + grp, 1);
-        m->nfin = n + 1;
-      }
+      if (n < kMaxSegs) m->fin_group[n] = grp;
+      else raise_err(p, kDevBadArg, 4);
     }
   }
 
@@ -541,24 +639,58 @@ struct Consumer {
   __device__ __forceinline__ float seg_sum(int kind, const StageGeo& g, int seg, int b, int row) const {
     const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
     const float* src = part_base(kind) + (size_t)seg * g.kbs * p.MB * kTileRows + (size_t)b * kTileRows + row;
+    const size_t st = (size_t)p.MB * kTileRows;
     float s = 0.f;
-    for (int c = 0; c < nc; ++c) s += ldcg(src + (size_t)c * p.MB * kTileRows);
+    for (int c0 = 0; c0 < nc; c0 += 8) {  // eight independent loads in flight, summed in slot order
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nc) ? ldcg(src + (size_t)(c0 + j) * st) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += v[j];
+    }
     return s;
+  }
+
+  // eight consecutive rows of one segment, all contributor slots loaded together
+  __device__ __forceinline__ void seg_sum8(int kind, const StageGeo& g, int seg, int b, int row0, float (&o)[8]) const {
+    const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
+    const float* src = part_base(kind) + (size_t)seg * g.kbs * p.MB * kTileRows + (size_t)b * kTileRows + row0;
+    const size_t st = (size_t)p.MB * kTileRows;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = 0.f;
+    for (int c0 = 0; c0 < nc; c0 += 4) {
+      float4 v[4][2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (c0 + j < nc) {
+          v[j][0] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * st));
+          v[j][1] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * st + 4));
+        } else {
+          v[j][0] = v[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o[0] += v[j][0].x; o[1] += v[j][0].y; o[2] += v[j][0].z; o[3] += v[j][0].w;
+        o[4] += v[j][1].x; o[5] += v[j][1].y; o[6] += v[j][1].z; o[7] += v[j][1].w;
+      }
+    }
   }
 
   __device__ void gemv_stage(int kind, int l, int U) {
     const StageGeo g = stage_geo(p, kind, U);
     const int G_ = gridDim.x;
     const int t0 = range_lo(g.T, blockIdx.x, G_), t1 = range_lo(g.T, blockIdx.x + 1, G_);
-    if (tid == 0) m->nfin = 0;
+    nflush = 0;
     cons_sync();
+    trace(kind << 4);
     float gmul[BM];
     float acc[4][BM];
     int seg_cur = -1, seg_first = 0;
     for (int t = t0; t < t1; ++t) {
       const int seg = t / g.kbs;
       if (seg != seg_cur) {
-        if (seg_cur >= 0) flush(kind, g, seg_cur, seg_first, acc);
+        if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, acc);
         seg_cur = seg;
         seg_first = t;
 #pragma unroll
@@ -575,14 +707,23 @@ struct Consumer {
 #pragma unroll
         for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
       }
-      const uint8_t* tile = wait_item();
-      if (!dead) tile_dot(tile, xoff, gmul, acc);
-      release_item();
+      if (mine()) {
+        const uint8_t* tile = wait_item();
+        if (!dead) tile_dot(tile, xoff, gmul, acc);
+        release_item();
+      }
+      ++item;
     }
-    if (seg_cur >= 0) flush(kind, g, seg_cur, seg_first, acc);
+    cons_sync();
+    trace(kind << 4 | 1);
+    if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, acc);
+    const int nf = min(nflush, kMaxSegs);
+    if (warp == 0 && lane < min(nflush, 32)) {
+      const int slot = nflush > 32 && lane < nflush - 32 ? lane + 32 : lane;
+      m->fin_old[slot] = pend;
+    }
     cons_sync();
     // finalise the output groups this CTA completed
-    const int nf = m->nfin;
     for (int f = 0; f < nf; ++f) {
       const int grp = m->fin_group[f];
       const int old = m->fin_old[f];
@@ -592,6 +733,7 @@ struct Consumer {
       cons_sync();
       if (tid == 0) atomicExch(cnt_base(kind) + grp, 0);
     }
+    trace(kind << 4 | 2);
   }
 
   // -------- finalisers (run by the CTA whose arrival completed an output group) --------
@@ -599,102 +741,78 @@ struct Consumer {
   __device__ void finalize(int kind, int l, const StageGeo& g, int grp, int U) {
     float* tmp = red;  // [BM][128]
     switch (kind) {
-      case K_QKV: {
-        for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
-          int b = idx / kTileRows, i = idx % kTileRows;
-          tmp[b * kTileRows + i] = seg_sum(kind, g, grp, b, i);
-        }
-        cons_sync();
-        const int hq_rows = p.hq * HD, hk_rows = p.hkv * HD;
-        for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
-          int b = idx / kTileRows, i = idx % kTileRows;
-          int r = grp * kTileRows + i;
-          if (r >= hq_rows + 2 * hk_rows) continue;
-          float val = tmp[b * kTileRows + i];
-          int ih = r % HD;
-          const int pos = m->len[b];
-          if (r < hq_rows + hk_rows) {  // q or k: rotate the (ih, ih + HD/2) pair
-            int j = ih % (HD / 2);
-            float2 cs = p.rope[(size_t)pos * (HD / 2) + j];
-            int partner = (ih < HD / 2) ? i + HD / 2 : i - HD / 2;
-            float other = tmp[b * kTileRows + partner];
-            val = (ih < HD / 2) ? val * cs.x - other * cs.y : val * cs.x + other * cs.y;
-          }
-          uint16_t bv = f2bf(val);
-          if (r < hq_rows) {
-            p.qbuf[(size_t)b * hq_rows + r] = bv;
-          } else if (r < hq_rows + hk_rows) {
-            int gh = (r - hq_rows) / HD;
-            p.kc[kv_row(p, l, b, gh, pos) + ih] = bv;
-          } else {
-            int gh = (r - hq_rows - hk_rows) / HD;
-            p.vc[kv_row(p, l, b, gh, pos) + ih] = bv;
-          }
-        }
-        break;
-      }
-      case K_O: {
-        for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
-          int b = idx / kTileRows, i = idx % kTileRows;
-          int r = grp * kTileRows + i;
-          float y = seg_sum(kind, g, grp, b, i);
-          float x = bf16f(ldcg_u16(x_in(l, b) + r));
-          p.xmid[(size_t)b * p.d + r] = f2bf(x + y);
-        }
-        break;
-      }
       case K_ROUTER: {
+        // logits -> per-token top-k (one warp per token, arg-max by shuffles, ties to the lower
+        // expert index) -> sigmoid scores normalised over the selection -> distinct expert list
         for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
           int b = idx / kTileRows, i = idx % kTileRows;
           tmp[b * kTileRows + i] = (i < p.E) ? seg_sum(kind, g, grp, b, i) : -INFINITY;
         }
-        cons_sync();
-        int* mark = reinterpret_cast<int*>(tmp + BM * kTileRows);  // [128]
+        int* mark = reinterpret_cast<int*>(tmp + BM * kTileRows);  // [128] rank + 1 of expert e
+        int* sel = mark + kMaxExperts;                              // [BM][16]
+        float* sg = reinterpret_cast<float*>(sel + BM * 16);        // [BM][16]
         if (tid < kMaxExperts) mark[tid] = 0;
         cons_sync();
-        if (tid < p.B) {
-          const int b = tid;
-          const float* r = tmp + b * kTileRows;
-          unsigned long long taken0 = 0, taken1 = 0;
-          int sel[16];
-          float sc[16];
-          float sum = 0.f;
-          for (int j = 0; j < p.topk; ++j) {
-            int best = -1;
-            for (int e = 0; e < p.E; ++e) {
-              bool tk = e < 64 ? ((taken0 >> e) & 1ull) : ((taken1 >> (e - 64)) & 1ull);
-              if (!tk && (best < 0 || r[e] > r[best])) best = e;
+        if (warp < p.B) {
+          const int b = warp;
+          float v[kMaxExperts / 32];
+#pragma unroll
+          for (int j = 0; j < kMaxExperts / 32; ++j) v[j] = tmp[b * kTileRows + lane + 32 * j];
+          float ssum = 0.f;
+          for (int k = 0; k < p.topk; ++k) {
+            float bv = v[0];
+            int bi = lane;
+#pragma unroll
+            for (int j = 1; j < kMaxExperts / 32; ++j)
+              if (v[j] > bv) { bv = v[j]; bi = lane + 32 * j; }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+              float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+              int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
             }
-            if (best < 64) taken0 |= 1ull << best; else taken1 |= 1ull << (best - 64);
-            sel[j] = best;
-            sc[j] = 1.0f / (1.0f + expf(-r[best]));
-            sum += sc[j];
+            if ((bi & 31) == lane) v[bi >> 5] = -INFINITY;
+            const float sc = 1.0f / (1.0f + expf(-bv));
+            ssum += sc;
+            if (lane == 0) {
+              sel[b * 16 + k] = bi;
+              sg[b * 16 + k] = sc;
+              mark[bi] = 1;
+            }
           }
-          for (int j = 0; j < p.topk; ++j) {
-            atomicOr(&mark[sel[j]], 1);
-            p.rt_idx[((size_t)l * p.MB + b) * p.topk + j] = sel[j];
-            p.rt_topk_gate[((size_t)l * p.MB + b) * p.topk + j] = sc[j] / sum;
+          __syncwarp();
+          if (lane < p.topk) {
+            const float gt = sg[b * 16 + lane] / ssum;
+            sg[b * 16 + lane] = gt;
+            p.rt_idx[((size_t)l * p.MB + b) * p.topk + lane] = sel[b * 16 + lane];
+            p.rt_topk_gate[((size_t)l * p.MB + b) * p.topk + lane] = gt;
           }
         }
         cons_sync();
-        if (tid == 0) {
+        if (warp == 0) {
+          // distinct experts in ascending order: ballot prefix over the marks
           int U2 = 0;
-          for (int e = 0; e < p.E; ++e)
-            if (mark[e]) {
-              mark[e] = U2 + 1;  // 1-based rank of expert e in the distinct list
-              p.rt_elist[U2++] = e;
+          for (int j = 0; j < kMaxExperts / 32; ++j) {
+            const int e = lane + 32 * j;
+            const bool on = e < p.E && mark[e] != 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, on);
+            const int rank = U2 + __popc(bal & ((1u << lane) - 1u));
+            if (on) {
+              mark[e] = rank + 1;
+              p.rt_elist[rank] = e;
             }
-          p.rt_u[0] = U2;
+            U2 += __popc(bal);
+          }
+          if (lane == 0) p.rt_u[0] = U2;
         }
         cons_sync();
-        for (int idx = tid; idx < p.B * p.E; idx += 256) {
-          int b = idx / p.E, e = idx % p.E;
-          if (mark[e] == 0) continue;
-          float gt = 0.f;
-          for (int j = 0; j < p.topk; ++j)
-            if (p.rt_idx[((size_t)l * p.MB + b) * p.topk + j] == e)
-              gt = p.rt_topk_gate[((size_t)l * p.MB + b) * p.topk + j];
-          p.rt_gate[(size_t)b * kMaxExperts + (mark[e] - 1)] = gt;
+        for (int idx = tid; idx < p.B * kMaxExperts; idx += 256)
+          p.rt_gate[(size_t)(idx / kMaxExperts) * kMaxExperts + (idx % kMaxExperts)] = 0.f;
+        cons_sync();
+        for (int idx = tid; idx < p.B * p.topk; idx += 256) {
+          const int b = idx / p.topk, k = idx % p.topk;
+          const int e = sel[b * 16 + k];
+          p.rt_gate[(size_t)b * kMaxExperts + (mark[e] - 1)] = sg[b * 16 + k];
         }
         __threadfence();
         cons_sync();
@@ -721,17 +839,51 @@ struct Consumer {
           else
             p.hrt[((size_t)u * p.MB + b) * p.inter + j] = f2bf(h);
         }
+        __threadfence();
+        cons_sync();
+        if (tid == 0) {
+          const int slot = kind == K_SHGU ? p.umax : u;
+          st_release(p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch);
+        }
         break;
       }
       case K_D: {
         const int nv = g.T / g.tpe;
+        // every expert's contributor slots for this row block, as offsets into the partials
+        int* list = reinterpret_cast<int*>(tmp + BM * kTileRows);
+        int* nlist = list + kListCap;
+        if (tid == 0) {
+          int n = 0;
+          for (int v = 0; v < nv; ++v) {
+            const int seg = v * p.n_rb_d + grp;
+            const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
+            for (int c = 0; c < nc; ++c) {
+              if (n < kListCap) list[n] = (seg * g.kbs + c) * p.MB * kTileRows;
+              ++n;
+            }
+          }
+          if (n > kListCap) {
+            raise_err(p, kDevBadArg, 3);
+            n = kListCap;
+          }
+          *nlist = n;
+        }
+        cons_sync();
+        const int nl = *nlist;
         for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
           int b = idx / kTileRows, i = idx % kTileRows;
           int r = grp * kTileRows + i;
+          const float* src = p.part_d + (size_t)b * kTileRows + i;
           float y = 0.f;
-          for (int v = 0; v < nv; ++v) y += seg_sum(kind, g, v * p.n_rb_d + grp, b, i);
-          float x = bf16f(ldcg_u16(p.xmid + (size_t)b * p.d + r));
-          uint16_t o = f2bf(x + y);
+          for (int e0 = 0; e0 < nl; e0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = (e0 + j < nl) ? ldcg(src + list[e0 + j]) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) y += v[j];
+          }
+          const float xm = bf16f(f2bf(bf16f(ldcg_u16(x_in(l, b) + r)) + seg_sum(K_O, stage_geo(p, K_O, 0), grp, b, i)));
+          uint16_t o = f2bf(xm + y);
           p.xbuf[((size_t)((l + 1) & 1) * p.MB + b) * p.d + r] = o;
           if (l == p.L - 1 && p.hidden_out) p.hidden_out[(size_t)b * p.d + r] = o;
         }
@@ -779,8 +931,25 @@ struct Consumer {
 
   // -------- split-KV GQA attention --------
 
-  // Reduce NV partial values across the warp; afterwards lane l holds the total of value
-  // index l / (32 / NV).
+  // DPL consecutive bf16 values -> fp32 (one 4- or 8-byte load); `l2` for data written by other
+  // CTAs in this launch (L2-coherent load), otherwise a plain (shared-memory) load
+  template <int DPL>
+  __device__ __forceinline__ void load_bf16_row(const uint16_t* src, bool l2, float (&f)[DPL]) {
+    if (DPL == 4) {
+      uint2 v = l2 ? __ldcg(reinterpret_cast<const uint2*>(src)) : *reinterpret_cast<const uint2*>(src);
+      f[0] = bf16lo(v.x);
+      f[1] = bf16hi(v.x);
+      f[2 % DPL] = bf16lo(v.y);
+      f[3 % DPL] = bf16hi(v.y);
+    } else {
+      uint32_t v = l2 ? __ldcg(reinterpret_cast<const unsigned int*>(src)) : *reinterpret_cast<const uint32_t*>(src);
+      f[0] = bf16lo(v);
+      f[1 % DPL] = bf16hi(v);
+    }
+  }
+
+  // Reduce NV partial values across the warp (a butterfly that halves the value count at each
+  // level); afterwards lane l holds the total of value index l / (32 / NV).
   template <int NV>
   __device__ __forceinline__ float warp_transpose_reduce(float (&v)[NV]) {
 #pragma unroll
@@ -801,25 +970,117 @@ struct Consumer {
     return r;
   }
 
+  // thread 0: wait until every contributor of the given q/k/v row blocks has published
+  __device__ bool wait_qkv_rows(int l, int row0, int row1, int where) {
+    const StageGeo gq = stage_geo(p, K_QKV, 0);
+    for (int rb = row0 / kTileRows; rb <= (row1 - 1) / kTileRows; ++rb) {
+      const int target = (int)p.epoch * n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x);
+      if (!wait_at_least(p, p.cnt_qkv + (size_t)l * p.n_rb_qkv + rb, target, where)) return false;
+    }
+    return true;
+  }
+
+  // The unit's q heads, key and value for this token: summed from the published split-K
+  // partials, rotated (half-split RoPE at the token's position, angles from the table), rounded
+  // to bf16. The unit whose chunk holds the new position also appends k and v to the cache.
+  __device__ void qkv_prologue(int l, const AttnUnit& a, float* qkvn) {
+    if (tid == 0) {
+      bool ok = !dead;
+      const int q0 = a.g * G * HD, k0 = p.hq * HD + a.g * HD, v0 = (p.hq + p.hkv) * HD + a.g * HD;
+      ok = ok && wait_qkv_rows(l, q0, q0 + G * HD, 13);
+      ok = ok && wait_qkv_rows(l, k0, k0 + HD, 14);
+      ok = ok && wait_qkv_rows(l, v0, v0 + HD, 15);
+      m->flag = ok ? 1 : 0;
+    }
+    cons_sync();
+    if (!m->flag) dead = true;
+    const StageGeo gq = stage_geo(p, K_QKV, 0);
+    float* raw = qkvn + (G + 2) * HD;
+    for (int idx = tid; idx < (G + 2) * HD; idx += kConsumerWarps * 32) {
+      const int t = idx / HD, d = idx % HD;
+      const int row = t < G ? (a.g * G + t) * HD + d : (t == G ? p.hq * HD : (p.hq + p.hkv) * HD) + a.g * HD + d;
+      raw[idx] = seg_sum(K_QKV, gq, row / kTileRows, a.b, row % kTileRows);
+    }
+    cons_sync();
+    const int pos = m->len[a.b];
+    const bool writer = (pos / kKvTilePos) >= a.tile0 && (pos / kKvTilePos) < a.tile1;
+    for (int idx = tid; idx < (G + 2) * HD; idx += kConsumerWarps * 32) {
+      const int t = idx / HD, d = idx % HD;
+      float val = raw[idx];
+      if (t <= G) {  // q heads and the key rotate; the value does not
+        const int j = d % (HD / 2);
+        const float2 cs = p.rope[(size_t)pos * (HD / 2) + j];
+        const float other = raw[t * HD + (d < HD / 2 ? d + HD / 2 : d - HD / 2)];
+        val = d < HD / 2 ? val * cs.x - other * cs.y : val * cs.x + other * cs.y;
+      }
+      const uint16_t bv = f2bf(val);
+      qkvn[idx] = bf16f(bv);
+      if (writer && t == G) p.kc[kv_row(p, l, a.b, a.g, pos) + d] = bv;
+      if (writer && t == G + 1) p.vc[kv_row(p, l, a.b, a.g, pos) + d] = bv;
+    }
+    cons_sync();
+  }
+
+  // thread 0: wait for the merged attention output of every (sequence, KV head) whose heads the
+  // CTA's output-projection tiles read
+  __device__ void wait_o_groups(int l) {
+    if (tid == 0) {
+      bool ok = !dead;
+      const StageGeo go = stage_geo(p, K_O, 0);
+      const int t0 = range_lo(go.T, blockIdx.x, gridDim.x), t1 = range_lo(go.T, blockIdx.x + 1, gridDim.x);
+      unsigned long long mask = 0;
+      const int span = min(t1 - t0, go.kbs);
+      for (int i = 0; i < span; ++i) {
+        const int kb = (t0 + i) % go.kbs;
+        for (int h = kb * kTileK / HD; h <= ((kb + 1) * kTileK - 1) / HD; ++h) mask |= 1ull << (h / G);
+      }
+      for (int g = 0; g < p.hkv && ok; ++g)
+        if ((mask >> g) & 1ull)
+          for (int b = 0; b < p.B && ok; ++b)
+            ok = wait_flag(p, p.o_flag + ((size_t)l * p.MB + b) * p.hkv + g, p.epoch, 16);
+      m->flag = ok ? 1 : 0;
+    }
+    cons_sync();
+    if (!m->flag) dead = true;
+  }
+
+  // thread 0: wait for the final SwiGLU rows of the experts the CTA's down-projection tiles read
+  __device__ void wait_h(int l, int v_lo, int v_hi, int U) {
+    if (tid == 0) {
+      bool ok = !dead;
+      for (int v = v_lo; v <= v_hi && ok; ++v) {
+        const int slot = v < U ? v : p.umax;
+        for (int rb = 0; rb < p.n_rb_gu && ok; ++rb)
+          ok = wait_flag(p, p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch, 17);
+      }
+      m->flag = ok ? 1 : 0;
+    }
+    cons_sync();
+    if (!m->flag) dead = true;
+  }
+
   __device__ void attn_stage(int l) {
     constexpr int DPL = HD / 32;       // dims per lane
-    constexpr int PPW = kKvTilePos / kConsumerWarps;  // positions per warp per tile (4)
-    constexpr int NV = PPW * G;        // scores per warp per tile
+    constexpr int PPW = kKvTilePos / kConsumerWarps;  // positions per warp in a KV tile (4)
+    constexpr int NV = PPW * G;                        // scores per warp per tile
     static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "scores per warp must be a power of two <= 32");
-    constexpr int LPV = 32 / NV;       // lanes per value after the reduction
+    constexpr int LPV = 32 / NV;                       // lanes holding each reduced score
+    static_assert(DPL == 2 || DPL == 4, "head_dim 64 or 128");
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e)/sqrt(hd)
     const unsigned row_bytes = HD * 2;
     const int NU = p.B * p.hkv * p.nch;
+    trace(7 << 4);
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
       AttnUnit a = attn_unit(p, m, u);
-      // q heads of the group, pre-scaled
+      // The group's q heads, k and v for this token, rotated and rounded to bf16, in shared
+      // memory: qkvn[t][HD] with t < G the query heads, t = G the key, t = G + 1 the value.
+      float* qkvn = red;
+      if (a.tile1 > a.tile0) qkv_prologue(l, a, qkvn);
       float q[G][DPL];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint16_t* qp = p.qbuf + (size_t)a.b * p.hq * HD + (size_t)(a.g * G + h) * HD + lane * DPL;
+      for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) q[h][j] = bf16f(ldcg_u16(qp + j)) * qscale;
-      }
+        for (int j = 0; j < DPL; ++j) q[h][j] = qkvn[h * HD + lane * DPL + j] * qscale;
       float mrun[G], lrun[G], acc[G][DPL];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -829,33 +1090,26 @@ struct Consumer {
         for (int j = 0; j < DPL; ++j) acc[h][j] = 0.f;
       }
       const int newpos = a.T - 1;
+      const int vidx = lane / LPV;
+      const int my_i = vidx / G, my_h = vidx % G;  // the (position, head) score this lane ends with
+      // All eight warps share each KV tile; warp w takes positions 4w..4w+3 and keeps its own
+      // online-softmax state (merged across warps after the unit's last tile).
       for (int t = a.tile0; t < a.tile1; ++t) {
         const uint8_t* slot = wait_item();
         if (!dead) {
           const int p0 = t * kKvTilePos;
           const int npos = min(kKvTilePos, a.T - p0);
           float s[NV];
-          const uint16_t* krow[PPW];
-          const uint16_t* vrow[PPW];
 #pragma unroll
           for (int i = 0; i < PPW; ++i) {
             const int j = warp * PPW + i;
-            const int pa = p0 + j;
-            if (pa == newpos) {
-              krow[i] = p.kc + kv_row(p, l, a.b, a.g, pa);
-              vrow[i] = p.vc + kv_row(p, l, a.b, a.g, pa);
-            } else {
-              krow[i] = reinterpret_cast<const uint16_t*>(slot + j * row_bytes);
-              vrow[i] = reinterpret_cast<const uint16_t*>(slot + kKvTilePos * row_bytes + j * row_bytes);
-            }
             float kf[DPL];
             if (j < npos) {
-              if (pa == newpos) {
+              if (p0 + j == newpos) {  // this step's key comes from the prologue, not the ring
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) kf[d] = bf16f(ldcg_u16(krow[i] + lane * DPL + d));
+                for (int d = 0; d < DPL; ++d) kf[d] = qkvn[G * HD + lane * DPL + d];
               } else {
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) kf[d] = bf16f(krow[i][lane * DPL + d]);
+                load_bf16_row<DPL>(reinterpret_cast<const uint16_t*>(slot + j * row_bytes) + lane * DPL, false, kf);
               }
             } else {
 #pragma unroll
@@ -869,18 +1123,16 @@ struct Consumer {
               s[i * G + h] = acc_s;
             }
           }
-          float mine = warp_transpose_reduce<NV>(s);
-          const int vidx = lane / LPV;
-          const int my_i = vidx / G, my_h = vidx % G;
-          if (warp * PPW + my_i >= npos) mine = -INFINITY;
-          // per-head maximum over this warp's positions: value index bits above log2(G)
-          float bm = mine;
+          float sc_own = warp_transpose_reduce<NV>(s);
+          if (warp * PPW + my_i >= npos) sc_own = -INFINITY;
+          // per-head maximum over this warp's positions (value-index bits above log2(G))
+          float bm = sc_own;
 #pragma unroll
           for (int off = LPV * G; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
           float mnew[G], corr[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            float bmh = __shfl_sync(0xffffffffu, bm, h * LPV);
+            const float bmh = __shfl_sync(0xffffffffu, bm, h * LPV);
             mnew[h] = fmaxf(mrun[h], bmh);
             corr[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(mrun[h] - mnew[h]);
           }
@@ -888,7 +1140,7 @@ struct Consumer {
 #pragma unroll
           for (int h = 1; h < G; ++h)
             if (my_h == h) mn_own = mnew[h];
-          const float pown = (mine == -INFINITY) ? 0.f : exp2f(mine - mn_own);
+          const float pown = (sc_own == -INFINITY) ? 0.f : exp2f(sc_own - mn_own);
           float pv[NV];
 #pragma unroll
           for (int v = 0; v < NV; ++v) pv[v] = __shfl_sync(0xffffffffu, pown, v * LPV);
@@ -909,10 +1161,10 @@ struct Consumer {
               float vf[DPL];
               if (p0 + j == newpos) {
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) vf[d] = bf16f(ldcg_u16(vrow[i] + lane * DPL + d));
+                for (int d = 0; d < DPL; ++d) vf[d] = qkvn[(G + 1) * HD + lane * DPL + d];
               } else {
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) vf[d] = bf16f(vrow[i][lane * DPL + d]);
+                load_bf16_row<DPL>(reinterpret_cast<const uint16_t*>(slot + (kKvTilePos + j) * row_bytes) + lane * DPL,
+                                   false, vf);
               }
 #pragma unroll
               for (int h = 0; h < G; ++h)
@@ -921,8 +1173,11 @@ struct Consumer {
             }
           }
         }
-        release_item();
+        release_item(1);
+        ++item;
       }
+      cons_sync();
+      trace(7 << 4 | 1);
       // merge the 8 warps' states: red = [warp][h][HD + 2]
       float* wst = red;
 #pragma unroll
@@ -964,48 +1219,74 @@ struct Consumer {
       if (m->fin_old[0] == p.nch - 1) {
         __threadfence();
         const float* src = p.attn_part + (((size_t)a.b * p.hkv + a.g) * p.nch * G) * (HD + 2);
+        // chunk maxima / sums -> shared memory, then per (head, dim) the rescaled sum of the
+        // chunks' accumulators with all loads in flight together
+        float* cm = red;                  // [G][nch]
+        float* cl = red + G * p.nch;      // [G][nch]
+        float* cw = red + 2 * G * p.nch;  // [G][nch] weights exp2(m_c - M) / L
+        for (int idx = tid; idx < G * p.nch; idx += 256) {
+          const int h = idx / p.nch, c = idx % p.nch;
+          const float* r = src + ((size_t)c * G + h) * (HD + 2);
+          cm[idx] = ldcg(r + HD);
+          cl[idx] = ldcg(r + HD + 1);
+        }
+        cons_sync();
+        for (int idx = tid; idx < G * p.nch; idx += 256) {
+          const int h = idx / p.nch;
+          float M = -INFINITY;
+          for (int c2 = 0; c2 < p.nch; ++c2) M = fmaxf(M, cm[h * p.nch + c2]);
+          float Lsum = 0.f;
+          for (int c2 = 0; c2 < p.nch; ++c2) {
+            const float mc = cm[h * p.nch + c2];
+            if (mc != -INFINITY) Lsum = fmaf(exp2f(mc - M), cl[h * p.nch + c2], Lsum);
+          }
+          const float mc = cm[idx];
+          cw[idx] = (mc == -INFINITY || !(Lsum > 0.f)) ? 0.f : exp2f(mc - M) / Lsum;
+        }
+        cons_sync();
         for (int idx = tid; idx < G * HD; idx += 256) {
           const int h = idx / HD, d = idx % HD;
-          float M = -INFINITY;
-          for (int c = 0; c < p.nch; ++c) M = fmaxf(M, ldcg(src + ((size_t)c * G + h) * (HD + 2) + HD));
-          float A = 0.f, Lsum = 0.f;
-          for (int c = 0; c < p.nch; ++c) {
-            const float* r = src + ((size_t)c * G + h) * (HD + 2);
-            const float mc = ldcg(r + HD);
-            if (mc == -INFINITY) continue;
-            const float e = exp2f(mc - M);
-            A = fmaf(e, ldcg(r + d), A);
-            Lsum = fmaf(e, ldcg(r + HD + 1), Lsum);
+          float A = 0.f;
+          for (int c0 = 0; c0 < p.nch; c0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[j] = (c0 + j < p.nch) ? ldcg(src + ((size_t)(c0 + j) * G + h) * (HD + 2) + d) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (c0 + j < p.nch) A = fmaf(cw[h * p.nch + c0 + j], v[j], A);
           }
-          const float o = Lsum > 0.f ? A / Lsum : 0.f;
-          p.obuf[(size_t)a.b * p.hq * HD + (size_t)(a.g * G + h) * HD + d] = f2bf(o);
+          p.obuf[(size_t)a.b * p.hq * HD + (size_t)(a.g * G + h) * HD + d] = f2bf(A);
         }
-        if (tid == 0) atomicExch(cnt, 0);
+        __threadfence();
+        cons_sync();
+        if (tid == 0) {
+          atomicExch(cnt, 0);
+          st_release(p.o_flag + ((size_t)l * p.MB + a.b) * p.hkv + a.g, p.epoch);
+        }
       }
       cons_sync();
     }
+    trace(7 << 4 | 2);
   }
 
   // -------- the step --------
 
   __device__ void run() {
-    trace();
+    trace(10 << 4);
     for (int l = 0; l < p.L; ++l) {
       const LayerDev& Ld = p.layers[l];
-      // attention block
+      // attention block: q/k/v partials -> attention units (wait on their row blocks) ->
+      // merged head outputs -> output projection (waits on the groups it reads)
       stage_rmsnorm(l, nullptr, Ld.attn_norm);
       gemv_stage(K_QKV, l, 0);
-      gsync(1);
-      if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
-        for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
       attn_stage(l);
-      gsync(2);
+      wait_o_groups(l);
       stage_copy(p.obuf, p.hq * HD, (size_t)p.hq * HD, 0);
       cons_sync();
       gemv_stage(K_O, l, 0);
-      gsync(3);
-      // FFN block
-      stage_rmsnorm(0, p.xmid, Ld.ffn_norm);
+      // FFN block: x_mid from the projection partials (waits on every row block)
+      stage_rmsnorm(l, nullptr, Ld.ffn_norm, true);
       int U = 0;
       if (p.dense) {
         gemv_stage(K_SHGU, l, 0);
@@ -1021,9 +1302,9 @@ struct Consumer {
           m->flag = dead ? 0 : 1;
         }
         cons_sync();
+        trace(9 << 4);
         if (!m->flag) dead = true;
         U = m->U;
-        for (int i = tid; i < U; i += 256) m->elist[i] = min(max(__ldcg(p.rt_elist + i), 0), p.E - 1);
         for (int i = tid; i < BM * kMaxExperts; i += 256) {
           int b = i / kMaxExperts, u = i % kMaxExperts;
           m->gate[b][u] = (b < p.B && u < U) ? __ldcg(p.rt_gate + (size_t)b * kMaxExperts + u) : 0.f;
@@ -1031,7 +1312,6 @@ struct Consumer {
         cons_sync();
         gemv_stage(K_RTGU, l, U);
       }
-      gsync(4);
       // down projections of all active experts, gate-weighted, + residual
       {
         const StageGeo g = stage_geo(p, K_D, U);
@@ -1041,22 +1321,27 @@ struct Consumer {
           v_lo = t0 / g.tpe;
           v_hi = (t1 - 1) / g.tpe;
         }
+        if ((v_hi - v_lo + 1) * p.inter > p.xmax) raise_err(p, kDevBadArg, 6);
+        wait_h(l, v_lo, v_hi, U);
         if (tid == 0) m->v_lo = v_lo;
         for (int i = tid; i < BM; i += 256) m->gate[i][U] = 1.f;  // shared / dense expert
-        for (int v = v_lo; v <= v_hi; ++v) {
+        for (int v = v_lo; v <= v_hi && (v - v_lo + 1) * p.inter <= p.xmax; ++v) {
           const uint16_t* src = (v < U) ? p.hrt + (size_t)v * p.MB * p.inter : p.hsh;
           stage_copy(src, p.inter, (size_t)p.inter, (v - v_lo) * p.inter);
         }
         cons_sync();
         gemv_stage(K_D, l, U);
       }
-      gsync(5);
+      // the layer's residual stream is complete only when every down-projection block is final
+      gsync(1);
+      if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
+        for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
     }
     if (p.V > 0) {
       stage_rmsnorm(p.L, nullptr, p.final_norm);
       gemv_stage(K_LM, 0, 0);
     }
-    trace();
+    trace(10 << 4 | 1);
   }
 };
 

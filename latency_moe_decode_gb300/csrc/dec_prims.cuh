@@ -50,6 +50,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* b, unsigned count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
   uint32_t ok;
   asm volatile(
@@ -62,16 +66,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier; false on timeout or abort.
+// Wait for phase `parity` of an mbarrier; false on timeout or abort. The clock and the status
+// word (an L2 round trip) are consulted only every 64 polls, so a wait that ends quickly costs
+// no global traffic.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const KParams& p, int where) {
   if (mbar_try_wait(b, parity)) return true;
   const unsigned long long t0 = gtimer();
-  while (true) {
+  for (unsigned it = 1;; ++it) {
     if (mbar_try_wait(b, parity)) return true;
-    if (aborted(p)) return false;
-    if (gtimer() - t0 > p.timeout_ns) {
-      raise_err(p, kDevTimeout, where);
-      return false;
+    if ((it & 63u) == 0) {
+      if (aborted(p)) return false;
+      if (gtimer() - t0 > p.timeout_ns) {
+        raise_err(p, kDevTimeout, where);
+        return false;
+      }
     }
   }
 }
@@ -122,33 +130,43 @@ __device__ __forceinline__ void cons_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Grid barrier among the consumer warps of all CTAs (sense by generation count). Called by all
-// consumer threads; returns false if the kernel is aborting.
-__device__ __noinline__ bool grid_sync(const KParams& p, int* s_flag, int where) {
+// Grid barrier among the consumer warps of all CTAs. Each CTA publishes the barrier's sequence
+// number in its own word (release) and warp 0 polls all the words (acquire) until every CTA has
+// reached it: arrival costs no round trip and there is no single contended counter. Sequence
+// numbers grow across steps (64 per launch epoch), so the words never need resetting. Called by
+// all consumer threads; returns false if the kernel is aborting.
+__device__ __noinline__ bool grid_sync(const KParams& p, int* s_flag, int where, unsigned seq) {
   cons_sync();
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    __threadfence();
-    unsigned* cnt = p.gbar;
-    unsigned* gen = p.gbar + 32;
-    const unsigned g0 = ld_acquire(gen);
-    const unsigned old = atomicAdd(cnt, 1u);
-    if (old == gridDim.x - 1) {
-      atomicExch(cnt, 0u);
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    unsigned* flags = p.gbar;
+    if (lane == 0) {
       __threadfence();
-      st_release(gen, g0 + 1);
-    } else {
-      const unsigned long long t0 = gtimer();
-      while (ld_acquire(gen) == g0) {
-        if (aborted(p)) { ok = 0; break; }
-        if (gtimer() - t0 > p.timeout_ns) {
-          raise_err(p, kDevTimeout, where);
+      st_release(flags + blockIdx.x, seq);
+    }
+    __syncwarp();
+    int ok = 1;
+    const unsigned long long t0 = gtimer();
+    for (unsigned it = 1;; ++it) {
+      bool mine_ok = true;
+      for (int c = lane; c < (int)gridDim.x; c += 32) mine_ok &= (int)(ld_acquire(flags + c) - seq) >= 0;
+      if (__all_sync(0xffffffffu, mine_ok)) break;
+      if ((it & 15u) == 0) {
+        int bad = 0;
+        if (lane == 0) {
+          if (aborted(p)) bad = 1;
+          else if (gtimer() - t0 > p.timeout_ns) {
+            raise_err(p, kDevTimeout, where);
+            bad = 1;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, bad, 0)) {
           ok = 0;
           break;
         }
       }
     }
-    *s_flag = ok && !aborted(p);
+    if (lane == 0) *s_flag = ok && !aborted(p);
   }
   cons_sync();
   return *reinterpret_cast<volatile int*>(s_flag) != 0;
@@ -158,11 +176,30 @@ __device__ __noinline__ bool grid_sync(const KParams& p, int* s_flag, int where)
 __device__ __forceinline__ bool wait_flag(const KParams& p, const unsigned* f, unsigned want, int where) {
   if (ld_acquire(f) == want) return true;
   const unsigned long long t0 = gtimer();
-  while (ld_acquire(f) != want) {
-    if (aborted(p)) return false;
-    if (gtimer() - t0 > p.timeout_ns) {
-      raise_err(p, kDevTimeout, where);
-      return false;
+  for (unsigned it = 1; ld_acquire(f) != want; ++it) {
+    if ((it & 15u) == 0) {
+      if (aborted(p)) return false;
+      if (gtimer() - t0 > p.timeout_ns) {
+        raise_err(p, kDevTimeout, where);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Wait until a counter that only grows reaches `target` (acquire); one thread polls.
+__device__ __forceinline__ bool wait_at_least(const KParams& p, const int* c, int target, int where) {
+  const unsigned* u = reinterpret_cast<const unsigned*>(c);
+  if ((int)ld_acquire(u) >= target) return true;
+  const unsigned long long t0 = gtimer();
+  for (unsigned it = 1; (int)ld_acquire(u) < target; ++it) {
+    if ((it & 15u) == 0) {
+      if (aborted(p)) return false;
+      if (gtimer() - t0 > p.timeout_ns) {
+        raise_err(p, kDevTimeout, where);
+        return false;
+      }
     }
   }
   return true;
@@ -174,6 +211,23 @@ __device__ __forceinline__ bool wait_flag(const KParams& p, const unsigned* f, u
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// two E4M3 codes (low 16 bits) -> packed f16x2, exact (every E4M3 value is an f16 value)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// acc0 += lo(w) * lo(x), acc1 += hi(w) * hi(x): f16 operands, fp32 product-and-sum (one rounding)
+__device__ __forceinline__ void fma_f16x2_f32(uint32_t w2, uint32_t x2, float& acc0, float& acc1) {
+  asm("{\n\t.reg .f16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %2;\n\t"
+      "mov.b32 {xl, xh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(w2), "r"(x2));
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -71,9 +71,9 @@ class StepCheck:
         if gpu_hidden is not None:
             self.max_hidden_rel = max(self.max_hidden_rel, rel_l2(bf16_to_f64(gpu_hidden), bf16_to_f64(orc_hidden)))
 
-    def assert_ok(self, check_tokens=True):
-        assert self.max_logit_err <= LOGIT_MAX_ABS, f"logits max abs err {self.max_logit_err}"
-        assert self.max_hidden_rel <= HIDDEN_REL_L2, f"hidden rel L2 {self.max_hidden_rel}"
+    def assert_ok(self, check_tokens=True, logit_abs=LOGIT_MAX_ABS, hidden_rel=HIDDEN_REL_L2):
+        assert self.max_logit_err <= logit_abs, f"logits max abs err {self.max_logit_err}"
+        assert self.max_hidden_rel <= hidden_rel, f"hidden rel L2 {self.max_hidden_rel}"
         if check_tokens and self.steps:
             rate = (self.agree + self.near_ties) / self.steps
             assert rate >= 0.99, f"greedy agreement {self.agree}/{self.steps} (+{self.near_ties} near ties)"
