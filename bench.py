@@ -249,10 +249,10 @@ def run_ours(args):
     per_layer_us = None
     if len(trace) >= 4:
         codes, ts = trace[0::2].astype(np.int64), trace[1::2].astype(np.int64)
-        bar5 = ts[codes == (8 << 4 | 5)]
+        layer_end = ts[codes == (8 << 4 | 1)]  # the grid barrier that closes each layer
         start = ts[codes == (10 << 4)]
-        if len(bar5) and len(start):
-            edges = np.concatenate([start[:1], bar5])
+        if len(layer_end) and len(start):
+            edges = np.concatenate([start[:1], layer_end])
             per_layer_us = [round(float(x) / 1e3, 2) for x in np.diff(edges)]
     info = eng.info()
     eng.close()
