@@ -329,6 +329,7 @@ struct Consumer {
   int nflush = 0;   // segments flushed in the current stage
   int pend = -1;    // pending counter arrival owned by this lane (warp 0 only)
   unsigned nbar = 0;  // grid barriers passed in this step
+  int nstamp = 0;     // per-CTA dependency stamps written in this step
 
   __device__ Consumer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint16_t* x, float* rd,
                       Misc* m_)
@@ -349,6 +350,12 @@ struct Consumer {
     }
   }
 
+  // every CTA's time at the k-th dependency point of the step (k < kBarTrace)
+  __device__ void cta_stamp() {
+    if (tid == 0 && nstamp < kBarTrace) p.trace[kTraceSlots + (size_t)nstamp * gridDim.x + blockIdx.x] = gtimer();
+    ++nstamp;
+  }
+
   __device__ bool gsync(int where) {
     if (dead) {
       // keep the named-barrier sequence identical across warps; no grid traffic
@@ -357,8 +364,6 @@ struct Consumer {
       return false;
     }
     const unsigned seq = p.epoch * 64u + (++nbar);
-    if (tid == 0 && nbar <= (unsigned)kBarTrace)  // every CTA's arrival time at this barrier
-      p.trace[kTraceSlots + (size_t)(nbar - 1) * gridDim.x + blockIdx.x] = gtimer();
     bool ok = grid_sync(p, &m->flag, where, seq);
     if (!ok) dead = true;
     trace(8 << 4 | where);
@@ -399,15 +404,10 @@ struct Consumer {
     constexpr int MAXV = 4;  // hidden <= 8192: four 8-element chunks per thread
     const StageGeo go = stage_geo(p, K_O, 0);
     if (from_o) {
-      if (tid == 0) {
-        bool ok = !dead;
-        for (int rb = 0; rb < p.n_rb_d && ok; ++rb)
-          ok = wait_at_least(p, p.cnt_o + (size_t)l_src * p.n_rb_d + rb,
-                             (int)p.epoch * n_contrib(rb * go.kbs, go.kbs, go.T, gridDim.x), 18);
-        m->flag = ok ? 1 : 0;
-      }
-      cons_sync();
-      if (!m->flag) dead = true;
+      const int* cnt = p.cnt_o + (size_t)l_src * p.n_rb_d;
+      cta_wait_all(p.n_rb_d, [&](int rb) {
+        return count_reached(cnt + rb, (int)p.epoch * n_contrib(rb * go.kbs, go.kbs, go.T, gridDim.x));
+      }, 18);
     }
     for (int b = 0; b < p.B; ++b) {
       const uint16_t* src = direct ? direct + (size_t)b * p.d : x_in(l_src, b);
@@ -970,31 +970,63 @@ struct Consumer {
     return r;
   }
 
-  // thread 0: wait until every contributor of the given q/k/v row blocks has published
-  __device__ bool wait_qkv_rows(int l, int row0, int row1, int where) {
-    const StageGeo gq = stage_geo(p, K_QKV, 0);
-    for (int rb = row0 / kTileRows; rb <= (row1 - 1) / kTileRows; ++rb) {
-      const int target = (int)p.epoch * n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x);
-      if (!wait_at_least(p, p.cnt_qkv + (size_t)l * p.n_rb_qkv + rb, target, where)) return false;
+  // Warp 0 waits until every one of n conditions holds; lane i checks conditions i, i+32, ...
+  // with one acquire load each, so a wait costs one L2 round trip per poll however many flags it
+  // spans. Afterwards the whole CTA agrees on the outcome (cons_sync). `check(i)` returns true
+  // once condition i holds.
+  template <class F>
+  __device__ void cta_wait_all(int n, F check, int where) {
+    if (warp == 0) {
+      int ok = dead ? 0 : 1;
+      if (ok) {
+        const unsigned long long t0 = gtimer();
+        for (unsigned it = 1;; ++it) {
+          bool mine_ok = true;
+          for (int i = lane; i < n; i += 32) mine_ok &= check(i);
+          if (__all_sync(0xffffffffu, mine_ok)) break;
+          if ((it & 15u) == 0) {
+            int bad = 0;
+            if (lane == 0) {
+              if (aborted(p)) bad = 1;
+              else if (gtimer() - t0 > p.timeout_ns) {
+                raise_err(p, kDevTimeout, where);
+                bad = 1;
+              }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) {
+              ok = 0;
+              break;
+            }
+          }
+        }
+      }
+      if (lane == 0) m->flag = ok;
     }
-    return true;
+    cons_sync();
+    if (!m->flag) dead = true;
+  }
+
+  __device__ __forceinline__ bool count_reached(const int* c, int target) const {
+    return (int)ld_acquire(reinterpret_cast<const unsigned*>(c)) >= target;
   }
 
   // The unit's q heads, key and value for this token: summed from the published split-K
   // partials, rotated (half-split RoPE at the token's position, angles from the table), rounded
   // to bf16. The unit whose chunk holds the new position also appends k and v to the cache.
   __device__ void qkv_prologue(int l, const AttnUnit& a, float* qkvn) {
-    if (tid == 0) {
-      bool ok = !dead;
-      const int q0 = a.g * G * HD, k0 = p.hq * HD + a.g * HD, v0 = (p.hq + p.hkv) * HD + a.g * HD;
-      ok = ok && wait_qkv_rows(l, q0, q0 + G * HD, 13);
-      ok = ok && wait_qkv_rows(l, k0, k0 + HD, 14);
-      ok = ok && wait_qkv_rows(l, v0, v0 + HD, 15);
-      m->flag = ok ? 1 : 0;
-    }
-    cons_sync();
-    if (!m->flag) dead = true;
     const StageGeo gq = stage_geo(p, K_QKV, 0);
+    {
+      // the row blocks holding the group's q heads, key and value (at most 6 for head_dim 128)
+      const int q0 = a.g * G * HD, k0 = p.hq * HD + a.g * HD, v0 = (p.hq + p.hkv) * HD + a.g * HD;
+      const int qa = q0 / kTileRows, qn = (q0 + G * HD - 1) / kTileRows - qa + 1;
+      const int ka = k0 / kTileRows, kn = (k0 + HD - 1) / kTileRows - ka + 1;
+      const int va = v0 / kTileRows, vn = (v0 + HD - 1) / kTileRows - va + 1;
+      const int* cnt = p.cnt_qkv + (size_t)l * p.n_rb_qkv;
+      cta_wait_all(qn + kn + vn, [&](int i) {
+        const int rb = i < qn ? qa + i : (i < qn + kn ? ka + i - qn : va + i - qn - kn);
+        return count_reached(cnt + rb, (int)p.epoch * n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x));
+      }, 13);
+    }
     float* raw = qkvn + (G + 2) * HD;
     for (int idx = tid; idx < (G + 2) * HD; idx += kConsumerWarps * 32) {
       const int t = idx / HD, d = idx % HD;
@@ -1024,39 +1056,30 @@ struct Consumer {
   // thread 0: wait for the merged attention output of every (sequence, KV head) whose heads the
   // CTA's output-projection tiles read
   __device__ void wait_o_groups(int l) {
-    if (tid == 0) {
-      bool ok = !dead;
-      const StageGeo go = stage_geo(p, K_O, 0);
-      const int t0 = range_lo(go.T, blockIdx.x, gridDim.x), t1 = range_lo(go.T, blockIdx.x + 1, gridDim.x);
-      unsigned long long mask = 0;
-      const int span = min(t1 - t0, go.kbs);
-      for (int i = 0; i < span; ++i) {
-        const int kb = (t0 + i) % go.kbs;
-        for (int h = kb * kTileK / HD; h <= ((kb + 1) * kTileK - 1) / HD; ++h) mask |= 1ull << (h / G);
-      }
-      for (int g = 0; g < p.hkv && ok; ++g)
-        if ((mask >> g) & 1ull)
-          for (int b = 0; b < p.B && ok; ++b)
-            ok = wait_flag(p, p.o_flag + ((size_t)l * p.MB + b) * p.hkv + g, p.epoch, 16);
-      m->flag = ok ? 1 : 0;
+    const StageGeo go = stage_geo(p, K_O, 0);
+    const int t0 = range_lo(go.T, blockIdx.x, gridDim.x), t1 = range_lo(go.T, blockIdx.x + 1, gridDim.x);
+    unsigned long long mask = 0;
+    const int span = min(t1 - t0, go.kbs);
+    for (int i = 0; i < span; ++i) {
+      const int kb = (t0 + i) % go.kbs;
+      for (int h = kb * kTileK / HD; h <= ((kb + 1) * kTileK - 1) / HD; ++h) mask |= 1ull << (h / G);
     }
-    cons_sync();
-    if (!m->flag) dead = true;
+    // condition i = (sequence b, KV head g) for the flagged groups; unflagged groups pass at once
+    const unsigned* f = p.o_flag + (size_t)l * p.MB * p.hkv;
+    cta_wait_all(p.B * p.hkv, [&](int i) {
+      const int b = i / p.hkv, g = i % p.hkv;
+      return !((mask >> g) & 1ull) || ld_acquire(f + (size_t)b * p.hkv + g) == p.epoch;
+    }, 16);
   }
 
   // thread 0: wait for the final SwiGLU rows of the experts the CTA's down-projection tiles read
   __device__ void wait_h(int l, int v_lo, int v_hi, int U) {
-    if (tid == 0) {
-      bool ok = !dead;
-      for (int v = v_lo; v <= v_hi && ok; ++v) {
-        const int slot = v < U ? v : p.umax;
-        for (int rb = 0; rb < p.n_rb_gu && ok; ++rb)
-          ok = wait_flag(p, p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch, 17);
-      }
-      m->flag = ok ? 1 : 0;
-    }
-    cons_sync();
-    if (!m->flag) dead = true;
+    const int nv = v_hi >= v_lo ? v_hi - v_lo + 1 : 0;
+    cta_wait_all(nv * p.n_rb_gu, [&](int i) {
+      const int v = v_lo + i / p.n_rb_gu, rb = i % p.n_rb_gu;
+      const int slot = v < U ? v : p.umax;
+      return ld_acquire(p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb) == p.epoch;
+    }, 17);
   }
 
   __device__ void attn_stage(int l) {
@@ -1280,13 +1303,18 @@ struct Consumer {
       // merged head outputs -> output projection (waits on the groups it reads)
       stage_rmsnorm(l, nullptr, Ld.attn_norm);
       gemv_stage(K_QKV, l, 0);
+      cta_stamp();
       attn_stage(l);
+      cta_stamp();
       wait_o_groups(l);
+      cta_stamp();
       stage_copy(p.obuf, p.hq * HD, (size_t)p.hq * HD, 0);
       cons_sync();
       gemv_stage(K_O, l, 0);
+      cta_stamp();
       // FFN block: x_mid from the projection partials (waits on every row block)
       stage_rmsnorm(l, nullptr, Ld.ffn_norm, true);
+      cta_stamp();
       int U = 0;
       if (p.dense) {
         gemv_stage(K_SHGU, l, 0);
@@ -1310,8 +1338,10 @@ struct Consumer {
           m->gate[b][u] = (b < p.B && u < U) ? __ldcg(p.rt_gate + (size_t)b * kMaxExperts + u) : 0.f;
         }
         cons_sync();
+        cta_stamp();
         gemv_stage(K_RTGU, l, U);
       }
+      cta_stamp();
       // down projections of all active experts, gate-weighted, + residual
       {
         const StageGeo g = stage_geo(p, K_D, U);
@@ -1323,6 +1353,7 @@ struct Consumer {
         }
         if ((v_hi - v_lo + 1) * p.inter > p.xmax) raise_err(p, kDevBadArg, 6);
         wait_h(l, v_lo, v_hi, U);
+        cta_stamp();
         if (tid == 0) m->v_lo = v_lo;
         for (int i = tid; i < BM; i += 256) m->gate[i][U] = 1.f;  // shared / dense expert
         for (int v = v_lo; v <= v_hi && (v - v_lo + 1) * p.inter <= p.xmax; ++v) {
@@ -1332,8 +1363,10 @@ struct Consumer {
         cons_sync();
         gemv_stage(K_D, l, U);
       }
+      cta_stamp();
       // the layer's residual stream is complete only when every down-projection block is final
       gsync(1);
+      cta_stamp();
       if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
         for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
     }
