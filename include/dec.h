@@ -141,6 +141,26 @@ typedef struct {
 } dec_ctx;
 dec_status dec_prefill_kv(dec_engine* eng, const dec_ctx* ctx);
 
+/* Token-mode prefill that allocates no device memory. The pages have no counterpart: this is a
+   property of the library boundary, not of the method. dec_prefill_kv's token mode stages the
+   step-major token ids in a buffer it takes with cudaMalloc and returns with cudaFree; a caller
+   that may not allocate device memory while serving (a framework whose caching allocator holds
+   the device's free memory, or a loop in which cudaFree's implicit device-wide synchronisation
+   would stall other streams) calls this instead. The ids are staged in a file-scope device
+   array of DEC_NOALLOC_PREFILL_MAX_IDS int32 (256 KiB), one per device.
+   - ctx must be token mode (k_import and v_import NULL); anything else is DEC_ERR_ARG.
+   - n_seq * n_tokens > DEC_NOALLOC_PREFILL_MAX_IDS returns DEC_ERR_ARG, with the sizes in
+     dec_last_error(), before any work is queued; split longer prompts into several calls.
+   - The first call on a device does a one-time setup: with that device current it looks up the
+     array's device address (cudaGetSymbolAddress) and caches it. Make that first call before
+     any stream capture begins.
+   - Nothing needs to start at zero: a call writes every id it reads before reading it.
+   - The array is shared by all engines on a device: overlapping calls (two host threads, or two
+     engines on one device) race on it; the caller must serialise them.
+   Results, capacity checks and synchronisation are those of dec_prefill_kv's token mode. */
+#define DEC_NOALLOC_PREFILL_MAX_IDS 65536
+dec_status dec_prefill_kv_noalloc(dec_engine* eng, const dec_ctx* ctx);
+
 /* One decode step of `batch` sequences in slots [seq0, seq0 + batch). Token b is written at
    position length[seq0 + b] and attends over positions 0..length (inclusive); the lengths grow
    by one. Exactly one kernel launch on `stream`; nothing is synchronised.

@@ -63,6 +63,7 @@ PROTOTYPES = {
     "dec_validate_cfg": (C.c_int, [C.POINTER(DecModelCfg)]),
     "dec_init": (C.c_int, [C.POINTER(DecModelCfg), C.POINTER(DecWeights), C.c_void_p, C.POINTER(C.c_void_p)]),
     "dec_prefill_kv": (C.c_int, [C.c_void_p, C.POINTER(DecCtx)]),
+    "dec_prefill_kv_noalloc": (C.c_int, [C.c_void_p, C.POINTER(DecCtx)]),
     "dec_step_ex": (C.c_int, [C.c_void_p, C.POINTER(DecStepArgs)]),
     "dec_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
     "dec_generate": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),

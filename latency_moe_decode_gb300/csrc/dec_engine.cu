@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -243,6 +244,46 @@ dec_status check_device_status(dec_engine* e) {
   }
   snprintf(buf, sizeof buf, "device check failed (code %d, site %d); engine poisoned", kind, where);
   return fail(e, DEC_ERR_DEVICE, buf);
+}
+
+}  // namespace
+
+// Staging for dec_prefill_kv_noalloc: the step-major token ids of one token-mode prefill, one copy
+// per device (a file-scope device array, so that entry point allocates no device memory).
+static __device__ __align__(256) int32_t g_prefill_ids[DEC_NOALLOC_PREFILL_MAX_IDS];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_prefill_ids_mu;
+int32_t* g_prefill_ids_addr[kMaxDevices] = {};
+
+// Device address of the engine's device's copy of g_prefill_ids. Looked up once per device, with
+// that device current, then cached; the caller's current device is restored.
+dec_status prefill_ids_scratch(dec_engine* e, int32_t** out) {
+  if (e->device < 0 || e->device >= kMaxDevices)
+    return fail(e, DEC_ERR_UNSUPPORTED, "device ordinal beyond the static scratch table");
+  std::lock_guard<std::mutex> lock(g_prefill_ids_mu);
+  if (!g_prefill_ids_addr[e->device]) {
+    int cur = -1;
+    cudaError_t ce = cudaGetDevice(&cur);
+    if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaGetDevice");
+    if (cur != e->device) {
+      ce = cudaSetDevice(e->device);
+      if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaSetDevice");
+    }
+    void* addr = nullptr;
+    ce = cudaGetSymbolAddress(&addr, g_prefill_ids);
+    if (cur != e->device) {
+      cudaError_t back = cudaSetDevice(cur);
+      if (ce == cudaSuccess && back != cudaSuccess) return cuda_fail(e, back, "cudaSetDevice (restore)");
+    }
+    if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaGetSymbolAddress");
+    if (!addr) return fail(e, DEC_ERR_CUDA, "cudaGetSymbolAddress returned a null address");
+    g_prefill_ids_addr[e->device] = static_cast<int32_t*>(addr);
+  }
+  *out = g_prefill_ids_addr[e->device];
+  return DEC_OK;
 }
 
 }  // namespace
@@ -692,6 +733,51 @@ dec_status dec_prefill_kv(dec_engine* e, const dec_ctx* x) {
   }
   cudaError_t ce = cudaStreamSynchronize(e->stream);
   cudaFree(tt);
+  if (st != DEC_OK) return st;
+  if (ce != cudaSuccess) return cuda_fail(e, ce, "prefill synchronize");
+  return check_device_status(e);
+}
+
+// Token-mode prefill with the ids staged in g_prefill_ids instead of a cudaMalloc'd buffer; for
+// callers that may not allocate device memory while serving (their framework's caching allocator
+// holds the free memory, or cudaFree's implicit device-wide synchronisation would stall other
+// streams). Overlapping calls on one device share g_prefill_ids and race; callers serialise them.
+dec_status dec_prefill_kv_noalloc(dec_engine* e, const dec_ctx* x) {
+  if (!e || !x) return DEC_ERR_ARG;
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  const dec_model_cfg& c = e->cfg;
+  if (x->k_import || x->v_import)
+    return fail(e, DEC_ERR_ARG, "dec_prefill_kv_noalloc takes token mode only; import mode is dec_prefill_kv");
+  if (x->n_seq < 1 || x->seq < 0 || x->seq + x->n_seq > c.max_batch || x->n_tokens < 0)
+    return fail(e, DEC_ERR_ARG, "bad slot range");
+  if (x->n_tokens == 0) return DEC_OK;
+  if ((long long)x->n_seq * x->n_tokens > DEC_NOALLOC_PREFILL_MAX_IDS) {
+    char buf[200];
+    snprintf(buf, sizeof buf,
+             "dec_prefill_kv_noalloc: n_seq * n_tokens = %lld exceeds its static scratch of %d ids; "
+             "split the prompt into several calls or use dec_prefill_kv",
+             (long long)x->n_seq * x->n_tokens, (int)DEC_NOALLOC_PREFILL_MAX_IDS);
+    return fail(e, DEC_ERR_ARG, buf);
+  }
+  if (!x->token_ids) return fail(e, DEC_ERR_ARG, "token_ids missing");
+  if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "token prefill needs an embedding");
+  for (int s = x->seq; s < x->seq + x->n_seq; ++s)
+    if (e->lengths[s] + x->n_tokens > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "prefill exceeds max_ctx");
+  int32_t* tt = nullptr;
+  dec_status st = prefill_ids_scratch(e, &tt);
+  if (st != DEC_OK) return st;
+  DEC_CUDA(cudaDeviceSynchronize());  // earlier steps (or an earlier call) may still read the ids
+  const int n = x->n_seq * x->n_tokens;
+  transpose_tokens_kernel<<<(n + 255) / 256, 256, 0, e->stream>>>(x->token_ids, x->n_seq, x->n_tokens, tt);
+  DEC_CUDA(cudaGetLastError());
+  for (int t = 0; t < x->n_tokens && st == DEC_OK; ++t) {
+    dec_step_args a{};
+    a.tokens = tt + (size_t)t * x->n_seq;
+    a.batch = x->n_seq;
+    a.seq0 = x->seq;
+    st = dec_step_ex(e, &a);
+  }
+  cudaError_t ce = cudaStreamSynchronize(e->stream);
   if (st != DEC_OK) return st;
   if (ce != cudaSuccess) return cuda_fail(e, ce, "prefill synchronize");
   return check_device_status(e);

@@ -113,6 +113,16 @@ class Engine:
         ctx = DecCtx(seq, t.shape[0], t.data_ptr(), t.shape[1], None, None)
         self._check(self.lib.dec_prefill_kv(self.h, C.byref(ctx)), "dec_prefill_kv")
 
+    def prefill_tokens_noalloc(self, tokens: torch.Tensor, seq: int = 0):
+        """As prefill_tokens, through dec_prefill_kv_noalloc (ids staged in the library's static
+        device scratch; at most DEC_NOALLOC_PREFILL_MAX_IDS ids per call). tokens must already be
+        a contiguous device int32 tensor: this wrapper makes no copy."""
+        if tokens.dtype != torch.int32 or not tokens.is_contiguous():
+            raise ValueError("tokens must be a contiguous int32 device tensor")
+        t = tokens if tokens.dim() == 2 else tokens[None]
+        ctx = DecCtx(seq, t.shape[0], t.data_ptr(), t.shape[1], None, None)
+        self._check(self.lib.dec_prefill_kv_noalloc(self.h, C.byref(ctx)), "dec_prefill_kv_noalloc")
+
     def prefill_import(self, k: torch.Tensor, v: torch.Tensor, seq: int = 0, n_seq: int = 1):
         """k, v: device bf16 [n_layers, n_kv_heads, n, head_dim]."""
         k, v = k.contiguous(), v.contiguous()
