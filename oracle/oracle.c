@@ -326,7 +326,7 @@ int32_t orc_decode_step(const orc_model* m, int32_t token, const uint16_t* hidde
   int d = c->hidden;
   double* x = (double*)malloc(sizeof(double) * (size_t)d);
   for (int i = 0; i < d; ++i)
-    x[i] = c->vocab > 0 ? orc_bf16_value(m->embed[(size_t)token * d + i]) : orc_bf16_value(hidden[i]);
+    x[i] = hidden ? orc_bf16_value(hidden[i]) : orc_bf16_value(m->embed[(size_t)token * d + i]);
   for (int l = 0; l < c->n_layers; ++l)
     if (orc_layer_step(m, l, x, pos, kv, tr) != 0) {
       free(x);

@@ -110,7 +110,8 @@ void orc_swiglu_expert(const orc_mat* gate, const orc_mat* up, const orc_mat* do
    layer's k/v for pos are written into kv. */
 int32_t orc_layer_step(const orc_model* m, int32_t layer, double* x, int32_t pos, orc_kv* kv,
                        orc_trace* tr);
-/* One decode step for one sequence. Input: token (vocab > 0) or hidden (bf16 bits, vocab == 0).
+/* One decode step for one sequence. Input: hidden (bf16 bits) when given, else the embedding row
+   of token (vocab > 0); the engine's hidden_in path starts from a hidden state the same way.
    Outputs: logits [vocab] (may be NULL), hidden_out [hidden] final residual stream as bf16 bits
    (may be NULL). Returns the greedy token (lowest id among equal maxima), or -1 if vocab == 0. */
 int32_t orc_decode_step(const orc_model* m, int32_t token, const uint16_t* hidden, int32_t pos,

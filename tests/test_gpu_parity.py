@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from latency_moe_decode_gb300 import synth
-from tests.parity import GATE_ABS, StepCheck, bf16_to_f64, rel_l2, t_bits, topk_ok
+from tests.parity import GATE_ABS, HIDDEN_REL_L2, LOGIT_MAX_ABS, StepCheck, bf16_to_f64, rel_l2, t_bits, topk_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -259,30 +259,70 @@ def test_moe8_every_layer_teacher_forced(moe8, ctx):
     chk.assert_ok()
 
 
-# Margin for the chained comparison: two correct implementations that round to bf16 at the same
-# points still flip an occasional rounding (fp32 vs double sums); one flip in an expert's SwiGLU
-# output moves every row of the layer output by ~1e-4 and cascades, and over several random
-# layers the hidden states drift apart by up to ~1e-2 relative. That moves router scores by up to
-# a few 1e-3, so a selection that differs from the oracle's is accepted when every expert in the
-# difference scores within ROUTE_MARGIN of the oracle's k-th score; such a step is counted as
-# "diverged at a near-tie" and its logits/hidden state are not compared.
-ROUTE_MARGIN = 5e-3
-# Chained over all eight layers the same drift reaches the logits and the hidden state: a few
-# flips per layer (fp32 sums carry ~6e-7 relative error, a bf16 step is 2^-8) each shift every
-# output row of the next projection, and the random layers amplify that ~3x per layer. Measured
-# on this stack: each layer alone matches the oracle to <= 1.4e-3 (the teacher-forced test above,
-# strict tolerances), the chained stack drifts to ~1-3e-2. The chained checks therefore use 3x
-# the single-layer tolerances.
-CHAIN_HIDDEN_REL = 3e-2
-CHAIN_LOGIT_ABS = 1.5e-1
+# The 8-layer stack is sensitive to bf16 rounding in the oracle itself: moving one input element
+# by one bf16 ulp changes every later RMS normalisation a little, so an ulp here and there flips
+# in each bf16 rounding of the normalised activations, and the layer outputs move by ~0.5%
+# (measured on this stack: 4.5e-3 relative after layer 0, 1.5e-2 after layer 7, router scores
+# up to 1e-2 apart, logits up to 7e-2 apart). The GPU's fp32 sums round differently from the
+# oracle's fp64 ones at many such points, so a chained comparison cannot hold the single-layer
+# tolerances (the teacher-forced test above holds them layer by layer). Instead, at every step
+# the oracle also runs the same step with SENS_FLIPS input elements moved by one ulp, and the GPU
+# may differ from the oracle by SENS_K times that spread (never less than the single-layer
+# tolerances): in the router scores of each layer (a selection that differs from the oracle's is
+# accepted when every expert in the difference scores within that margin of the oracle's k-th
+# score; the step then counts as "diverged at a near-tie" and its outputs are not compared), in
+# the final hidden state and in the logits.
+SENS_FLIPS = 8
+SENS_K = 4.0
 CHAIN_KV_REL = 5e-2
 
 
-def _admissible(gpu_sel, orc_sel, scores, k):
+def _route_gap(gpu_sel, orc_sel, scores, k):
+    """Largest distance from the oracle's k-th score among the experts the two selections differ on."""
     s = np.sort(scores)[::-1]
     kth = s[k - 1]
     diff = set(int(x) for x in gpu_sel) ^ set(int(x) for x in orc_sel)
-    return all(abs(scores[e] - kth) <= ROUTE_MARGIN for e in diff)
+    return max((abs(scores[e] - kth) for e in diff), default=0.0)
+
+
+class OracleSpread:
+    """The oracle's own output spread under a one-ulp perturbation of SENS_FLIPS input elements."""
+
+    def __init__(self, orc, kv, pos, x_bits, seed):
+        kv2 = {kk: (vv.copy() if isinstance(vv, np.ndarray) else vv) for kk, vv in kv.items()}
+        bits = np.array(x_bits, np.uint16)
+        idx = np.random.default_rng(seed).choice(bits.size, SENS_FLIPS, replace=False)
+        bits[idx] ^= 1
+        self.o = orc.decode_step(kv2, pos, hidden=bits, want_trace=True)
+
+    def bounds(self, o):
+        """(per-layer router-score margins, hidden rel L2 bound, logits max abs bound) around o."""
+        ds = np.abs(self.o["trace"]["router_score"] - o["trace"]["router_score"]).max(axis=1)
+        margins = SENS_K * np.maximum(ds, 1e-3)
+        h = rel_l2(bf16_to_f64(self.o["hidden"]), bf16_to_f64(o["hidden"]))
+        g = float(np.abs(self.o["logits"] - o["logits"]).max())
+        return margins, max(HIDDEN_REL_L2, SENS_K * h), max(LOGIT_MAX_ABS, SENS_K * g)
+
+
+def _check_chained_step(eng, o, spread, g_logits, g_next, g_hidden, n_layers, where):
+    """Compare one chained GPU step with the oracle's within the oracle's own spread. Returns
+    False when the step diverged at a near-tie of the routing (outputs not compared)."""
+    margins, hid_tol, logit_tol = spread.bounds(o)
+    for l in range(n_layers):
+        gi, _ = eng.routing(l)
+        sc = o["trace"]["router_score"][l]
+        if not topk_ok(gi[0], o["trace"]["topk_idx"][l], sc, 8):
+            gap = _route_gap(gi[0], o["trace"]["topk_idx"][l], sc, 8)
+            assert gap <= margins[l], f"{where} layer {l}: selections differ at score gap {gap:.3e} > {margins[l]:.3e}"
+            return False
+    err = float(np.abs(np.asarray(g_logits[0], np.float64) - o["logits"]).max())
+    assert err <= logit_tol, f"{where}: logits max abs err {err:.3e} > {logit_tol:.3e}"
+    hrel = rel_l2(bf16_to_f64(g_hidden[0]), bf16_to_f64(o["hidden"]))
+    assert hrel <= hid_tol, f"{where}: hidden rel L2 {hrel:.3e} > {hid_tol:.3e}"
+    if int(g_next[0]) != int(o["token"]):
+        top2 = np.sort(o["logits"])[::-1][:2]
+        assert top2[0] - top2[1] < 2 * logit_tol, f"{where}: greedy token differs away from a near-tie"
+    return True
 
 
 @pytest.mark.parametrize("ctx,steps", [(1024, 3), (8192, 1)], ids=["1k", "8k"])
@@ -296,27 +336,19 @@ def test_moe8_chained_decode_steps(moe8, ctx, steps):
     orc.import_kv(kv, k.cpu(), v.cpu(), ctx)
     eng = _engine(m_gpu, max_ctx=cfg.max_ctx)
     eng.prefill_import(k, v, seq=0)
-    chk = StepCheck()
-    diverged = 0
+    embed = m_cpu["embed"].view(torch.int16).numpy().view(np.uint16)
+    compared = diverged = 0
     tok = 1234
     for i in range(steps):
+        spread = OracleSpread(orc, kv, ctx + i, embed[tok], seed=i)
         o = orc.decode_step(kv, ctx + i, token=tok, want_trace=True)
         g_logits, g_next, g_hidden = _gpu_step(eng, tok=[tok])
-        same = True
-        for l in range(cfg.n_layers):
-            gi, _ = eng.routing(l)
-            sc = o["trace"]["router_score"][l]
-            if not topk_ok(gi[0], o["trace"]["topk_idx"][l], sc, 8):
-                assert _admissible(gi[0], o["trace"]["topk_idx"][l], sc, 8), f"step {i} layer {l}"
-                same = False
-        if same:
-            chk.add(g_logits[0], o["logits"], g_next[0], o["token"], g_hidden[0], o["hidden"])
+        if _check_chained_step(eng, o, spread, g_logits, g_next, g_hidden, cfg.n_layers, f"step {i}"):
+            compared += 1
         else:
             diverged += 1
         tok = o["token"]
-    chk.assert_ok(logit_abs=CHAIN_LOGIT_ABS, hidden_rel=CHAIN_HIDDEN_REL)
-    print(f"chained: {chk.steps} compared steps, {diverged} diverged at near-ties, "
-          f"max logit err {chk.max_logit_err:.3e}, max hidden rel {chk.max_hidden_rel:.3e}")
+    print(f"chained: {compared} compared steps, {diverged} diverged at near-ties")
 
 
 def test_moe8_token_prefill(moe8):
@@ -334,16 +366,8 @@ def test_moe8_token_prefill(moe8):
         tol = 1e-2 if l == 0 else CHAIN_KV_REL  # layer 0 sees the embeddings directly
         assert rel_l2(bf16_to_f64(t_bits(kg)), bf16_to_f64(kv["k"][l, :, :3])) < tol, l
         assert rel_l2(bf16_to_f64(t_bits(vg)), bf16_to_f64(kv["v"][l, :, :3])) < tol, l
+    embed = m_cpu["embed"].view(torch.int16).numpy().view(np.uint16)
+    spread = OracleSpread(orc, kv, 3, embed[first["token"]], seed=3)
     o = orc.decode_step(kv, 3, token=first["token"], want_trace=True)
     g_logits, g_next, g_hidden = _gpu_step(eng, tok=[first["token"]])
-    same = True
-    for l in range(cfg.n_layers):
-        gi, _ = eng.routing(l)
-        sc = o["trace"]["router_score"][l]
-        if not topk_ok(gi[0], o["trace"]["topk_idx"][l], sc, 8):
-            assert _admissible(gi[0], o["trace"]["topk_idx"][l], sc, 8)
-            same = False
-    if same:
-        chk = StepCheck()
-        chk.add(g_logits[0], o["logits"], g_next[0], o["token"], g_hidden[0], o["hidden"])
-        chk.assert_ok(logit_abs=CHAIN_LOGIT_ABS, hidden_rel=CHAIN_HIDDEN_REL)
+    _check_chained_step(eng, o, spread, g_logits, g_next, g_hidden, cfg.n_layers, "after token prefill")
