@@ -12,10 +12,15 @@ constexpr int kTileRows = 128;
 constexpr int kTileK = 128;
 constexpr int kTileData = kTileRows * kTileK;  // 16384
 constexpr int kTileBytes = kTileData + 16;     // 16400
-constexpr int kSlotBytes = kTileBytes;         // one ring slot holds one weight tile or one KV tile
+// One ring slot holds two consecutive weight tiles of a CTA's share (or one KV tile of 64
+// positions): each slot is one bulk-copy hand-off, and on this GPU the streaming rate of one SM
+// grows with the bytes per hand-off up to ~32 KB (16 KB slots streamed ~4.3 TB/s in total,
+// 32 KB slots ~7.0 TB/s).
+constexpr int kSlotTiles = 2;
+constexpr int kSlotBytes = kSlotTiles * kTileBytes;  // 32800
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kKvTilePos = 32;                       // KV positions per ring slot
+constexpr int kKvTilePos = 64;                       // KV positions per ring slot
 constexpr int kMaxBatch = 8;
 constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
 constexpr int kBarTrace = 64;                        // grid barriers whose per-CTA arrival times are kept

@@ -603,8 +603,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     KernelFn k = kernel_for(bm, e->hd, e->group);
     if (!k) return bail(DEC_ERR_UNSUPPORTED);
     int ring = 16;
-    while (ring >= 4 && smem_layout(ring, bm, p.xmax, e->hd, e->group).total > max_optin) --ring;
-    if (ring < 4) return bail(fail(e, DEC_ERR_UNSUPPORTED, "shared memory too small for the ring"));
+    while (ring >= 3 && smem_layout(ring, bm, p.xmax, e->hd, e->group).total > max_optin) --ring;
+    if (ring < 3) return bail(fail(e, DEC_ERR_UNSUPPORTED, "shared memory too small for the ring"));
     const int smem = smem_layout(ring, bm, p.xmax, e->hd, e->group).total;
     ce = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaFuncSetAttribute"));

@@ -64,7 +64,7 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   s.empty_off = s.full_off + ring * 8;
   s.xs_off = align_up(s.empty_off + ring * 8, 128);
   s.red_off = align_up(s.xs_off + bm * xmax * 2, 128);
-  int red_gemv = kConsumerWarps * kTileRows * bm * 4;
+  int red_gemv = 2 * kTileRows * bm * 4;
   int red_attn = kConsumerWarps * group * (hd + 2) * 4;
   int red_fin = (bm * kTileRows + kListCap + 16) * 4;
   int red = red_gemv > red_attn ? red_gemv : red_attn;
@@ -137,6 +137,34 @@ __device__ __forceinline__ const uint8_t* tile_addr(const KParams& p, const Laye
   }
 }
 
+// Walks a stage's tiles in order: the address of tile t, then of t + 1, ... Expert stages keep
+// the (expert, tile within expert) pair instead of dividing t by the tiles per expert.
+struct TileCursor {
+  const uint8_t* addr;
+  int u, r;  // expert stages: expert slot and tile within it
+  __device__ __forceinline__ void next(const KParams& p, const LayerDev& Ld, int kind, const StageGeo& g, int U,
+                                       const int* elist) {
+    if (kind == K_RTGU || kind == K_D) {
+      if (++r == g.tpe) {
+        r = 0;
+        ++u;
+        // past the stage's last expert there is no next tile (the caller stops before using it)
+        if (u < g.T / g.tpe) addr = tile_addr(p, Ld, kind, u * g.tpe, g, U, elist);
+        return;
+      }
+    }
+    addr += kTileBytes;
+  }
+};
+__device__ __forceinline__ TileCursor tile_cursor(const KParams& p, const LayerDev& Ld, int kind, int t,
+                                                  const StageGeo& g, int U, const int* elist) {
+  TileCursor c;
+  c.u = g.tpe > 0 ? t / g.tpe : 0;
+  c.r = t - c.u * g.tpe;
+  c.addr = tile_addr(p, Ld, kind, t, g, U, elist);
+  return c;
+}
+
 // attention work units: (sequence b, KV head g, context chunk c)
 struct AttnUnit {
   int b, g, c, tile0, tile1, T;
@@ -169,7 +197,9 @@ struct Producer {
   uint64_t* full;
   uint64_t* empty;
   Misc* m;
-  unsigned item = 0;
+  unsigned item = 0;  // slots issued so far in this step
+  int pslot = 0;      // ring slot of the next item (item % ring, kept without divisions)
+  unsigned plap = 0;  // times the ring has wrapped (item / ring)
   bool dead = false;
   int stamp = 0;
 
@@ -197,15 +227,21 @@ struct Producer {
 
   // claim the next slot: wait until the consumers released it
   __device__ bool claim(int& slot) {
-    slot = item % p.ring;
-    if (item >= (unsigned)p.ring) {
-      unsigned par = ((item / p.ring) - 1) & 1;
-      if (!mbar_wait(&empty[slot], par, p, 10)) {
+    slot = pslot;
+    if (plap > 0) {
+      if (!mbar_wait(&empty[slot], (plap - 1) & 1, p, 10)) {
         dead = true;
         return false;
       }
     }
     return true;
+  }
+  __device__ __forceinline__ void advance() {
+    ++item;
+    if (++pslot == p.ring) {
+      pslot = 0;
+      ++plap;
+    }
   }
 
   __device__ void issue_gemv(int kind, int l, int U, const int* elist) {
@@ -215,19 +251,38 @@ struct Producer {
     const int t0 = range_lo(g.T, blockIdx.x, G_), t1 = range_lo(g.T, blockIdx.x + 1, G_);
     const LayerDev& Ld = p.layers[l < p.L ? l : 0];
     if (t1 > t0) trace(kind << 4);
-    for (int t = t0; t < t1; ++t) {
+    // a slot takes the next kSlotTiles tiles of the CTA's range (fewer at its end): one copy when
+    // they are adjacent in memory, one per tile otherwise (an expert boundary). The tile address
+    // is advanced tile by tile (no divisions in the loop).
+    TileCursor cur = tile_cursor(p, Ld, kind, t0, g, U, elist);
+    for (int t = t0; t < t1; t += kSlotTiles) {
       int slot;
       if (!claim(slot)) return;
-      const uint8_t* src = tile_addr(p, Ld, kind, t, g, U, elist);
+      const int n = min(kSlotTiles, t1 - t);
+      const uint8_t* src[kSlotTiles];
+      bool ok = true;
+#pragma unroll
+      for (int j = 0; j < kSlotTiles; ++j) {
+        src[j] = nullptr;
+        if (j < n) {
+          src[j] = cur.addr;
+          ok = ok && in_range(src[j], kTileBytes, p.warena, p.warena_bytes, 30);
+          cur.next(p, Ld, kind, g, U, elist);
+        }
+      }
       uint8_t* dst = ring + (size_t)slot * kSlotBytes;
-      if (!in_range(src, kTileBytes, p.warena, p.warena_bytes, 30)) {
+      if (!ok) {
         mbar_arrive(&full[slot]);  // keep the ring consistent; the status word stops the step
-        ++item;
+        advance();
         continue;
       }
-      mbar_arrive_expect_tx(&full[slot], kTileBytes);
-      bulk_g2s(dst, src, kTileBytes, &full[slot]);
-      ++item;
+      mbar_arrive_expect_tx(&full[slot], (unsigned)n * kTileBytes);
+      if (n == 2 && src[1] == src[0] + kTileBytes) {
+        bulk_g2s(dst, src[0], 2 * kTileBytes, &full[slot]);
+      } else {
+        for (int j = 0; j < n; ++j) bulk_g2s(dst + (size_t)j * kTileBytes, src[j], kTileBytes, &full[slot]);
+      }
+      advance();
     }
     if (t1 > t0) trace(kind << 4 | 1);
   }
@@ -248,13 +303,13 @@ struct Producer {
         if (n < 1 || n > kKvTilePos || !in_range(p.kc + r0, n * row_bytes, p.kc, p.kv_bytes, 31) ||
             !in_range(p.vc + r0, n * row_bytes, p.vc, p.kv_bytes, 32)) {
           mbar_arrive(&full[slot]);
-          ++item;
+          advance();
           continue;
         }
         mbar_arrive_expect_tx(&full[slot], 2u * n * row_bytes);
         bulk_g2s(dst, p.kc + r0, n * row_bytes, &full[slot]);
         bulk_g2s(dst + kKvTilePos * row_bytes, p.vc + r0, n * row_bytes, &full[slot]);
-        ++item;
+        advance();
       }
     }
   }
@@ -322,7 +377,9 @@ struct Consumer {
   uint16_t* xs;
   float* red;
   Misc* m;
-  unsigned item = 0;
+  unsigned item = 0;  // slots consumed so far in this step
+  int rslot = 0;      // ring slot of the next item (item % ring, kept without divisions)
+  unsigned rpar = 0;  // its full-barrier phase parity ((item / ring) & 1)
   bool dead = false;
   int warp, lane, tid;
   int stamp = 0;
@@ -370,21 +427,23 @@ struct Consumer {
     return ok;
   }
 
-  // Every consumer warp walks the same item sequence; item i is consumed by warp i % 8 alone,
-  // so eight tiles are in flight across the warps of a CTA.
-  __device__ bool mine() const { return (item % kConsumerWarps) == (unsigned)warp; }
+  // Every consumer warp walks the same item sequence and takes part in every item (a GEMV tile
+  // or a KV tile): a slot's "empty" barrier expects one arrival per consumer warp.
   __device__ const uint8_t* wait_item() {
-    int slot = item % p.ring;
     if (!dead) {
-      if (!mbar_wait(&full[slot], (item / p.ring) & 1, p, 20)) dead = true;
+      if (!mbar_wait(&full[rslot], rpar, p, 20)) dead = true;
     }
-    return ring + (size_t)slot * kSlotBytes;
+    return ring + (size_t)rslot * kSlotBytes;
   }
-  // A slot's "empty" barrier expects kConsumerWarps arrivals: a GEMV tile's owner arrives for all
-  // of them at once, a KV tile (shared by all warps) gets one arrival per warp.
-  __device__ void release_item(unsigned count = kConsumerWarps) {
+  // release the current item's slot and move to the next item
+  __device__ void release_item() {
     __syncwarp();
-    if (lane == 0) mbar_arrive_cnt(&empty[item % p.ring], count);
+    if (lane == 0) mbar_arrive(&empty[rslot]);
+    ++item;
+    if (++rslot == p.ring) {
+      rslot = 0;
+      rpar ^= 1;
+    }
   }
 
   // -------- activation staging --------
@@ -505,51 +564,48 @@ struct Consumer {
 
   // -------- split-K GEMV over one stage --------
 
-  // One warp consumes a whole 128x128 tile: lane l owns rows l, l+32, l+64, l+96 and walks the
-  // 128 columns in eight 16-byte chunks (the repacked tile stores chunk c of row 32r + l at
-  // 16 * ((4c + r) * 32 + l), so every shared-memory load is conflict-free). The activation chunk
-  // is the same for all lanes (a broadcast load). E4M3 pairs become f16 pairs exactly (CUDA's
-  // cvt); each product is then formed and accumulated in fp32 by one mixed-precision FMA
-  // (f16 x f16 + f32, one rounding, as converting both operands to fp32 first would give).
-  // The tile's block scale (rows 0..63 / 64..127) multiplies the tile sum.
-  __device__ __forceinline__ void tile_dot(const uint8_t* tile, int xoff, const float* gmul,
-                                           float (&acc)[4][BM]) {
+  // All eight consumer warps share each 128x128 tile, so a slot is held for an eighth of the
+  // time one warp would need and most of the ring stays in flight. Warp w takes rows
+  // 32 * (w & 3) + lane (lane = its row) and the column chunks 4 * (w >> 2) .. + 3 (the repacked
+  // tile stores the 16-byte chunk c of row 32r + l at 16 * ((4c + r) * 32 + l): each load of a
+  // warp reads 512 contiguous bytes, conflict-free). The activation chunk is the same for all
+  // lanes (a broadcast load). E4M3 pairs become f16 pairs exactly (CUDA's cvt); each product is
+  // then formed and accumulated in fp32 by one mixed-precision FMA (f16 x f16 + f32, one
+  // rounding, as converting both operands to fp32 first would give). The tile's block scale
+  // (rows 0..63 / 64..127) multiplies the tile sum.
+  __device__ __forceinline__ void tile_dot(const uint8_t* tile, int xoff, const float* gmul, float (&acc)[BM]) {
+    const int r = warp & 3, c0 = (warp >> 2) * 4;
     const float2 sc = *reinterpret_cast<const float2*>(tile + kTileData);
-    float part[4][BM][2];  // two FMA chains per (row, token)
+    const float s_r = r < 2 ? sc.x : sc.y;
+    float part[BM][2];  // two FMA chains per token
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int b = 0; b < BM; ++b) part[b][0] = part[b][1] = 0.f;
+    uint4 wv[4];
 #pragma unroll
-      for (int b = 0; b < BM; ++b) part[r][b][0] = part[r][b][1] = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint4 wv[4];
+    for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(tile + ((((c0 + c) * 4 + r) * 32 + lane) << 4));
 #pragma unroll
-      for (int r = 0; r < 4; ++r) wv[r] = *reinterpret_cast<const uint4*>(tile + (((c * 4 + r) * 32 + lane) << 4));
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t* u = reinterpret_cast<const uint32_t*>(&wv[c]);
+      uint32_t wh[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wh[2 * j] = e4m3x2_to_f16x2(u[j]);
+        wh[2 * j + 1] = e4m3x2_to_f16x2(u[j] >> 16);
+      }
 #pragma unroll
       for (int b = 0; b < BM; ++b) {
         if (b < p.B) {
-          const uint16_t* xp = xs + (size_t)b * p.xmax + xoff + c * 16;
+          const uint16_t* xp = xs + (size_t)b * p.xmax + xoff + (c0 + c) * 16;
           const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
           const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 8);
           const uint32_t xh[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const uint32_t* u = reinterpret_cast<const uint32_t*>(&wv[r]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              fma_f16x2_f32(e4m3x2_to_f16x2(u[j]), xh[2 * j], part[r][b][0], part[r][b][1]);
-              fma_f16x2_f32(e4m3x2_to_f16x2(u[j] >> 16), xh[2 * j + 1], part[r][b][0], part[r][b][1]);
-            }
-          }
+          for (int j = 0; j < 8; ++j) fma_f16x2_f32(wh[j], xh[j], part[b][0], part[b][1]);
         }
       }
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float s_r = r < 2 ? sc.x : sc.y;
-#pragma unroll
-      for (int b = 0; b < BM; ++b) acc[r][b] = fmaf(s_r * gmul[b], part[r][b][0] + part[r][b][1], acc[r][b]);
-    }
+    for (int b = 0; b < BM; ++b) acc[b] = fmaf(s_r * gmul[b], part[b][0] + part[b][1], acc[b]);
   }
 
   __device__ float* part_base(int kind) const {
@@ -585,22 +641,17 @@ struct Consumer {
     return kind == K_QKV ? p.cnt_qkv + (size_t)l * p.n_rb_qkv : p.cnt_o + (size_t)l * p.n_rb_d;
   }
 
-  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, float (&acc)[4][BM]) {
-    // red[w][row][b]
+  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, float (&acc)[BM]) {
+    // red[column half][row][b]: warp w holds row 32 * (w & 3) + lane of column half w >> 2
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int b = 0; b < BM; ++b) red[((size_t)warp * kTileRows + i * 32 + lane) * BM + b] = acc[i][b];
+    for (int b = 0; b < BM; ++b) red[((size_t)(warp >> 2) * kTileRows + (warp & 3) * 32 + lane) * BM + b] = acc[b];
     cons_sync();
     const int a = seg * g.kbs;
     const int slot = contrib_slot(blockIdx.x, first_tile, a, g.T, gridDim.x);
     float* dst = part_base(kind) + ((size_t)seg * g.kbs + slot) * p.MB * kTileRows;
     for (int idx = tid; idx < p.B * kTileRows; idx += kConsumerWarps * 32) {
       const int b = idx / kTileRows, row = idx % kTileRows;
-      float s = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) s += red[((size_t)w * kTileRows + row) * BM + b];
-      dst[(size_t)b * kTileRows + row] = s;
+      dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
     }
     __threadfence();
     cons_sync();
@@ -685,34 +736,48 @@ struct Consumer {
     cons_sync();
     trace(kind << 4);
     float gmul[BM];
-    float acc[4][BM];
+    float acc[BM];
     int seg_cur = -1, seg_first = 0;
+    const uint8_t* slot_base = ring;
+    // position of tile t, advanced without divisions: segment, k block within it, and for the
+    // down projection the expert (whose gates scale the tile) and the tile within the expert
+    int seg = t1 > t0 ? t0 / g.kbs : 0, kb = t0 - seg * g.kbs;
+    int v = 0, rv = 0, xbase = 0;
+#pragma unroll
+    for (int b = 0; b < BM; ++b) gmul[b] = 1.f;
+    if (kind == K_D && t1 > t0) {
+      v = t0 / g.tpe;
+      rv = t0 - v * g.tpe;
+      xbase = (v - m->v_lo) * p.inter;
+#pragma unroll
+      for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
+    }
+    int j = 0;  // tile j of the current slot (the producer packs kSlotTiles consecutive tiles per slot)
     for (int t = t0; t < t1; ++t) {
-      const int seg = t / g.kbs;
       if (seg != seg_cur) {
         if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, acc);
         seg_cur = seg;
         seg_first = t;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int b = 0; b < BM; ++b) acc[i][b] = 0.f;
+        for (int b = 0; b < BM; ++b) acc[b] = 0.f;
       }
-      int xoff = (t % g.kbs) * kTileK;
-#pragma unroll
-      for (int b = 0; b < BM; ++b) gmul[b] = 1.f;
-      if (kind == K_D) {
-        const int v = t / g.tpe;
-        xoff += (v - m->v_lo) * p.inter;
+      if (j == 0) slot_base = wait_item();
+      if (!dead) tile_dot(slot_base + (size_t)j * kTileBytes, xbase + kb * kTileK, gmul, acc);
+      if (++j == kSlotTiles || t == t1 - 1) {
+        release_item();
+        j = 0;
+      }
+      if (++kb == g.kbs) {
+        kb = 0;
+        ++seg;
+      }
+      if (kind == K_D && ++rv == g.tpe) {
+        rv = 0;
+        ++v;
+        xbase = (v - m->v_lo) * p.inter;
 #pragma unroll
         for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
       }
-      if (mine()) {
-        const uint8_t* tile = wait_item();
-        if (!dead) tile_dot(tile, xoff, gmul, acc);
-        release_item();
-      }
-      ++item;
     }
     cons_sync();
     trace(kind << 4 | 1);
@@ -1084,7 +1149,8 @@ struct Consumer {
 
   __device__ void attn_stage(int l) {
     constexpr int DPL = HD / 32;       // dims per lane
-    constexpr int PPW = kKvTilePos / kConsumerWarps;  // positions per warp in a KV tile (4)
+    constexpr int PPW = kKvTilePos / kConsumerWarps;  // positions per warp in a KV tile (8)
+    static_assert(2 * kKvTilePos * HD * 2 <= kSlotBytes, "a KV tile (K and V rows) must fit one slot");
     constexpr int NV = PPW * G;                        // scores per warp per tile
     static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "scores per warp must be a power of two <= 32");
     constexpr int LPV = 32 / NV;                       // lanes holding each reduced score
@@ -1196,8 +1262,7 @@ struct Consumer {
             }
           }
         }
-        release_item(1);
-        ++item;
+        release_item();
       }
       cons_sync();
       trace(7 << 4 | 1);
