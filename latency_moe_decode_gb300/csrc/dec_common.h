@@ -23,7 +23,9 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kKvTilePos = 64;                       // KV positions per ring slot
 constexpr int kMaxBatch = 8;
 constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
-constexpr int kBarTrace = 64;                        // grid barriers whose per-CTA arrival times are kept
+constexpr int kStampsPerLayer = 16;                  // per-CTA dependency time stamps of a layer
+constexpr int kStampLayers = 8;                      // layers whose stamps are kept
+constexpr int kBarTrace = kStampsPerLayer * kStampLayers;  // per-CTA stamp words per CTA
 
 // Device error codes (low byte) -- the upper bytes carry where it happened.
 enum : int {

@@ -77,6 +77,25 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
 // GEMV stage kinds
 enum Kind : int { K_QKV = 0, K_O, K_ROUTER, K_SHGU, K_RTGU, K_D, K_LM };
 
+// per-CTA dependency stamps of a layer (trace words from kTraceSlots on)
+enum Stamp : int {
+  S_QKV_TILES = 0,  // q/k/v tiles consumed
+  S_QKV_DONE,       // q/k/v partials published
+  S_ATTN_DONE,      // the CTA's attention units merged
+  S_OGRP_READY,     // the attention outputs its projection tiles read are final
+  S_O_TILES,        // output-projection tiles consumed
+  S_O_DONE,         // output-projection partials published
+  S_XMID_READY,     // x_mid summed and normalised
+  S_FFN_PRE_DONE,   // router and shared-expert gate/up done
+  S_ROUTED,         // routing known
+  S_GU_TILES,       // routed (or dense) gate/up tiles consumed
+  S_GU_DONE,        // gate/up partials published, SwiGLU finalisers run
+  S_H_READY,        // the SwiGLU rows its down tiles read are final
+  S_D_TILES,        // down-projection tiles consumed
+  S_D_DONE,         // down partials published, finalisers run
+  S_BARRIER,        // layer barrier passed
+};
+
 // ---------------------------------------------------------------------------------------------
 // schedule arithmetic shared by producer and consumers
 
@@ -341,26 +360,38 @@ struct Producer {
     }
   }
 
+  // The load program: per layer q/k/v, KV tiles, output projection, router, shared expert,
+  // (routing) routed gate/up, down; then the LM head. Every GEMV stage goes through the one
+  // issue_gemv call below, so its code exists once in the kernel.
   __device__ void run() {
     int elist[kMaxExperts];
-    for (int l = 0; l < p.L; ++l) {
-      issue_gemv(K_QKV, l, 0, nullptr);
-      issue_attn(l);
-      issue_gemv(K_O, l, 0, nullptr);
-      if (p.dense) {
-        issue_gemv(K_SHGU, l, 0, nullptr);
-        issue_gemv(K_D, l, 0, nullptr);
-      } else {
-        issue_gemv(K_ROUTER, l, 0, nullptr);
-        if (p.nsh) issue_gemv(K_SHGU, l, 0, nullptr);
-        int U = 0;
-        if (!routing(l, U, elist)) break;
-        issue_gemv(K_RTGU, l, U, elist);
-        issue_gemv(K_D, l, U, elist);
+    int U = 0;
+#pragma unroll 1
+    for (int l = 0; l <= p.L && !dead; ++l) {
+      const bool lm = l == p.L;
+#pragma unroll 1
+      for (int ph = 0; ph < 6 && !dead; ++ph) {
+        int kind = -1;
+        if (lm) {
+          if (ph == 0 && p.V > 0) kind = K_LM;
+        } else {
+          switch (ph) {
+            case 0: kind = K_QKV; break;
+            case 1: issue_attn(l); kind = K_O; break;
+            case 2: U = 0; kind = p.dense ? K_SHGU : K_ROUTER; break;
+            case 3: kind = (!p.dense && p.nsh) ? K_SHGU : -1; break;
+            case 4:
+              if (!p.dense) {
+                if (!routing(l, U, elist)) break;
+                kind = K_RTGU;
+              }
+              break;
+            default: kind = K_D; break;
+          }
+        }
+        if (kind >= 0) issue_gemv(kind, lm ? 0 : l, U, elist);
       }
-      if (dead) break;
     }
-    if (!dead && p.V > 0) issue_gemv(K_LM, 0, 0, nullptr);
     if (dead) drain();
   }
 };
@@ -386,7 +417,6 @@ struct Consumer {
   int nflush = 0;   // segments flushed in the current stage
   int pend = -1;    // pending counter arrival owned by this lane (warp 0 only)
   unsigned nbar = 0;  // grid barriers passed in this step
-  int nstamp = 0;     // per-CTA dependency stamps written in this step
 
   __device__ Consumer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint16_t* x, float* rd,
                       Misc* m_)
@@ -407,10 +437,10 @@ struct Consumer {
     }
   }
 
-  // every CTA's time at the k-th dependency point of the step (k < kBarTrace)
-  __device__ void cta_stamp() {
-    if (tid == 0 && nstamp < kBarTrace) p.trace[kTraceSlots + (size_t)nstamp * gridDim.x + blockIdx.x] = gtimer();
-    ++nstamp;
+  // every CTA's time at dependency point k (a Stamp) of layer l < kStampLayers
+  __device__ void cta_stamp(int l, int k) {
+    if (tid == 0 && l < kStampLayers)
+      p.trace[kTraceSlots + ((size_t)l * kStampsPerLayer + k) * gridDim.x + blockIdx.x] = gtimer();
   }
 
   __device__ bool gsync(int where) {
@@ -468,6 +498,13 @@ struct Consumer {
         return count_reached(cnt + rb, (int)p.epoch * n_contrib(rb * go.kbs, go.kbs, go.T, gridDim.x));
       }, 18);
     }
+    // the norm weights of this thread's chunks, loaded once, in flight with the first activations
+    uint4 wv[MAXV];
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+      const int k = (tid + j * kConsumerWarps * 32) * 8;
+      if (k < p.d) wv[j] = __ldg(reinterpret_cast<const uint4*>(w + k));
+    }
     for (int b = 0; b < p.B; ++b) {
       const uint16_t* src = direct ? direct + (size_t)b * p.d : x_in(l_src, b);
       uint4 v[MAXV];
@@ -477,18 +514,57 @@ struct Consumer {
         if (k < p.d) v[j] = ldcg4(src + k);
       }
       if (from_o) {
+        // the output projection's partials of this thread's chunks: two chunks at a time, four
+        // contributors per batch, every load of a batch in flight before any is added (one L2
+        // round trip per batch); each row is summed in contributor order
+        const size_t st = (size_t)p.MB * kTileRows;
 #pragma unroll
-        for (int j = 0; j < MAXV; ++j) {
-          const int k = (tid + j * kConsumerWarps * 32) * 8;
-          if (k < p.d) {
-            float o8[8];
-            seg_sum8(K_O, go, k / kTileRows, b, k % kTileRows, o8);
-            uint32_t* u = reinterpret_cast<uint32_t*>(&v[j]);
+        for (int jp = 0; jp < MAXV; jp += 2) {
+          if ((tid + jp * kConsumerWarps * 32) * 8 >= p.d) break;
+          float o8[2][8];
+          int nc[2];
+          const float* base[2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint16_t lo = f2bf(bf16lo(u[q]) + o8[2 * q]);
-              const uint16_t hi = f2bf(bf16hi(u[q]) + o8[2 * q + 1]);
-              u[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+          for (int jj = 0; jj < 2; ++jj) {
+            const int k = (tid + (jp + jj) * kConsumerWarps * 32) * 8;
+            const int rb = k / kTileRows;
+            nc[jj] = k < p.d ? n_contrib(rb * go.kbs, go.kbs, go.T, gridDim.x) : 0;
+            base[jj] = p.part_o + (size_t)rb * go.kbs * st + (size_t)b * kTileRows + k % kTileRows;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[jj][e] = 0.f;
+          }
+          const int ncm = max(nc[0], nc[1]);
+          for (int c0 = 0; c0 < ncm; c0 += 4) {
+            float4 t[2][4][2];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                if (c0 + c < nc[jj]) {
+                  t[jj][c][0] = __ldcg(reinterpret_cast<const float4*>(base[jj] + (size_t)(c0 + c) * st));
+                  t[jj][c][1] = __ldcg(reinterpret_cast<const float4*>(base[jj] + (size_t)(c0 + c) * st + 4));
+                } else {
+                  t[jj][c][0] = t[jj][c][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+              }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                o8[jj][0] += t[jj][c][0].x; o8[jj][1] += t[jj][c][0].y; o8[jj][2] += t[jj][c][0].z; o8[jj][3] += t[jj][c][0].w;
+                o8[jj][4] += t[jj][c][1].x; o8[jj][5] += t[jj][c][1].y; o8[jj][6] += t[jj][c][1].z; o8[jj][7] += t[jj][c][1].w;
+              }
+          }
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            if ((tid + (jp + jj) * kConsumerWarps * 32) * 8 < p.d) {
+              uint32_t* u = reinterpret_cast<uint32_t*>(&v[jp + jj]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint16_t lo = f2bf(bf16lo(u[q]) + o8[jj][2 * q]);
+                const uint16_t hi = f2bf(bf16hi(u[q]) + o8[jj][2 * q + 1]);
+                u[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+              }
             }
           }
         }
@@ -518,11 +594,13 @@ struct Consumer {
 #pragma unroll
       for (int wi = 0; wi < kConsumerWarps; ++wi) ss += m->rsum[wi][b];
       const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
-      for (int k = tid * 8; k < p.d; k += kConsumerWarps * 32 * 8) {
+#pragma unroll
+      for (int j = 0; j < MAXV; ++j) {
+        const int k = (tid + j * kConsumerWarps * 32) * 8;
+        if (k >= p.d) break;
         const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)b * p.xmax + k);
-        const uint4 wv = *reinterpret_cast<const uint4*>(w + k);
         const uint32_t* u = reinterpret_cast<const uint32_t*>(&xv);
-        const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv);
+        const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv[j]);
         uint4 o;
         uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
@@ -653,11 +731,15 @@ struct Consumer {
       const int b = idx / kTileRows, row = idx % kTileRows;
       dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
     }
-    __threadfence();
+    // The CTA barrier orders every thread's partial before the arriving thread's fence and
+    // counter update (one fence per arrival; the other warps move on at once).
     cons_sync();
     if (kind == K_QKV || kind == K_O) {
       // published partials: the readers wait for every contributor of the row block
-      if (tid == 0 && !dead) atomicAdd(pub_counter(kind, l) + seg, 1);
+      if (tid == 0 && !dead) {
+        __threadfence();
+        atomicAdd(pub_counter(kind, l) + seg, 1);
+      }
       return;
     }
     // Arrive on the output group's counter. The result is only needed at the end of the stage,
@@ -666,6 +748,7 @@ struct Consumer {
     const int grp = seg_group(kind, seg);
     if (warp == 0 && lane == (n & 31)) {
       if (n >= 32) m->fin_old[n - 32] = pend;  // more than 32 segments: retire the older one
+      if (!dead) __threadfence();
       pend = dead ? -1 : atom_add_acqrel(cnt_base(kind) + grp, 1);
     }
     if (tid == 0) {
@@ -700,6 +783,28 @@ struct Consumer {
       for (int j = 0; j < 8; ++j) s += v[j];
     }
     return s;
+  }
+
+  // seg_sum of two rows of one segment, with both rows' loads of a batch in flight together
+  __device__ __forceinline__ void seg_sum2(int kind, const StageGeo& g, int seg, int b, int r0, int r1, float& s0,
+                                           float& s1) const {
+    const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
+    const float* src = part_base(kind) + (size_t)seg * g.kbs * p.MB * kTileRows + (size_t)b * kTileRows;
+    const size_t st = (size_t)p.MB * kTileRows;
+    s0 = s1 = 0.f;
+    for (int c0 = 0; c0 < nc; c0 += 8) {
+      float v0[8], v1[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v0[j] = (c0 + j < nc) ? ldcg(src + (size_t)(c0 + j) * st + r0) : 0.f;
+        v1[j] = (c0 + j < nc) ? ldcg(src + (size_t)(c0 + j) * st + r1) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        s0 += v0[j];
+        s1 += v1[j];
+      }
+    }
   }
 
   // eight consecutive rows of one segment, all contributor slots loaded together
@@ -753,9 +858,19 @@ struct Consumer {
       for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
     }
     int j = 0;  // tile j of the current slot (the producer packs kSlotTiles consecutive tiles per slot)
-    for (int t = t0; t < t1; ++t) {
-      if (seg != seg_cur) {
+    for (int t = t0;; ++t) {
+      // a segment ends at a segment boundary or at the end of the range (one flush call site)
+      if (t == t1 || seg != seg_cur) {
+        if (t == t1) {
+          cons_sync();
+          trace(kind << 4 | 1);
+          if (kind == K_QKV) cta_stamp(l, S_QKV_TILES);
+          if (kind == K_O) cta_stamp(l, S_O_TILES);
+          if (kind == K_RTGU || (kind == K_SHGU && p.dense)) cta_stamp(l, S_GU_TILES);
+          if (kind == K_D) cta_stamp(l, S_D_TILES);
+        }
         if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, acc);
+        if (t == t1) break;
         seg_cur = seg;
         seg_first = t;
 #pragma unroll
@@ -779,9 +894,6 @@ struct Consumer {
         for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
       }
     }
-    cons_sync();
-    trace(kind << 4 | 1);
-    if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, acc);
     const int nf = min(nflush, kMaxSegs);
     if (warp == 0 && lane < min(nflush, 32)) {
       const int slot = nflush > 32 && lane < nflush - 32 ? lane + 32 : lane;
@@ -793,7 +905,8 @@ struct Consumer {
       const int grp = m->fin_group[f];
       const int old = m->fin_old[f];
       if (old < 0 || old + 1 != group_expected(kind, g, grp)) continue;
-      __threadfence();
+      // this CTA's acquiring arrival completed the group; the CTA barriers since then order the
+      // finaliser's reads after every contributor's publication
       finalize(kind, l, g, grp, U);
       cons_sync();
       if (tid == 0) atomicExch(cnt_base(kind) + grp, 0);
@@ -879,9 +992,11 @@ struct Consumer {
           const int e = sel[b * 16 + k];
           p.rt_gate[(size_t)b * kMaxExperts + (mark[e] - 1)] = sg[b * 16 + k];
         }
-        __threadfence();
         cons_sync();
-        if (tid == 0) st_release(p.rt_flag + l, p.epoch);
+        if (tid == 0) {
+          __threadfence();
+          st_release(p.rt_flag + l, p.epoch);
+        }
         break;
       }
       case K_SHGU:
@@ -895,8 +1010,8 @@ struct Consumer {
         }
         for (int idx = tid; idx < p.B * half; idx += 256) {
           int b = idx / half, i = idx % half;
-          float gv = seg_sum(kind, g, seg, b, i);
-          float uv = seg_sum(kind, g, seg, b, i + half);
+          float gv, uv;
+          seg_sum2(kind, g, seg, b, i, i + half, gv, uv);
           float h = (gv / (1.0f + expf(-gv))) * uv;
           int j = rb * half + i;
           if (kind == K_SHGU)
@@ -904,9 +1019,9 @@ struct Consumer {
           else
             p.hrt[((size_t)u * p.MB + b) * p.inter + j] = f2bf(h);
         }
-        __threadfence();
         cons_sync();
         if (tid == 0) {
+          __threadfence();
           const int slot = kind == K_SHGU ? p.umax : u;
           st_release(p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch);
         }
@@ -914,40 +1029,69 @@ struct Consumer {
       }
       case K_D: {
         const int nv = g.T / g.tpe;
-        // every expert's contributor slots for this row block, as offsets into the partials
+        // every expert's contributor slots for this row block, as offsets into the partials:
+        // warp 0 lane v counts expert v's contributors, a prefix sum places them
         int* list = reinterpret_cast<int*>(tmp + BM * kTileRows);
         int* nlist = list + kListCap;
-        if (tid == 0) {
-          int n = 0;
-          for (int v = 0; v < nv; ++v) {
+        if (warp == 0) {
+          int base = 0;
+          for (int v0 = 0; v0 < nv; v0 += 32) {
+            const int v = v0 + lane;
             const int seg = v * p.n_rb_d + grp;
-            const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
-            for (int c = 0; c < nc; ++c) {
-              if (n < kListCap) list[n] = (seg * g.kbs + c) * p.MB * kTileRows;
-              ++n;
+            const int nc = v < nv ? n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x) : 0;
+            int incl = nc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
             }
+            const int first = base + incl - nc;
+            for (int c = 0; c < nc; ++c)
+              if (first + c < kListCap) list[first + c] = (seg * g.kbs + c) * p.MB * kTileRows;
+            base += __shfl_sync(0xffffffffu, incl, 31);
           }
-          if (n > kListCap) {
-            raise_err(p, kDevBadArg, 3);
-            n = kListCap;
+          if (lane == 0) {
+            if (base > kListCap) raise_err(p, kDevBadArg, 3);
+            *nlist = min(base, kListCap);
           }
-          *nlist = n;
         }
         cons_sync();
         const int nl = *nlist;
+        const StageGeo go = stage_geo(p, K_O, 0);
+        const int nco = n_contrib(grp * go.kbs, go.kbs, go.T, gridDim.x);
+        const size_t ost = (size_t)p.MB * kTileRows;
         for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
           int b = idx / kTileRows, i = idx % kTileRows;
           int r = grp * kTileRows + i;
           const float* src = p.part_d + (size_t)b * kTileRows + i;
+          const float* osrc = p.part_o + (size_t)grp * go.kbs * ost + (size_t)b * kTileRows + i;
+          // the residual input, the output projection's partials (x_mid, as the norm stage
+          // formed it) and the first sixteen down-projection partials, all in flight together
+          const uint16_t xin = ldcg_u16(x_in(l, b) + r);
+          float ov[8], v[16];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ov[j] = (j < nco) ? ldcg(osrc + (size_t)j * ost) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = (j < nl) ? ldcg(src + list[j]) : 0.f;
           float y = 0.f;
-          for (int e0 = 0; e0 < nl; e0 += 16) {
-            float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) y += v[j];
+          for (int e0 = 16; e0 < nl; e0 += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = (e0 + j < nl) ? ldcg(src + list[e0 + j]) : 0.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) y += v[j];
           }
-          const float xm = bf16f(f2bf(bf16f(ldcg_u16(x_in(l, b) + r)) + seg_sum(K_O, stage_geo(p, K_O, 0), grp, b, i)));
+          float os = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) os += ov[j];
+          for (int c0 = 8; c0 < nco; c0 += 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ov[j] = (c0 + j < nco) ? ldcg(osrc + (size_t)(c0 + j) * ost) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) os += ov[j];
+          }
+          const float xm = bf16f(f2bf(bf16f(xin) + os));
           uint16_t o = f2bf(xm + y);
           p.xbuf[((size_t)((l + 1) & 1) * p.MB + b) * p.d + r] = o;
           if (l == p.L - 1 && p.hidden_out) p.hidden_out[(size_t)b * p.d + r] = o;
@@ -976,9 +1120,9 @@ struct Consumer {
                                    (unsigned long long)(0xFFFFFFFFu - (unsigned)(grp * kTileRows + best));
           atomicMax(p.amax + b, key);
         }
-        __threadfence();
         cons_sync();
         if (tid == 0) {
+          __threadfence();
           int old = atom_add_acqrel(p.cnt_lm_done, 1);
           if (old + 1 == p.n_rb_lm) {
             __threadfence();
@@ -1092,23 +1236,58 @@ struct Consumer {
         return count_reached(cnt + rb, (int)p.epoch * n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x));
       }, 13);
     }
-    float* raw = qkvn + (G + 2) * HD;
-    for (int idx = tid; idx < (G + 2) * HD; idx += kConsumerWarps * 32) {
+    // Each thread sums the contributor partials of its NPT values. All loads of a batch of eight
+    // contributors (for all NPT values, and the thread's RoPE angles) are issued before any is
+    // used, so the sums cost one L2 round trip per batch; each value is still summed in
+    // contributor order.
+    constexpr int NV_ = (G + 2) * HD;
+    constexpr int NPT = (NV_ + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    float* raw = qkvn + NV_;
+    const int pos = m->len[a.b];
+    const size_t pst = (size_t)p.MB * kTileRows;
+    const float* pbase[NPT];
+    int pnc[NPT], ncmax = 0;
+    float psum[NPT];
+    float2 cs[NPT];
+#pragma unroll
+    for (int i = 0; i < NPT; ++i) {
+      const int idx = tid + i * kConsumerWarps * 32;
       const int t = idx / HD, d = idx % HD;
       const int row = t < G ? (a.g * G + t) * HD + d : (t == G ? p.hq * HD : (p.hq + p.hkv) * HD) + a.g * HD + d;
-      raw[idx] = seg_sum(K_QKV, gq, row / kTileRows, a.b, row % kTileRows);
+      const int rb = row / kTileRows;
+      pnc[i] = idx < NV_ ? n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x) : 0;
+      pbase[i] = p.part_qkv + (size_t)rb * gq.kbs * pst + (size_t)a.b * kTileRows + row % kTileRows;
+      ncmax = max(ncmax, pnc[i]);
+      psum[i] = 0.f;
+      cs[i] = (idx < NV_ && t <= G) ? __ldg(p.rope + (size_t)pos * (HD / 2) + d % (HD / 2)) : make_float2(1.f, 0.f);
+    }
+    for (int c0 = 0; c0 < ncmax; c0 += 8) {
+      float v[NPT][8];
+#pragma unroll
+      for (int i = 0; i < NPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[i][j] = (c0 + j < pnc[i]) ? ldcg(pbase[i] + (size_t)(c0 + j) * pst) : 0.f;
+#pragma unroll
+      for (int i = 0; i < NPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) psum[i] += v[i][j];
+    }
+#pragma unroll
+    for (int i = 0; i < NPT; ++i) {
+      const int idx = tid + i * kConsumerWarps * 32;
+      if (idx < NV_) raw[idx] = psum[i];
     }
     cons_sync();
-    const int pos = m->len[a.b];
     const bool writer = (pos / kKvTilePos) >= a.tile0 && (pos / kKvTilePos) < a.tile1;
-    for (int idx = tid; idx < (G + 2) * HD; idx += kConsumerWarps * 32) {
+#pragma unroll
+    for (int i = 0; i < NPT; ++i) {
+      const int idx = tid + i * kConsumerWarps * 32;
+      if (idx >= NV_) break;
       const int t = idx / HD, d = idx % HD;
       float val = raw[idx];
       if (t <= G) {  // q heads and the key rotate; the value does not
-        const int j = d % (HD / 2);
-        const float2 cs = p.rope[(size_t)pos * (HD / 2) + j];
         const float other = raw[t * HD + (d < HD / 2 ? d + HD / 2 : d - HD / 2)];
-        val = d < HD / 2 ? val * cs.x - other * cs.y : val * cs.x + other * cs.y;
+        val = d < HD / 2 ? val * cs[i].x - other * cs[i].y : val * cs[i].x + other * cs[i].y;
       }
       const uint16_t bv = f2bf(val);
       qkvn[idx] = bf16f(bv);
@@ -1299,24 +1478,40 @@ struct Consumer {
           dst[(size_t)h * (HD + 2) + HD + 1] = Lsum;
         }
       }
-      __threadfence();
+      // publish: the CTA barrier orders every thread's partial before thread 0's fence and
+      // arrival; the last arriver's acquiring arrival orders its reads after all chunks
       cons_sync();
       int* cnt = p.attn_cnt + (size_t)a.b * p.hkv + a.g;
-      if (tid == 0) m->fin_old[0] = dead ? -1 : atom_add_acqrel(cnt, 1);
+      if (tid == 0) {
+        __threadfence();
+        m->fin_old[0] = dead ? -1 : atom_add_acqrel(cnt, 1);
+      }
       cons_sync();
       if (m->fin_old[0] == p.nch - 1) {
-        __threadfence();
         const float* src = p.attn_part + (((size_t)a.b * p.hkv + a.g) * p.nch * G) * (HD + 2);
-        // chunk maxima / sums -> shared memory, then per (head, dim) the rescaled sum of the
-        // chunks' accumulators with all loads in flight together
+        // Chunk merge. The chunk accumulators of the thread's (head, dim) pairs for the first
+        // kMergeBatch chunks are loaded first and the chunk maxima / sums after them, all in
+        // flight together; the weights exp2(m_c - M) / L go through shared memory.
+        constexpr int PER = (G * HD + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+        constexpr int kMergeBatch = 24;
         float* cm = red;                  // [G][nch]
         float* cl = red + G * p.nch;      // [G][nch]
         float* cw = red + 2 * G * p.nch;  // [G][nch] weights exp2(m_c - M) / L
+        float mv[PER][kMergeBatch];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int idx = tid + i * kConsumerWarps * 32;
+          const int h = idx / HD, d = idx % HD;
+#pragma unroll
+          for (int j = 0; j < kMergeBatch; ++j)
+            mv[i][j] = (idx < G * HD && j < p.nch) ? ldcg(src + ((size_t)j * G + h) * (HD + 2) + d) : 0.f;
+        }
         for (int idx = tid; idx < G * p.nch; idx += 256) {
           const int h = idx / p.nch, c = idx % p.nch;
           const float* r = src + ((size_t)c * G + h) * (HD + 2);
-          cm[idx] = ldcg(r + HD);
-          cl[idx] = ldcg(r + HD + 1);
+          const float mm = ldcg(r + HD), ll = ldcg(r + HD + 1);
+          cm[idx] = mm;
+          cl[idx] = ll;
         }
         cons_sync();
         for (int idx = tid; idx < G * p.nch; idx += 256) {
@@ -1332,10 +1527,16 @@ struct Consumer {
           cw[idx] = (mc == -INFINITY || !(Lsum > 0.f)) ? 0.f : exp2f(mc - M) / Lsum;
         }
         cons_sync();
-        for (int idx = tid; idx < G * HD; idx += 256) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const int idx = tid + i * kConsumerWarps * 32;
+          if (idx >= G * HD) break;
           const int h = idx / HD, d = idx % HD;
           float A = 0.f;
-          for (int c0 = 0; c0 < p.nch; c0 += 8) {
+#pragma unroll
+          for (int j = 0; j < kMergeBatch; ++j)
+            if (j < p.nch) A = fmaf(cw[h * p.nch + j], mv[i][j], A);
+          for (int c0 = kMergeBatch; c0 < p.nch; c0 += 8) {  // more chunks than one batch (small models)
             float v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -1346,9 +1547,9 @@ struct Consumer {
           }
           p.obuf[(size_t)a.b * p.hq * HD + (size_t)(a.g * G + h) * HD + d] = f2bf(A);
         }
-        __threadfence();
         cons_sync();
         if (tid == 0) {
+          __threadfence();
           atomicExch(cnt, 0);
           st_release(p.o_flag + ((size_t)l * p.MB + a.b) * p.hkv + a.g, p.epoch);
         }
@@ -1360,84 +1561,114 @@ struct Consumer {
 
   // -------- the step --------
 
+  // The step: per layer a fixed sequence of phases, each ending in at most one GEMV stage; then
+  // the final norm and the LM head. Every GEMV stage goes through the one gemv_stage call below,
+  // so its code (the hot tile loop, flushes and finalisers) exists once in the kernel: the
+  // instruction working set of a layer then stays small enough to be cached.
   __device__ void run() {
     trace(10 << 4);
-    for (int l = 0; l < p.L; ++l) {
-      const LayerDev& Ld = p.layers[l];
-      // attention block: q/k/v partials -> attention units (wait on their row blocks) ->
-      // merged head outputs -> output projection (waits on the groups it reads)
-      stage_rmsnorm(l, nullptr, Ld.attn_norm);
-      gemv_stage(K_QKV, l, 0);
-      cta_stamp();
-      attn_stage(l);
-      cta_stamp();
-      wait_o_groups(l);
-      cta_stamp();
-      stage_copy(p.obuf, p.hq * HD, (size_t)p.hq * HD, 0);
-      cons_sync();
-      gemv_stage(K_O, l, 0);
-      cta_stamp();
-      // FFN block: x_mid from the projection partials (waits on every row block)
-      stage_rmsnorm(l, nullptr, Ld.ffn_norm, true);
-      cta_stamp();
-      int U = 0;
-      if (p.dense) {
-        gemv_stage(K_SHGU, l, 0);
-      } else {
-        gemv_stage(K_ROUTER, l, 0);
-        if (p.nsh) gemv_stage(K_SHGU, l, 0);
-        // routing result (published by the router's finaliser)
-        if (tid == 0) {
-          int Uv = 0;
-          if (!dead && wait_flag(p, p.rt_flag + l, p.epoch, 12)) Uv = min(max(__ldcg(p.rt_u), 0), p.umax);
-          else dead = true;
-          m->U = Uv;
-          m->flag = dead ? 0 : 1;
+    int U = 0;
+#pragma unroll 1
+    for (int l = 0; l <= p.L; ++l) {
+      const bool lm = l == p.L;
+      if (lm && p.V == 0) break;
+#pragma unroll 1
+      for (int ph = 0; ph < 7; ++ph) {
+        int kind = -1;
+        if (lm) {
+          if (ph == 0) {
+            stage_rmsnorm(p.L, nullptr, p.final_norm);
+            kind = K_LM;
+          }
+        } else {
+          const LayerDev& Ld = p.layers[l];
+          switch (ph) {
+            case 0:
+              // attention block: q/k/v partials -> attention units (wait on their row blocks) ->
+              // merged head outputs -> output projection (waits on the groups it reads)
+              stage_rmsnorm(l, nullptr, Ld.attn_norm);
+              kind = K_QKV;
+              break;
+            case 1:
+              cta_stamp(l, S_QKV_DONE);
+              attn_stage(l);
+              cta_stamp(l, S_ATTN_DONE);
+              wait_o_groups(l);
+              cta_stamp(l, S_OGRP_READY);
+              stage_copy(p.obuf, p.hq * HD, (size_t)p.hq * HD, 0);
+              cons_sync();
+              kind = K_O;
+              break;
+            case 2:
+              cta_stamp(l, S_O_DONE);
+              // FFN block: x_mid from the projection partials (waits on every row block)
+              stage_rmsnorm(l, nullptr, Ld.ffn_norm, true);
+              cta_stamp(l, S_XMID_READY);
+              U = 0;
+              kind = p.dense ? K_SHGU : K_ROUTER;
+              break;
+            case 3:
+              if (!p.dense && p.nsh) kind = K_SHGU;
+              break;
+            case 4:
+              if (!p.dense) {
+                cta_stamp(l, S_FFN_PRE_DONE);
+                // routing result (published by the router's finaliser)
+                if (tid == 0) {
+                  int Uv = 0;
+                  if (!dead && wait_flag(p, p.rt_flag + l, p.epoch, 12)) Uv = min(max(__ldcg(p.rt_u), 0), p.umax);
+                  else dead = true;
+                  m->U = Uv;
+                  m->flag = dead ? 0 : 1;
+                }
+                cons_sync();
+                trace(9 << 4);
+                if (!m->flag) dead = true;
+                U = m->U;
+                for (int i = tid; i < BM * kMaxExperts; i += 256) {
+                  int b = i / kMaxExperts, u = i % kMaxExperts;
+                  m->gate[b][u] = (b < p.B && u < U) ? __ldcg(p.rt_gate + (size_t)b * kMaxExperts + u) : 0.f;
+                }
+                cons_sync();
+                cta_stamp(l, S_ROUTED);
+                kind = K_RTGU;
+              }
+              break;
+            case 5: {
+              cta_stamp(l, S_GU_DONE);
+              // down projections of all active experts, gate-weighted, + residual
+              const StageGeo g = stage_geo(p, K_D, U);
+              const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
+              int v_lo = 0, v_hi = -1;
+              if (t1 > t0) {
+                v_lo = t0 / g.tpe;
+                v_hi = (t1 - 1) / g.tpe;
+              }
+              if ((v_hi - v_lo + 1) * p.inter > p.xmax) raise_err(p, kDevBadArg, 6);
+              wait_h(l, v_lo, v_hi, U);
+              cta_stamp(l, S_H_READY);
+              if (tid == 0) m->v_lo = v_lo;
+              for (int i = tid; i < BM; i += 256) m->gate[i][U] = 1.f;  // shared / dense expert
+              for (int v = v_lo; v <= v_hi && (v - v_lo + 1) * p.inter <= p.xmax; ++v) {
+                const uint16_t* src = (v < U) ? p.hrt + (size_t)v * p.MB * p.inter : p.hsh;
+                stage_copy(src, p.inter, (size_t)p.inter, (v - v_lo) * p.inter);
+              }
+              cons_sync();
+              kind = K_D;
+              break;
+            }
+            default:
+              cta_stamp(l, S_D_DONE);
+              // the layer's residual stream is complete only when every down-projection block is final
+              gsync(1);
+              cta_stamp(l, S_BARRIER);
+              if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
+                for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
+              break;
+          }
         }
-        cons_sync();
-        trace(9 << 4);
-        if (!m->flag) dead = true;
-        U = m->U;
-        for (int i = tid; i < BM * kMaxExperts; i += 256) {
-          int b = i / kMaxExperts, u = i % kMaxExperts;
-          m->gate[b][u] = (b < p.B && u < U) ? __ldcg(p.rt_gate + (size_t)b * kMaxExperts + u) : 0.f;
-        }
-        cons_sync();
-        cta_stamp();
-        gemv_stage(K_RTGU, l, U);
+        if (kind >= 0) gemv_stage(kind, lm ? 0 : l, lm ? 0 : U);
       }
-      cta_stamp();
-      // down projections of all active experts, gate-weighted, + residual
-      {
-        const StageGeo g = stage_geo(p, K_D, U);
-        const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
-        int v_lo = 0, v_hi = -1;
-        if (t1 > t0) {
-          v_lo = t0 / g.tpe;
-          v_hi = (t1 - 1) / g.tpe;
-        }
-        if ((v_hi - v_lo + 1) * p.inter > p.xmax) raise_err(p, kDevBadArg, 6);
-        wait_h(l, v_lo, v_hi, U);
-        cta_stamp();
-        if (tid == 0) m->v_lo = v_lo;
-        for (int i = tid; i < BM; i += 256) m->gate[i][U] = 1.f;  // shared / dense expert
-        for (int v = v_lo; v <= v_hi && (v - v_lo + 1) * p.inter <= p.xmax; ++v) {
-          const uint16_t* src = (v < U) ? p.hrt + (size_t)v * p.MB * p.inter : p.hsh;
-          stage_copy(src, p.inter, (size_t)p.inter, (v - v_lo) * p.inter);
-        }
-        cons_sync();
-        gemv_stage(K_D, l, U);
-      }
-      cta_stamp();
-      // the layer's residual stream is complete only when every down-projection block is final
-      gsync(1);
-      cta_stamp();
-      if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
-        for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
-    }
-    if (p.V > 0) {
-      stage_rmsnorm(p.L, nullptr, p.final_norm);
-      gemv_stage(K_LM, 0, 0);
     }
     trace(10 << 4 | 1);
   }
