@@ -236,7 +236,7 @@ dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* 
    Words from 512 on hold per-CTA %globaltimer stamps of the first 8 layers: word
    512 + (layer * 16 + point) * grid + cta, for the points q/k/v tiles consumed (0), q/k/v done
    (1), attention merged (2), attention outputs ready (3), output-projection tiles consumed (4)
-   and done (5), x_mid ready (6), router + shared gate/up done (7), routing known (8), gate/up
+   and done (5), x_mid ready (6), router partials published (7), routing known (8), gate/up
    tiles consumed (9) and done (10), SwiGLU rows ready (11), down tiles consumed (12) and done
    (13), layer barrier passed (14). Copies up to n words and returns the count in *n_written.
    Synchronises. */

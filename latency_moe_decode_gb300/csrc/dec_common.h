@@ -85,20 +85,16 @@ struct KParams {
   // only grow (one arrival per contributor per launch), [L][row blocks]
   int *cnt_qkv, *cnt_o;
   // finalised outputs (router, SwiGLU h, down projection + residual, logits): last-arriver counters
-  int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
+  int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;  // cnt_router: [L], growing
   unsigned* o_flag;  // [L][MB][hkv] = epoch once the attention output of (sequence, KV head) is merged
   unsigned* h_flag;  // [L][umax + 1][n_rb_gu] = epoch once an expert's 64 SwiGLU rows are final
                      // (slot umax: the shared / dense expert)
   // attention split-KV partials: [MB][hkv][nch][group][hd + 2], counters [MB][hkv]
   float* attn_part;
   int* attn_cnt;
-  // routing result of the current layer
-  int* rt_u;          // [1] number of distinct experts
-  int* rt_elist;      // [E] distinct experts, ascending
-  float* rt_gate;     // [MB][E] gate of token b for distinct expert u (0 if not selected)
-  int* rt_idx;        // [L][MB][topk] selections (score-descending) for inspection
+  // routing of each layer, written by CTA 0 for inspection (every CTA computes it itself)
+  int* rt_idx;        // [L][MB][topk] selections (score-descending)
   float* rt_topk_gate;// [L][MB][topk]
-  unsigned* rt_flag;  // [L] = epoch once the layer's routing is published
   unsigned long long* amax;  // [MB] packed (ordered logit, ~id) maxima
   unsigned* gbar;     // [grid] per-CTA grid-barrier sequence words
   int* err;           // device status word

@@ -554,7 +554,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d);
     Z(p.o_flag, sizeof(unsigned) * (size_t)c.n_layers * MB * c.n_kv_heads);
     Z(p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu);
-    Z(p.cnt_router, sizeof(int) * std::max(1, p.n_rb_router));
+    Z(p.cnt_router, sizeof(int) * c.n_layers);
     Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
     Z(p.cnt_rtgu, sizeof(int) * std::max(1, p.umax) * p.n_rb_gu);
     Z(p.cnt_d, sizeof(int) * p.n_rb_d);
@@ -563,12 +563,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     e->nch_max = std::max(1, G / c.n_kv_heads);
     Z(p.attn_part, sizeof(float) * MB * c.n_kv_heads * e->nch_max * e->group * (c.head_dim + 2));
     Z(p.attn_cnt, sizeof(int) * MB * c.n_kv_heads);
-    Z(p.rt_u, sizeof(int) * 32);
-    Z(p.rt_elist, sizeof(int) * kMaxExperts);
-    Z(p.rt_gate, sizeof(float) * MB * kMaxExperts);
     Z(p.rt_idx, sizeof(int) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
-    Z(p.rt_flag, sizeof(unsigned) * c.n_layers);
     Z(p.amax, sizeof(unsigned long long) * MB);
     Z(p.gbar, sizeof(unsigned) * std::max(1024, G + 32));
     Z(p.err, sizeof(int) * 32);

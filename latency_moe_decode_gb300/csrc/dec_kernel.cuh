@@ -42,6 +42,7 @@ constexpr int kMaxSegs = 64;    // split-K segments one CTA may flush in one sta
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
 struct Misc {
+  uint64_t rt_bar;  // consumers -> producer: this layer's routing is in elist / U (one phase per layer)
   int flag;
   int nfin;
   int U;
@@ -86,7 +87,7 @@ enum Stamp : int {
   S_O_TILES,        // output-projection tiles consumed
   S_O_DONE,         // output-projection partials published
   S_XMID_READY,     // x_mid summed and normalised
-  S_FFN_PRE_DONE,   // router and shared-expert gate/up done
+  S_FFN_PRE_DONE,   // router partials published
   S_ROUTED,         // routing known
   S_GU_TILES,       // routed (or dense) gate/up tiles consumed
   S_GU_DONE,        // gate/up partials published, SwiGLU finalisers run
@@ -333,17 +334,18 @@ struct Producer {
     }
   }
 
-  // Routed experts are known only after the router: wait for this layer's routing flag.
+  // Routed experts are known only after the router: the CTA's consumers compute the routing and
+  // arrive on the routing mbarrier (one phase per layer) once it is in shared memory.
   __device__ bool routing(int l, int& U, int* elist) {
     if (dead) return false;
     trace(9 << 4);
-    if (!wait_flag(p, p.rt_flag + l, p.epoch, 11)) {
+    if (!mbar_wait(&m->rt_bar, (unsigned)l & 1u, p, 11)) {
       dead = true;
       return false;
     }
     trace(9 << 4 | 1);
-    U = min(max(__ldcg(p.rt_u), 0), p.umax);
-    for (int i = 0; i < U; ++i) elist[i] = min(max(__ldcg(p.rt_elist + i), 0), p.E - 1);
+    U = min(max(m->U, 0), p.umax);
+    for (int i = 0; i < U; ++i) elist[i] = min(max(m->elist[i], 0), p.E - 1);
     return true;
   }
 
@@ -716,6 +718,7 @@ struct Consumer {
   // Cross-warp reduction of one segment's accumulators, publication of the CTA's partial sums,
   // and the arrival on the output group's counter (result kept for the end of the stage).
   __device__ int* pub_counter(int kind, int l) const {
+    if (kind == K_ROUTER) return p.cnt_router + l;
     return kind == K_QKV ? p.cnt_qkv + (size_t)l * p.n_rb_qkv : p.cnt_o + (size_t)l * p.n_rb_d;
   }
 
@@ -734,7 +737,7 @@ struct Consumer {
     // The CTA barrier orders every thread's partial before the arriving thread's fence and
     // counter update (one fence per arrival; the other warps move on at once).
     cons_sync();
-    if (kind == K_QKV || kind == K_O) {
+    if (kind == K_QKV || kind == K_O || kind == K_ROUTER) {
       // published partials: the readers wait for every contributor of the row block
       if (tid == 0 && !dead) {
         __threadfence();
@@ -914,91 +917,125 @@ struct Consumer {
     trace(kind << 4 | 2);
   }
 
+  // -------- routing (every CTA computes it) --------
+
+  // Routing of layer l from the router's published partials: logits -> per-token top-k (ties to
+  // the lower expert index) -> sigmoid scores normalised over the selection -> the distinct
+  // experts in ascending order (m->elist, m->U) and each token's gate per distinct expert
+  // (m->gate). Every CTA computes the same result (same partials, same order), so no CTA waits
+  // for another one's selection; the CTA's producer is told through the routing mbarrier.
+  // CTA 0 also writes the selections for inspection.
+  __device__ void local_routing(int l) {
+    const StageGeo g = stage_geo(p, K_ROUTER, 0);
+    const int nc = n_contrib(0, g.kbs, g.T, gridDim.x);
+    const int* cnt = p.cnt_router + l;
+    cta_wait_all(1, [&](int) { return count_reached(cnt, (int)p.epoch * nc); }, 19);
+    float* tmp = red;                                        // [BM][128] logits
+    int* mark = reinterpret_cast<int*>(tmp + BM * kTileRows);  // [128] rank + 1 of expert e
+    int* sel = mark + kMaxExperts;                              // [BM][16]
+    float* sg = reinterpret_cast<float*>(sel + BM * 16);        // [BM][16]
+    // logits: TPI threads per (token, expert) sum interleaved contributor subsets, eight loads
+    // in flight per batch, then combine with a fixed butterfly (deterministic order)
+    {
+      const int items = p.B * p.E;
+      int tpi = 1;
+      while (tpi < 8 && tpi * 2 * items <= kConsumerWarps * 32) tpi *= 2;
+      const size_t st = (size_t)p.MB * kTileRows;
+      const int per = kConsumerWarps * 32 / tpi;  // items handled per pass
+      for (int i0 = 0; i0 < items; i0 += per) {
+        const int it = i0 + tid / tpi, part = tid % tpi;
+        const int b = it / max(p.E, 1), e = it % max(p.E, 1);
+        const bool ok = it < items;
+        const float* src = p.part_router + (size_t)b * kTileRows + e;
+        float s = 0.f;
+        for (int c0 = part; c0 < nc; c0 += 8 * tpi) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = (ok && c0 + j * tpi < nc) ? ldcg(src + (size_t)(c0 + j * tpi) * st) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s += v[j];
+        }
+        for (int o = 1; o < tpi; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (ok && part == 0) tmp[b * kTileRows + e] = s;
+      }
+      for (int idx = tid; idx < BM * kTileRows; idx += kConsumerWarps * 32) {
+        const int b = idx / kTileRows, e = idx % kTileRows;
+        if (b >= p.B || e >= p.E) tmp[idx] = -INFINITY;
+      }
+    }
+    if (tid < kMaxExperts) mark[tid] = 0;
+    cons_sync();
+    if (warp < p.B) {
+      const int b = warp;
+      float v[kMaxExperts / 32];
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j) v[j] = tmp[b * kTileRows + lane + 32 * j];
+      float ssum = 0.f;
+      for (int k = 0; k < p.topk; ++k) {
+        float bv = v[0];
+        int bi = lane;
+#pragma unroll
+        for (int j = 1; j < kMaxExperts / 32; ++j)
+          if (v[j] > bv) { bv = v[j]; bi = lane + 32 * j; }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) v[bi >> 5] = -INFINITY;
+        const float sc = 1.0f / (1.0f + expf(-bv));
+        ssum += sc;
+        if (lane == 0) {
+          sel[b * 16 + k] = bi;
+          sg[b * 16 + k] = sc;
+          mark[bi] = 1;
+        }
+      }
+      __syncwarp();
+      if (lane < p.topk) {
+        const float gt = sg[b * 16 + lane] / ssum;
+        sg[b * 16 + lane] = gt;
+        if (blockIdx.x == 0) {
+          p.rt_idx[((size_t)l * p.MB + b) * p.topk + lane] = sel[b * 16 + lane];
+          p.rt_topk_gate[((size_t)l * p.MB + b) * p.topk + lane] = gt;
+        }
+      }
+    }
+    cons_sync();
+    if (warp == 0) {
+      // distinct experts in ascending order: ballot prefix over the marks
+      int U2 = 0;
+      for (int j = 0; j < kMaxExperts / 32; ++j) {
+        const int e = lane + 32 * j;
+        const bool on = e < p.E && mark[e] != 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, on);
+        const int rank = U2 + __popc(bal & ((1u << lane) - 1u));
+        if (on) {
+          mark[e] = rank + 1;
+          m->elist[rank] = e;
+        }
+        U2 += __popc(bal);
+      }
+      if (lane == 0) m->U = min(U2, p.umax);
+    }
+    for (int idx = tid; idx < BM * (kMaxExperts + 1); idx += kConsumerWarps * 32)
+      m->gate[idx / (kMaxExperts + 1)][idx % (kMaxExperts + 1)] = 0.f;
+    cons_sync();
+    for (int idx = tid; idx < p.B * p.topk; idx += kConsumerWarps * 32) {
+      const int b = idx / p.topk, k = idx % p.topk;
+      const int e = sel[b * 16 + k];
+      m->gate[b][mark[e] - 1] = sg[b * 16 + k];
+    }
+    cons_sync();
+    if (tid == 0) mbar_arrive(&m->rt_bar);  // the producer may now issue the routed experts
+  }
+
   // -------- finalisers (run by the CTA whose arrival completed an output group) --------
 
   __device__ void finalize(int kind, int l, const StageGeo& g, int grp, int U) {
     float* tmp = red;  // [BM][128]
     switch (kind) {
-      case K_ROUTER: {
-        // logits -> per-token top-k (one warp per token, arg-max by shuffles, ties to the lower
-        // expert index) -> sigmoid scores normalised over the selection -> distinct expert list
-        for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
-          int b = idx / kTileRows, i = idx % kTileRows;
-          tmp[b * kTileRows + i] = (i < p.E) ? seg_sum(kind, g, grp, b, i) : -INFINITY;
-        }
-        int* mark = reinterpret_cast<int*>(tmp + BM * kTileRows);  // [128] rank + 1 of expert e
-        int* sel = mark + kMaxExperts;                              // [BM][16]
-        float* sg = reinterpret_cast<float*>(sel + BM * 16);        // [BM][16]
-        if (tid < kMaxExperts) mark[tid] = 0;
-        cons_sync();
-        if (warp < p.B) {
-          const int b = warp;
-          float v[kMaxExperts / 32];
-#pragma unroll
-          for (int j = 0; j < kMaxExperts / 32; ++j) v[j] = tmp[b * kTileRows + lane + 32 * j];
-          float ssum = 0.f;
-          for (int k = 0; k < p.topk; ++k) {
-            float bv = v[0];
-            int bi = lane;
-#pragma unroll
-            for (int j = 1; j < kMaxExperts / 32; ++j)
-              if (v[j] > bv) { bv = v[j]; bi = lane + 32 * j; }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-              float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-              int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-              if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            if ((bi & 31) == lane) v[bi >> 5] = -INFINITY;
-            const float sc = 1.0f / (1.0f + expf(-bv));
-            ssum += sc;
-            if (lane == 0) {
-              sel[b * 16 + k] = bi;
-              sg[b * 16 + k] = sc;
-              mark[bi] = 1;
-            }
-          }
-          __syncwarp();
-          if (lane < p.topk) {
-            const float gt = sg[b * 16 + lane] / ssum;
-            sg[b * 16 + lane] = gt;
-            p.rt_idx[((size_t)l * p.MB + b) * p.topk + lane] = sel[b * 16 + lane];
-            p.rt_topk_gate[((size_t)l * p.MB + b) * p.topk + lane] = gt;
-          }
-        }
-        cons_sync();
-        if (warp == 0) {
-          // distinct experts in ascending order: ballot prefix over the marks
-          int U2 = 0;
-          for (int j = 0; j < kMaxExperts / 32; ++j) {
-            const int e = lane + 32 * j;
-            const bool on = e < p.E && mark[e] != 0;
-            const unsigned bal = __ballot_sync(0xffffffffu, on);
-            const int rank = U2 + __popc(bal & ((1u << lane) - 1u));
-            if (on) {
-              mark[e] = rank + 1;
-              p.rt_elist[rank] = e;
-            }
-            U2 += __popc(bal);
-          }
-          if (lane == 0) p.rt_u[0] = U2;
-        }
-        cons_sync();
-        for (int idx = tid; idx < p.B * kMaxExperts; idx += 256)
-          p.rt_gate[(size_t)(idx / kMaxExperts) * kMaxExperts + (idx % kMaxExperts)] = 0.f;
-        cons_sync();
-        for (int idx = tid; idx < p.B * p.topk; idx += 256) {
-          const int b = idx / p.topk, k = idx % p.topk;
-          const int e = sel[b * 16 + k];
-          p.rt_gate[(size_t)b * kMaxExperts + (mark[e] - 1)] = sg[b * 16 + k];
-        }
-        cons_sync();
-        if (tid == 0) {
-          __threadfence();
-          st_release(p.rt_flag + l, p.epoch);
-        }
-        break;
-      }
       case K_SHGU:
       case K_RTGU: {
         const int half = kTileRows / 2;
@@ -1608,31 +1645,17 @@ struct Consumer {
               kind = p.dense ? K_SHGU : K_ROUTER;
               break;
             case 3:
-              if (!p.dense && p.nsh) kind = K_SHGU;
-              break;
-            case 4:
               if (!p.dense) {
                 cta_stamp(l, S_FFN_PRE_DONE);
-                // routing result (published by the router's finaliser)
-                if (tid == 0) {
-                  int Uv = 0;
-                  if (!dead && wait_flag(p, p.rt_flag + l, p.epoch, 12)) Uv = min(max(__ldcg(p.rt_u), 0), p.umax);
-                  else dead = true;
-                  m->U = Uv;
-                  m->flag = dead ? 0 : 1;
-                }
-                cons_sync();
+                local_routing(l);
                 trace(9 << 4);
-                if (!m->flag) dead = true;
                 U = m->U;
-                for (int i = tid; i < BM * kMaxExperts; i += 256) {
-                  int b = i / kMaxExperts, u = i % kMaxExperts;
-                  m->gate[b][u] = (b < p.B && u < U) ? __ldcg(p.rt_gate + (size_t)b * kMaxExperts + u) : 0.f;
-                }
-                cons_sync();
                 cta_stamp(l, S_ROUTED);
-                kind = K_RTGU;
+                if (p.nsh) kind = K_SHGU;
               }
+              break;
+            case 4:
+              if (!p.dense) kind = K_RTGU;
               break;
             case 5: {
               cta_stamp(l, S_GU_DONE);
@@ -1693,6 +1716,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(&m->rt_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < kMaxBatch) {
