@@ -84,9 +84,11 @@ struct KParams {
   // q/k/v and output-projection partials are read directly by the next stage: their counters
   // only grow (one arrival per contributor per launch), [L][row blocks]
   int *cnt_qkv, *cnt_o;
-  // finalised outputs (router, SwiGLU h, down projection + residual, logits): last-arriver counters
-  int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;  // cnt_router: [L], growing
+  // router partials: growing counter per layer [L]. Finalised outputs (SwiGLU h, down projection +
+  // residual, logits): arrival counters that the group's designated finaliser waits on and resets
+  int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
   unsigned* o_flag;  // [L][MB][hkv] = epoch once the attention output of (sequence, KV head) is merged
+  unsigned* x_flag;  // [L][n_rb_d] = epoch once a row block of the layer's output is final
   unsigned* h_flag;  // [L][umax + 1][n_rb_gu] = epoch once an expert's 64 SwiGLU rows are final
                      // (slot umax: the shared / dense expert)
   // attention split-KV partials: [MB][hkv][nch][group][hd + 2], counters [MB][hkv]
@@ -96,7 +98,6 @@ struct KParams {
   int* rt_idx;        // [L][MB][topk] selections (score-descending)
   float* rt_topk_gate;// [L][MB][topk]
   unsigned long long* amax;  // [MB] packed (ordered logit, ~id) maxima
-  unsigned* gbar;     // [grid] per-CTA grid-barrier sequence words
   int* err;           // device status word
   float* logits_ws;   // [MB][V] when the caller gives no logits buffer
   unsigned long long* trace;  // [kTraceSlots + kBarTrace * grid]

@@ -553,6 +553,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv);
     Z(p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d);
     Z(p.o_flag, sizeof(unsigned) * (size_t)c.n_layers * MB * c.n_kv_heads);
+    Z(p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d);
     Z(p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu);
     Z(p.cnt_router, sizeof(int) * c.n_layers);
     Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
@@ -566,7 +567,6 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.rt_idx, sizeof(int) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.amax, sizeof(unsigned long long) * MB);
-    Z(p.gbar, sizeof(unsigned) * std::max(1024, G + 32));
     Z(p.err, sizeof(int) * 32);
     Z(p.logits_ws, sizeof(float) * MB * std::max(1, c.vocab));
     Z(p.trace, sizeof(unsigned long long) * (kTraceSlots + (size_t)kBarTrace * G));

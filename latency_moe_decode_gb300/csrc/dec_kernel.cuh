@@ -19,11 +19,15 @@
 //               synchronisation wait).
 //   warps 0..7  consumers: dequantise E4M3 tiles (CUDA's cvt), multiply by the bf16 activations
 //               held in shared memory, accumulate in fp32, reduce across warps, and publish
-//               split-K partial sums. The last CTA to publish a partial of an output block
-//               finalises it (RoPE/KV append, residual add, SwiGLU, routing, logits + argmax):
-//               the "last arriver" pattern replaces a second pass.
-// Stage boundaries are grid-wide barriers on a generation counter (acquire/release); there are
-// five per layer. Every wait is bounded and turns into an error status instead of a hang.
+//               split-K partial sums with a releasing counter arrival (no CTA ever waits for
+//               the result of its own arrival).
+// Cross-CTA data flow of a layer: the q/k/v, output-projection and router partials are read
+// directly by every CTA that needs them (attention units, the x_mid norm, the routing, which
+// every CTA computes itself); the attention chunks are merged by the unit of the last chunk;
+// SwiGLU rows and the layer output row blocks are finalised by the owner of each group's last
+// tile, which waits for the group's counter and publishes an epoch flag. There is no grid
+// barrier: each consumer waits only for the data it reads. Every wait is bounded and turns into
+// an error status instead of a hang.
 #pragma once
 #include "dec_prims.cuh"
 
@@ -38,7 +42,6 @@ struct SmemLayout {
 
 constexpr int kMaxExperts = 128;
 constexpr int kListCap = 1024;  // contributor slots one down-projection row block may gather
-constexpr int kMaxSegs = 64;    // split-K segments one CTA may flush in one stage
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
 struct Misc {
@@ -48,8 +51,6 @@ struct Misc {
   int U;
   int v_lo;
   int len[kMaxBatch];
-  int fin_group[kMaxSegs];
-  int fin_old[kMaxSegs];
   int elist[kMaxExperts];
   float gate[kMaxBatch][kMaxExperts + 1];
   float rsum[kConsumerWarps][kMaxBatch];
@@ -94,7 +95,7 @@ enum Stamp : int {
   S_H_READY,        // the SwiGLU rows its down tiles read are final
   S_D_TILES,        // down-projection tiles consumed
   S_D_DONE,         // down partials published, finalisers run
-  S_BARRIER,        // layer barrier passed
+  S_BARRIER,        // layer done (its down stage and finalisers)
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -416,9 +417,6 @@ struct Consumer {
   bool dead = false;
   int warp, lane, tid;
   int stamp = 0;
-  int nflush = 0;   // segments flushed in the current stage
-  int pend = -1;    // pending counter arrival owned by this lane (warp 0 only)
-  unsigned nbar = 0;  // grid barriers passed in this step
 
   __device__ Consumer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint16_t* x, float* rd,
                       Misc* m_)
@@ -443,20 +441,6 @@ struct Consumer {
   __device__ void cta_stamp(int l, int k) {
     if (tid == 0 && l < kStampLayers)
       p.trace[kTraceSlots + ((size_t)l * kStampsPerLayer + k) * gridDim.x + blockIdx.x] = gtimer();
-  }
-
-  __device__ bool gsync(int where) {
-    if (dead) {
-      // keep the named-barrier sequence identical across warps; no grid traffic
-      cons_sync();
-      cons_sync();
-      return false;
-    }
-    const unsigned seq = p.epoch * 64u + (++nbar);
-    bool ok = grid_sync(p, &m->flag, where, seq);
-    if (!ok) dead = true;
-    trace(8 << 4 | where);
-    return ok;
   }
 
   // Every consumer warp walks the same item sequence and takes part in every item (a GEMV tile
@@ -494,6 +478,11 @@ struct Consumer {
   __device__ void stage_rmsnorm(int l_src, const uint16_t* direct, const uint16_t* w, bool from_o = false) {
     constexpr int MAXV = 4;  // hidden <= 8192: four 8-element chunks per thread
     const StageGeo go = stage_geo(p, K_O, 0);
+    if (!direct && !from_o && l_src > 0) {
+      // the previous layer's output rows (published by the down projection's finalisers)
+      const unsigned* f = p.x_flag + (size_t)(l_src - 1) * p.n_rb_d;
+      cta_wait_all(p.n_rb_d, [&](int rb) { return ld_acquire(f + rb) == p.epoch; }, 22);
+    }
     if (from_o) {
       const int* cnt = p.cnt_o + (size_t)l_src * p.n_rb_d;
       cta_wait_all(p.n_rb_d, [&](int rb) {
@@ -722,6 +711,13 @@ struct Consumer {
     return kind == K_QKV ? p.cnt_qkv + (size_t)l * p.n_rb_qkv : p.cnt_o + (size_t)l * p.n_rb_d;
   }
 
+  // output groups of a finalised stage (SwiGLU row blocks of each expert, output row blocks,
+  // vocabulary row blocks)
+  __device__ __forceinline__ int n_groups(int kind, const StageGeo& g) const {
+    if (kind == K_D) return p.n_rb_d;
+    return g.T / g.kbs;
+  }
+
   __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, float (&acc)[BM]) {
     // red[column half][row][b]: warp w holds row 32 * (w & 3) + lane of column half w >> 2
 #pragma unroll
@@ -734,30 +730,16 @@ struct Consumer {
       const int b = idx / kTileRows, row = idx % kTileRows;
       dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
     }
-    // The CTA barrier orders every thread's partial before the arriving thread's fence and
-    // counter update (one fence per arrival; the other warps move on at once).
+    // The CTA barrier orders every thread's partial before thread 0's releasing arrival; no
+    // thread waits for the arrival to complete.
     cons_sync();
+    if (dead) return;
     if (kind == K_QKV || kind == K_O || kind == K_ROUTER) {
       // published partials: the readers wait for every contributor of the row block
-      if (tid == 0 && !dead) {
-        __threadfence();
-        atomicAdd(pub_counter(kind, l) + seg, 1);
-      }
+      if (tid == 0) red_release_add(pub_counter(kind, l) + seg, 1);
       return;
     }
-    // Arrive on the output group's counter. The result is only needed at the end of the stage,
-    // so lane n of warp 0 keeps it in a register and the warp moves on to its next tile.
-    const int n = nflush++;
-    const int grp = seg_group(kind, seg);
-    if (warp == 0 && lane == (n & 31)) {
-      if (n >= 32) m->fin_old[n - 32] = pend;  // more than 32 segments: retire the older one
-      if (!dead) __threadfence();
-      pend = dead ? -1 : atom_add_acqrel(cnt_base(kind) + grp, 1);
-    }
-    if (tid == 0) {
-      if (n < kMaxSegs) m->fin_group[n] = grp;
-      else raise_err(p, kDevBadArg, 4);
-    }
+    if (tid == 0) red_release_add(cnt_base(kind) + seg_group(kind, seg), 1);
   }
 
   // number of arrivals that complete an output group
@@ -840,7 +822,6 @@ struct Consumer {
     const StageGeo g = stage_geo(p, kind, U);
     const int G_ = gridDim.x;
     const int t0 = range_lo(g.T, blockIdx.x, G_), t1 = range_lo(g.T, blockIdx.x + 1, G_);
-    nflush = 0;
     cons_sync();
     trace(kind << 4);
     float gmul[BM];
@@ -897,22 +878,22 @@ struct Consumer {
         for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
       }
     }
-    const int nf = min(nflush, kMaxSegs);
-    if (warp == 0 && lane < min(nflush, 32)) {
-      const int slot = nflush > 32 && lane < nflush - 32 ? lane + 32 : lane;
-      m->fin_old[slot] = pend;
-    }
-    cons_sync();
-    // finalise the output groups this CTA completed
-    for (int f = 0; f < nf; ++f) {
-      const int grp = m->fin_group[f];
-      const int old = m->fin_old[f];
-      if (old < 0 || old + 1 != group_expected(kind, g, grp)) continue;
-      // this CTA's acquiring arrival completed the group; the CTA barriers since then order the
-      // finaliser's reads after every contributor's publication
+    // Finalise the output groups this CTA is designated for (groups spread evenly over the
+    // CTAs, so no CTA finalises two while others finalise none): wait (acquire) until every
+    // contributor has arrived, finalise, and reset the counter for the next launch (nothing else
+    // touches it before then: every later arrival on it depends on this group's result). No
+    // contributor ever waits for the result of its own arrival.
+    const int ng = (kind == K_QKV || kind == K_O || kind == K_ROUTER) ? 0 : n_groups(kind, g);
+    const int f_lo = (int)(((long long)blockIdx.x * ng + G_ - 1) / G_);
+    const int f_hi = (int)(((long long)(blockIdx.x + 1) * ng + G_ - 1) / G_);
+    for (int grp = f_lo; grp < f_hi && !dead; ++grp) {
+      const int* c = cnt_base(kind) + grp;
+      const int want = group_expected(kind, g, grp);
+      cta_wait_all(1, [&](int) { return count_reached(c, want); }, 21);
+      if (dead) break;
       finalize(kind, l, g, grp, U);
       cons_sync();
-      if (tid == 0) atomicExch(cnt_base(kind) + grp, 0);
+      if (tid == 0) *const_cast<volatile int*>(c) = 0;
     }
     trace(kind << 4 | 2);
   }
@@ -1132,6 +1113,12 @@ struct Consumer {
           uint16_t o = f2bf(xm + y);
           p.xbuf[((size_t)((l + 1) & 1) * p.MB + b) * p.d + r] = o;
           if (l == p.L - 1 && p.hidden_out) p.hidden_out[(size_t)b * p.d + r] = o;
+        }
+        // the next layer's input row block is final
+        cons_sync();
+        if (tid == 0) {
+          __threadfence();
+          st_release(p.x_flag + (size_t)l * p.n_rb_d + grp, p.epoch);
         }
         break;
       }
@@ -1519,12 +1506,12 @@ struct Consumer {
       // arrival; the last arriver's acquiring arrival orders its reads after all chunks
       cons_sync();
       int* cnt = p.attn_cnt + (size_t)a.b * p.hkv + a.g;
-      if (tid == 0) {
-        __threadfence();
-        m->fin_old[0] = dead ? -1 : atom_add_acqrel(cnt, 1);
+      if (tid == 0 && !dead) red_release_add(cnt, 1);
+      // the unit of the last chunk merges (it waits for every chunk's arrival)
+      if (a.c == p.nch - 1 && !dead) {
+        cta_wait_all(1, [&](int) { return count_reached(cnt, p.nch); }, 23);
       }
-      cons_sync();
-      if (m->fin_old[0] == p.nch - 1) {
+      if (a.c == p.nch - 1 && !dead) {
         const float* src = p.attn_part + (((size_t)a.b * p.hkv + a.g) * p.nch * G) * (HD + 2);
         // Chunk merge. The chunk accumulators of the thread's (head, dim) pairs for the first
         // kMergeBatch chunks are loaded first and the chunk maxima / sums after them, all in
@@ -1586,8 +1573,8 @@ struct Consumer {
         }
         cons_sync();
         if (tid == 0) {
+          *const_cast<volatile int*>(cnt) = 0;
           __threadfence();
-          atomicExch(cnt, 0);
           st_release(p.o_flag + ((size_t)l * p.MB + a.b) * p.hkv + a.g, p.epoch);
         }
       }
@@ -1682,8 +1669,10 @@ struct Consumer {
             }
             default:
               cta_stamp(l, S_D_DONE);
-              // the layer's residual stream is complete only when every down-projection block is final
-              gsync(1);
+              // no grid barrier: the next layer's norm waits for the output row blocks it reads,
+              // and every buffer a later stage overwrites is read before an all-to-all exchange
+              // that the overwriting stage depends on
+              trace(8 << 4 | 1);
               cta_stamp(l, S_BARRIER);
               if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
                 for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;

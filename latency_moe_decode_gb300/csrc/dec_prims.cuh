@@ -1,5 +1,5 @@
 // Device primitives of the persistent decode kernel: mbarrier rings fed by bulk (TMA) copies,
-// L2 prefetch, acquire/release flags, a grid barrier, and FP8/bf16 conversions. Every wait is
+// acquire/release flags and counters, and FP8/bf16 conversions. Every wait is
 // bounded by %globaltimer: on expiry it records an error code in the device status word and
 // returns false, and every caller unwinds without touching the GPU further.
 #pragma once
@@ -113,6 +113,13 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Counter arrival that publishes: the release orders the writes before it (this thread's, and
+// through a preceding CTA barrier the whole CTA's) before the increment, without stalling the
+// issuing thread the way a full fence does.
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int atom_add_acqrel(int* p, int v) {
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -130,47 +137,6 @@ __device__ __forceinline__ void cons_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Grid barrier among the consumer warps of all CTAs. Each CTA publishes the barrier's sequence
-// number in its own word (release) and warp 0 polls all the words (acquire) until every CTA has
-// reached it: arrival costs no round trip and there is no single contended counter. Sequence
-// numbers grow across steps (64 per launch epoch), so the words never need resetting. Called by
-// all consumer threads; returns false if the kernel is aborting.
-__device__ __noinline__ bool grid_sync(const KParams& p, int* s_flag, int where, unsigned seq) {
-  cons_sync();
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 32) {
-    unsigned* flags = p.gbar;
-    if (lane == 0) {
-      __threadfence();
-      st_release(flags + blockIdx.x, seq);
-    }
-    __syncwarp();
-    int ok = 1;
-    const unsigned long long t0 = gtimer();
-    for (unsigned it = 1;; ++it) {
-      bool mine_ok = true;
-      for (int c = lane; c < (int)gridDim.x; c += 32) mine_ok &= (int)(ld_acquire(flags + c) - seq) >= 0;
-      if (__all_sync(0xffffffffu, mine_ok)) break;
-      if ((it & 15u) == 0) {
-        int bad = 0;
-        if (lane == 0) {
-          if (aborted(p)) bad = 1;
-          else if (gtimer() - t0 > p.timeout_ns) {
-            raise_err(p, kDevTimeout, where);
-            bad = 1;
-          }
-        }
-        if (__shfl_sync(0xffffffffu, bad, 0)) {
-          ok = 0;
-          break;
-        }
-      }
-    }
-    if (lane == 0) *s_flag = ok && !aborted(p);
-  }
-  cons_sync();
-  return *reinterpret_cast<volatile int*>(s_flag) != 0;
-}
 
 // Wait until a published flag reaches `want` (acquire); one thread polls.
 __device__ __forceinline__ bool wait_flag(const KParams& p, const unsigned* f, unsigned want, int where) {
