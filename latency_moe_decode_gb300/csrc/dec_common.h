@@ -22,6 +22,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kKvTilePos = 64;                       // KV positions per ring slot
 constexpr int kMaxBatch = 8;
+constexpr int kMaxHidden = 4096;                     // hidden sizes the kernel handles
 constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
 constexpr int kStampsPerLayer = 16;                  // per-CTA dependency time stamps of a layer
 constexpr int kStampLayers = 8;                      // layers whose stamps are kept

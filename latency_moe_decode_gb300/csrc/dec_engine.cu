@@ -325,7 +325,7 @@ dec_status dec_validate_cfg(const dec_model_cfg* c) {
   } else if (c->dense_ffn % 128 != 0) {
     return DEC_ERR_UNSUPPORTED;
   }
-  if (c->max_batch > kMaxBatch || c->n_kv_heads > 64 || c->hidden > 8192) return DEC_ERR_UNSUPPORTED;
+  if (c->max_batch > kMaxBatch || c->n_kv_heads > 64 || c->hidden > kMaxHidden) return DEC_ERR_UNSUPPORTED;
   return DEC_OK;
 }
 
@@ -396,6 +396,13 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   p.umax = dense ? 0 : std::min(c.n_experts, c.max_batch * c.top_k);
   e->grid = e->sms;
   const int G = e->grid;
+  {
+    // the kernel's tile-ownership arithmetic is 32-bit: (tiles of a stage + 1) x grid < 2^31
+    const long long t_max = std::max({(long long)p.n_rb_lm * p.kb_d, (long long)p.n_rb_qkv * p.kb_d,
+                                      (long long)(p.umax + p.nsh) * p.n_rb_d * p.kb_i,
+                                      (long long)std::max(1, p.umax) * p.n_rb_gu * p.kb_d});
+    if ((t_max + 1) * G >= (1LL << 31)) return bail(fail(e, DEC_ERR_UNSUPPORTED, "too many tiles in one stage"));
+  }
 
   // ---- weights: one arena for every repacked tile
   {

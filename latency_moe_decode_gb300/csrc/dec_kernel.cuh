@@ -44,7 +44,11 @@ constexpr int kMaxExperts = 128;
 constexpr int kListCap = 1024;  // contributor slots one down-projection row block may gather
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
+constexpr int kWaitMax = 128;  // conditions one CTA-wide wait may span
+
 struct Misc {
+  const unsigned* wt_addr[kWaitMax];  // CTA-wide wait: *wt_addr[i] >= wt_want[i] for all i
+  unsigned wt_want[kWaitMax];
   uint64_t rt_bar;  // consumers -> producer: this layer's routing is in elist / U (one phase per layer)
   int flag;
   int nfin;
@@ -55,6 +59,11 @@ struct Misc {
   float gate[kMaxBatch][kMaxExperts + 1];
   float rsum[kConsumerWarps][kMaxBatch];
   int tok[kMaxBatch];
+};
+
+struct WaitCond {
+  const unsigned* addr;  // null: holds at once
+  unsigned want;         // holds once *addr >= want
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -101,9 +110,10 @@ enum Stamp : int {
 // ---------------------------------------------------------------------------------------------
 // schedule arithmetic shared by producer and consumers
 
-__device__ __forceinline__ int range_lo(int T, int c, int G) { return (int)((long long)T * c / G); }
+// 32-bit arithmetic: a stage has far fewer than 2^31 / grid tiles (the host checks the largest)
+__device__ __forceinline__ int range_lo(int T, int c, int G) { return (int)((unsigned)T * (unsigned)c / (unsigned)G); }
 __device__ __forceinline__ int owner_of(int t, int T, int G) {
-  return (int)(((long long)(t + 1) * G - 1) / T);
+  return (int)(((unsigned)(t + 1) * (unsigned)G - 1u) / (unsigned)T);
 }
 // contributors to a segment of kbs consecutive tiles starting at tile a
 __device__ __forceinline__ int n_contrib(int a, int kbs, int T, int G) {
@@ -417,6 +427,7 @@ struct Consumer {
   bool dead = false;
   int warp, lane, tid;
   int stamp = 0;
+  bool range_bad = false;  // an activation staged as f16 was outside its range
 
   __device__ Consumer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint16_t* x, float* rd,
                       Misc* m_)
@@ -476,12 +487,12 @@ struct Consumer {
   // With `from_o`, the input is x_mid = bf16(x_in + output projection), summed here from the
   // projection's published split-K partials (after every contributor has arrived).
   __device__ void stage_rmsnorm(int l_src, const uint16_t* direct, const uint16_t* w, bool from_o = false) {
-    constexpr int MAXV = 4;  // hidden <= 8192: four 8-element chunks per thread
+    constexpr int MAXV = kMaxHidden / (kConsumerWarps * 32 * 8);  // 8-element chunks per thread
     const StageGeo go = stage_geo(p, K_O, 0);
     if (!direct && !from_o && l_src > 0) {
       // the previous layer's output rows (published by the down projection's finalisers)
       const unsigned* f = p.x_flag + (size_t)(l_src - 1) * p.n_rb_d;
-      cta_wait_all(p.n_rb_d, [&](int rb) { return ld_acquire(f + rb) == p.epoch; }, 22);
+      cta_wait_all(p.n_rb_d, [&](int rb) { return WaitCond{f + rb, p.epoch}; }, 22);
     }
     if (from_o) {
       const int* cnt = p.cnt_o + (size_t)l_src * p.n_rb_d;
@@ -510,7 +521,7 @@ struct Consumer {
         // round trip per batch); each row is summed in contributor order
         const size_t st = (size_t)p.MB * kTileRows;
 #pragma unroll
-        for (int jp = 0; jp < MAXV; jp += 2) {
+        for (int jp = 0; jp < MAXV; jp += 2) {  // MAXV == 2: one pass
           if ((tid + jp * kConsumerWarps * 32) * 8 >= p.d) break;
           float o8[2][8];
           int nc[2];
@@ -603,6 +614,7 @@ struct Consumer {
         *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) = o;
       }
     }
+    range_check();
     cons_sync();
   }
 
@@ -610,10 +622,17 @@ struct Consumer {
   // [2^-17, 65504] converts exactly (8 significant bits fit in f16's 11); smaller ones round with
   // an absolute error below 2^-25, far under the fp32 accumulation error of the sums they feed.
   // A value beyond the f16 range would become infinite, so it is reported as a device error.
+  // (The range test only sets a per-thread flag; range_check() reports it once per staging.)
   __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) raise_err(p, kDevRange, 5);
+    range_bad |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  __device__ __forceinline__ void range_check() {
+    if (range_bad) {
+      raise_err(p, kDevRange, 5);
+      range_bad = false;
+    }
   }
 
   // xs[b][dst_off + 0..n) = f16(src[b][0..n)) for a bf16 activation written by other CTAs
@@ -629,6 +648,7 @@ struct Consumer {
         for (int q = 0; q < 4; ++q) ou[q] = pack_f16x2(bf16lo(u[q]), bf16hi(u[q]));
         *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k) = o;
       }
+    range_check();
   }
 
   // -------- split-K GEMV over one stage --------
@@ -1094,21 +1114,15 @@ struct Consumer {
           float y = 0.f;
 #pragma unroll
           for (int j = 0; j < 16; ++j) y += v[j];
-          for (int e0 = 16; e0 < nl; e0 += 16) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = (e0 + j < nl) ? ldcg(src + list[e0 + j]) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) y += v[j];
-          }
+          // more contributors than one batch (not at the sizes this kernel is tuned for): one
+          // load at a time, in the same order
+#pragma unroll 1
+          for (int e = 16; e < nl; ++e) y += ldcg(src + list[e]);
           float os = 0.f;
 #pragma unroll
           for (int j = 0; j < 8; ++j) os += ov[j];
-          for (int c0 = 8; c0 < nco; c0 += 8) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) ov[j] = (c0 + j < nco) ? ldcg(osrc + (size_t)(c0 + j) * ost) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) os += ov[j];
-          }
+#pragma unroll 1
+          for (int c = 8; c < nco; ++c) os += ldcg(osrc + (size_t)c * ost);
           const float xm = bf16f(f2bf(bf16f(xin) + os));
           uint16_t o = f2bf(xm + y);
           p.xbuf[((size_t)((l + 1) & 1) * p.MB + b) * p.d + r] = o;
@@ -1203,35 +1217,27 @@ struct Consumer {
     return r;
   }
 
-  // Warp 0 waits until every one of n conditions holds; lane i checks conditions i, i+32, ...
-  // with one acquire load each, so a wait costs one L2 round trip per poll however many flags it
-  // spans. Afterwards the whole CTA agrees on the outcome (cons_sync). `check(i)` returns true
-  // once condition i holds.
+  // Warp 0 waits until every one of n conditions holds: `cond(i)` gives condition i as an
+  // address and a value it must reach (unsigned >=; a null address always holds). The lanes
+  // write the conditions into a shared table once, then the one out-of-line poller checks them
+  // (lane j conditions j, j + 32, ..., one acquire load each), so a wait costs one L2 round trip
+  // per poll however many flags it spans. Afterwards the whole CTA agrees on the outcome.
   template <class F>
-  __device__ void cta_wait_all(int n, F check, int where) {
+  __device__ void cta_wait_all(int n, F cond, int where) {
     if (warp == 0) {
       int ok = dead ? 0 : 1;
+      if (n > kWaitMax) {
+        if (lane == 0) raise_err(p, kDevBadArg, 7);
+        ok = 0;
+      }
       if (ok) {
-        const unsigned long long t0 = gtimer();
-        for (unsigned it = 1;; ++it) {
-          bool mine_ok = true;
-          for (int i = lane; i < n; i += 32) mine_ok &= check(i);
-          if (__all_sync(0xffffffffu, mine_ok)) break;
-          if ((it & 15u) == 0) {
-            int bad = 0;
-            if (lane == 0) {
-              if (aborted(p)) bad = 1;
-              else if (gtimer() - t0 > p.timeout_ns) {
-                raise_err(p, kDevTimeout, where);
-                bad = 1;
-              }
-            }
-            if (__shfl_sync(0xffffffffu, bad, 0)) {
-              ok = 0;
-              break;
-            }
-          }
+        for (int i = lane; i < n; i += 32) {
+          const WaitCond c = cond(i);
+          m->wt_addr[i] = c.addr;
+          m->wt_want[i] = c.want;
         }
+        __syncwarp();
+        ok = poll_all_geq(m->wt_addr, m->wt_want, n, p.err, p.timeout_ns, where);
       }
       if (lane == 0) m->flag = ok;
     }
@@ -1239,8 +1245,9 @@ struct Consumer {
     if (!m->flag) dead = true;
   }
 
-  __device__ __forceinline__ bool count_reached(const int* c, int target) const {
-    return (int)ld_acquire(reinterpret_cast<const unsigned*>(c)) >= target;
+  // a wait condition: a counter reaching target, or a flag reaching a value
+  __device__ __forceinline__ WaitCond count_reached(const int* c, int target) const {
+    return WaitCond{reinterpret_cast<const unsigned*>(c), (unsigned)target};
   }
 
   // The unit's q heads, key and value for this token: summed from the published split-K
@@ -1336,7 +1343,7 @@ struct Consumer {
     const unsigned* f = p.o_flag + (size_t)l * p.MB * p.hkv;
     cta_wait_all(p.B * p.hkv, [&](int i) {
       const int b = i / p.hkv, g = i % p.hkv;
-      return !((mask >> g) & 1ull) || ld_acquire(f + (size_t)b * p.hkv + g) == p.epoch;
+      return ((mask >> g) & 1ull) ? WaitCond{f + (size_t)b * p.hkv + g, p.epoch} : WaitCond{nullptr, 0u};
     }, 16);
   }
 
@@ -1346,7 +1353,7 @@ struct Consumer {
     cta_wait_all(nv * p.n_rb_gu, [&](int i) {
       const int v = v_lo + i / p.n_rb_gu, rb = i % p.n_rb_gu;
       const int slot = v < U ? v : p.umax;
-      return ld_acquire(p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb) == p.epoch;
+      return WaitCond{p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch};
     }, 17);
   }
 
@@ -1560,15 +1567,9 @@ struct Consumer {
 #pragma unroll
           for (int j = 0; j < kMergeBatch; ++j)
             if (j < p.nch) A = fmaf(cw[h * p.nch + j], mv[i][j], A);
-          for (int c0 = kMergeBatch; c0 < p.nch; c0 += 8) {  // more chunks than one batch (small models)
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              v[j] = (c0 + j < p.nch) ? ldcg(src + ((size_t)(c0 + j) * G + h) * (HD + 2) + d) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (c0 + j < p.nch) A = fmaf(cw[h * p.nch + c0 + j], v[j], A);
-          }
+#pragma unroll 1
+          for (int c = kMergeBatch; c < p.nch; ++c)  // more chunks than one batch (small models)
+            A = fmaf(cw[h * p.nch + c], ldcg(src + ((size_t)c * G + h) * (HD + 2) + d), A);
           p.obuf[(size_t)a.b * p.hq * HD + (size_t)(a.g * G + h) * HD + d] = f2bf(A);
         }
         cons_sync();
@@ -1599,9 +1600,12 @@ struct Consumer {
 #pragma unroll 1
       for (int ph = 0; ph < 7; ++ph) {
         int kind = -1;
+        // a norm stage runs right before the GEMV stage it feeds (one call site, see below)
+        const uint16_t* norm_w = nullptr;
+        bool norm_from_o = false;
         if (lm) {
           if (ph == 0) {
-            stage_rmsnorm(p.L, nullptr, p.final_norm);
+            norm_w = p.final_norm;
             kind = K_LM;
           }
         } else {
@@ -1610,7 +1614,7 @@ struct Consumer {
             case 0:
               // attention block: q/k/v partials -> attention units (wait on their row blocks) ->
               // merged head outputs -> output projection (waits on the groups it reads)
-              stage_rmsnorm(l, nullptr, Ld.attn_norm);
+              norm_w = Ld.attn_norm;
               kind = K_QKV;
               break;
             case 1:
@@ -1626,8 +1630,8 @@ struct Consumer {
             case 2:
               cta_stamp(l, S_O_DONE);
               // FFN block: x_mid from the projection partials (waits on every row block)
-              stage_rmsnorm(l, nullptr, Ld.ffn_norm, true);
-              cta_stamp(l, S_XMID_READY);
+              norm_w = Ld.ffn_norm;
+              norm_from_o = true;
               U = 0;
               kind = p.dense ? K_SHGU : K_ROUTER;
               break;
@@ -1678,6 +1682,10 @@ struct Consumer {
                 for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
               break;
           }
+        }
+        if (norm_w) {
+          stage_rmsnorm(lm ? p.L : l, nullptr, norm_w, norm_from_o);
+          if (norm_from_o) cta_stamp(l, S_XMID_READY);
         }
         if (kind >= 0) gemv_stage(kind, lm ? 0 : l, lm ? 0 : U);
       }

@@ -34,6 +34,7 @@ __device__ __noinline__ void raise_err(const KParams& p, int code, int where) {
   atomicCAS(p.err, 0, code | (where << 8));
 }
 
+
 // ---------------------------------------------------------------------------------------------
 // mbarrier
 
@@ -111,6 +112,33 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Called by all 32 lanes of one warp: wait until *addr[i] >= want[i] (unsigned, acquire) for
+// every i < n with a non-null address; lane j polls conditions j, j + 32, ... Returns 1 when they
+// all hold, 0 on abort or after timeout_ns (then the status word records a timeout at `where`).
+// One out-of-line copy serves every wait of the kernel.
+__device__ __noinline__ int poll_all_geq(const unsigned* const* addr, const unsigned* want, int n,
+                                         int* err, unsigned long long timeout_ns, int where) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long t0 = gtimer();
+  for (unsigned it = 1;; ++it) {
+    bool ok = true;
+    for (int i = lane; i < n; i += 32)
+      if (addr[i] && ld_acquire(addr[i]) < want[i]) ok = false;
+    if (__all_sync(0xffffffffu, ok)) return 1;
+    if ((it & 15u) == 0) {
+      int bad = 0;
+      if (lane == 0) {
+        if (*reinterpret_cast<volatile int*>(err) != 0) bad = 1;
+        else if (gtimer() - t0 > timeout_ns) {
+          atomicCAS(err, 0, kDevTimeout | (where << 8));
+          bad = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, bad, 0)) return 0;
+    }
+  }
 }
 
 // Counter arrival that publishes: the release orders the writes before it (this thread's, and
