@@ -147,54 +147,45 @@ __device__ __forceinline__ StageGeo stage_geo(const KParams& p, int kind, int U)
   return g;
 }
 
-__device__ __forceinline__ const uint8_t* tile_addr(const KParams& p, const LayerDev& Ld, int kind,
-                                                    int t, const StageGeo& g, int U, const int* elist) {
-  const size_t TB = kTileBytes;
-  switch (kind) {
-    case K_QKV: return Ld.qkv + (size_t)t * TB;
-    case K_O: return Ld.o + (size_t)t * TB;
-    case K_ROUTER: return Ld.router + (size_t)t * TB;
-    case K_SHGU: return Ld.sh_gu + (size_t)t * TB;
-    case K_RTGU: {
-      int u = t / g.tpe, r = t - u * g.tpe;
-      return Ld.e_gu + (size_t)elist[u] * p.e_gu_stride + (size_t)r * TB;
-    }
-    case K_D: {
-      int v = t / g.tpe, r = t - v * g.tpe;
-      if (v < U) return Ld.e_d + (size_t)elist[v] * p.e_d_stride + (size_t)r * TB;
-      return Ld.sh_d + (size_t)r * TB;
-    }
-    default: return p.lm + (size_t)t * TB;
-  }
-}
-
-// Walks a stage's tiles in order: the address of tile t, then of t + 1, ... Expert stages keep
-// the (expert, tile within expert) pair instead of dividing t by the tiles per expert.
+// Walks a stage's tiles in order (no divisions per tile). Plain stages are one contiguous run of
+// tiles; expert stages are a run of tpe tiles per expert slot u, at that expert's weights (the
+// shared / dense expert's after the routed ones for the down projections).
 struct TileCursor {
   const uint8_t* addr;
   int u, r;  // expert stages: expert slot and tile within it
+  __device__ __forceinline__ static const uint8_t* expert_base(const KParams& p, const LayerDev& Ld, int kind, int u,
+                                                               int U, const int* elist) {
+    if (kind == K_RTGU) return Ld.e_gu + (size_t)elist[u] * p.e_gu_stride;
+    return u < U ? Ld.e_d + (size_t)elist[u] * p.e_d_stride : Ld.sh_d;
+  }
+  __device__ void init(const KParams& p, const LayerDev& Ld, int kind, int t, const StageGeo& g, int U,
+                       const int* elist) {
+    if (kind == K_RTGU || kind == K_D) {
+      u = t / g.tpe;
+      r = t - u * g.tpe;
+      addr = expert_base(p, Ld, kind, u, U, elist) + (size_t)r * kTileBytes;
+      return;
+    }
+    const uint8_t* base = kind == K_QKV ? Ld.qkv
+                        : kind == K_O ? Ld.o
+                        : kind == K_ROUTER ? Ld.router
+                        : kind == K_SHGU ? Ld.sh_gu
+                                         : p.lm;
+    u = 0;
+    r = t;
+    addr = base + (size_t)t * kTileBytes;
+  }
+  // advance to the next tile; past the stage's last expert there is none (the caller stops first)
   __device__ __forceinline__ void next(const KParams& p, const LayerDev& Ld, int kind, const StageGeo& g, int U,
                                        const int* elist) {
-    if (kind == K_RTGU || kind == K_D) {
-      if (++r == g.tpe) {
-        r = 0;
-        ++u;
-        // past the stage's last expert there is no next tile (the caller stops before using it)
-        if (u < g.T / g.tpe) addr = tile_addr(p, Ld, kind, u * g.tpe, g, U, elist);
-        return;
-      }
-    }
     addr += kTileBytes;
+    if ((kind == K_RTGU || kind == K_D) && ++r == g.tpe) {
+      r = 0;
+      ++u;
+      if (u * g.tpe < g.T) addr = expert_base(p, Ld, kind, u, U, elist);
+    }
   }
 };
-__device__ __forceinline__ TileCursor tile_cursor(const KParams& p, const LayerDev& Ld, int kind, int t,
-                                                  const StageGeo& g, int U, const int* elist) {
-  TileCursor c;
-  c.u = g.tpe > 0 ? t / g.tpe : 0;
-  c.r = t - c.u * g.tpe;
-  c.addr = tile_addr(p, Ld, kind, t, g, U, elist);
-  return c;
-}
 
 // attention work units: (sequence b, KV head g, context chunk c)
 struct AttnUnit {
@@ -249,11 +240,9 @@ struct Producer {
       : p(p_), ring(r), full(f), empty(e), m(m_) {}
 
   // every bulk copy source must lie inside its allocation (checked before the copy is issued)
-  __device__ bool in_range(const void* src, size_t bytes, const void* base, size_t extent, int where) {
+  __device__ __forceinline__ static bool within(const void* src, size_t bytes, const void* base, size_t extent) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(base);
-    if (a >= b && a + bytes <= b + extent && (a & 15u) == 0 && (bytes & 15u) == 0) return true;
-    raise_err(p, kDevBadArg, where);
-    return false;
+    return a >= b && a + bytes <= b + extent && (a & 15u) == 0 && (bytes & 15u) == 0;
   }
 
   // claim the next slot: wait until the consumers released it
@@ -285,7 +274,8 @@ struct Producer {
     // a slot takes the next kSlotTiles tiles of the CTA's range (fewer at its end): one copy when
     // they are adjacent in memory, one per tile otherwise (an expert boundary). The tile address
     // is advanced tile by tile (no divisions in the loop).
-    TileCursor cur = tile_cursor(p, Ld, kind, t0, g, U, elist);
+    TileCursor cur;
+    if (t1 > t0) cur.init(p, Ld, kind, t0, g, U, elist);
     for (int t = t0; t < t1; t += kSlotTiles) {
       int slot;
       if (!claim(slot)) return;
@@ -294,15 +284,15 @@ struct Producer {
       bool ok = true;
 #pragma unroll
       for (int j = 0; j < kSlotTiles; ++j) {
-        src[j] = nullptr;
+        src[j] = cur.addr;
         if (j < n) {
-          src[j] = cur.addr;
-          ok = ok && in_range(src[j], kTileBytes, p.warena, p.warena_bytes, 30);
+          ok = ok && within(src[j], kTileBytes, p.warena, p.warena_bytes);
           cur.next(p, Ld, kind, g, U, elist);
         }
       }
       uint8_t* dst = ring + (size_t)slot * kSlotBytes;
       if (!ok) {
+        raise_err(p, kDevBadArg, 30);
         mbar_arrive(&full[slot]);  // keep the ring consistent; the status word stops the step
         advance();
         continue;
@@ -331,8 +321,9 @@ struct Producer {
         int n = min(kKvTilePos, a.T - p0);
         uint8_t* dst = ring + (size_t)slot * kSlotBytes;
         const size_t r0 = kv_row(p, l, a.b, a.g, p0);
-        if (n < 1 || n > kKvTilePos || !in_range(p.kc + r0, n * row_bytes, p.kc, p.kv_bytes, 31) ||
-            !in_range(p.vc + r0, n * row_bytes, p.vc, p.kv_bytes, 32)) {
+        if (n < 1 || n > kKvTilePos || !within(p.kc + r0, n * row_bytes, p.kc, p.kv_bytes) ||
+            !within(p.vc + r0, n * row_bytes, p.vc, p.kv_bytes)) {
+          raise_err(p, kDevBadArg, 31);
           mbar_arrive(&full[slot]);
           advance();
           continue;
@@ -1600,9 +1591,12 @@ struct Consumer {
 #pragma unroll 1
       for (int ph = 0; ph < 7; ++ph) {
         int kind = -1;
-        // a norm stage runs right before the GEMV stage it feeds (one call site, see below)
+        // a norm stage or an activation copy runs right before the GEMV stage it feeds (one call
+        // site each, see below): the attention output, or the SwiGLU rows of experts cp_lo..cp_hi
         const uint16_t* norm_w = nullptr;
         bool norm_from_o = false;
+        int cp_lo = 0, cp_hi = -1;
+        bool cp_obuf = false;
         if (lm) {
           if (ph == 0) {
             norm_w = p.final_norm;
@@ -1623,8 +1617,8 @@ struct Consumer {
               cta_stamp(l, S_ATTN_DONE);
               wait_o_groups(l);
               cta_stamp(l, S_OGRP_READY);
-              stage_copy(p.obuf, p.hq * HD, (size_t)p.hq * HD, 0);
-              cons_sync();
+              cp_obuf = true;
+              cp_hi = 0;
               kind = K_O;
               break;
             case 2:
@@ -1663,11 +1657,8 @@ struct Consumer {
               cta_stamp(l, S_H_READY);
               if (tid == 0) m->v_lo = v_lo;
               for (int i = tid; i < BM; i += 256) m->gate[i][U] = 1.f;  // shared / dense expert
-              for (int v = v_lo; v <= v_hi && (v - v_lo + 1) * p.inter <= p.xmax; ++v) {
-                const uint16_t* src = (v < U) ? p.hrt + (size_t)v * p.MB * p.inter : p.hsh;
-                stage_copy(src, p.inter, (size_t)p.inter, (v - v_lo) * p.inter);
-              }
-              cons_sync();
+              cp_lo = v_lo;
+              cp_hi = (v_hi - v_lo + 1) * p.inter <= p.xmax ? v_hi : v_lo - 1;
               kind = K_D;
               break;
             }
@@ -1686,6 +1677,14 @@ struct Consumer {
         if (norm_w) {
           stage_rmsnorm(lm ? p.L : l, nullptr, norm_w, norm_from_o);
           if (norm_from_o) cta_stamp(l, S_XMID_READY);
+        }
+        if (cp_hi >= cp_lo) {
+          for (int v = cp_lo; v <= cp_hi; ++v) {
+            const uint16_t* src = cp_obuf ? p.obuf : (v < U ? p.hrt + (size_t)v * p.MB * p.inter : p.hsh);
+            const int n = cp_obuf ? p.hq * HD : p.inter;
+            stage_copy(src, n, (size_t)n, (v - cp_lo) * n);
+          }
+          cons_sync();
         }
         if (kind >= 0) gemv_stage(kind, lm ? 0 : l, lm ? 0 : U);
       }

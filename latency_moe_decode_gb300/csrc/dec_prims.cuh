@@ -67,22 +67,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier; false on timeout or abort. The clock and the status
-// word (an L2 round trip) are consulted only every 64 polls, so a wait that ends quickly costs
-// no global traffic.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const KParams& p, int where) {
-  if (mbar_try_wait(b, parity)) return true;
+// Wait for phase `parity` of an mbarrier; false on timeout or abort. The first test is inline;
+// the polling loop is one out-of-line copy. The clock and the status word (an L2 round trip) are
+// consulted only every 64 polls, so a wait that ends quickly costs no global traffic.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, unsigned parity, int* err, unsigned long long timeout_ns,
+                                            int where) {
   const unsigned long long t0 = gtimer();
   for (unsigned it = 1;; ++it) {
     if (mbar_try_wait(b, parity)) return true;
     if ((it & 63u) == 0) {
-      if (aborted(p)) return false;
-      if (gtimer() - t0 > p.timeout_ns) {
-        raise_err(p, kDevTimeout, where);
+      if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+      if (gtimer() - t0 > timeout_ns) {
+        atomicCAS(err, 0, kDevTimeout | (where << 8));
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const KParams& p, int where) {
+  if (mbar_try_wait(b, parity)) return true;
+  return mbar_wait_slow(b, parity, p.err, p.timeout_ns, where);
 }
 
 // ---------------------------------------------------------------------------------------------
