@@ -1386,6 +1386,20 @@ struct Consumer {
       // online-softmax state (merged across warps after the unit's last tile).
       for (int t = a.tile0; t < a.tile1; ++t) {
         const uint8_t* slot = wait_item();
+        {
+          // This step's key and value (from the prologue; the slot's copy of the cache may predate
+          // them) are written into the slot once, so the loops below read every position alike.
+          const int jn = newpos - t * kKvTilePos;
+          if (!dead && jn >= 0 && jn < kKvTilePos) {  // the same for all warps
+            uint16_t* kr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + jn * row_bytes);
+            uint16_t* vr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + (kKvTilePos + jn) * row_bytes);
+            for (int d = tid; d < HD; d += kConsumerWarps * 32) {
+              kr[d] = f2bf(qkvn[G * HD + d]);
+              vr[d] = f2bf(qkvn[(G + 1) * HD + d]);
+            }
+            cons_sync();
+          }
+        }
         if (!dead) {
           const int p0 = t * kKvTilePos;
           const int npos = min(kKvTilePos, a.T - p0);
@@ -1395,12 +1409,7 @@ struct Consumer {
             const int j = warp * PPW + i;
             float kf[DPL];
             if (j < npos) {
-              if (p0 + j == newpos) {  // this step's key comes from the prologue, not the ring
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) kf[d] = qkvn[G * HD + lane * DPL + d];
-              } else {
-                load_bf16_row<DPL>(reinterpret_cast<const uint16_t*>(slot + j * row_bytes) + lane * DPL, false, kf);
-              }
+              load_bf16_row<DPL>(reinterpret_cast<const uint16_t*>(slot + j * row_bytes) + lane * DPL, false, kf);
             } else {
 #pragma unroll
               for (int d = 0; d < DPL; ++d) kf[d] = 0.f;
@@ -1449,13 +1458,8 @@ struct Consumer {
             const int j = warp * PPW + i;
             if (j < npos) {
               float vf[DPL];
-              if (p0 + j == newpos) {
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) vf[d] = qkvn[(G + 1) * HD + lane * DPL + d];
-              } else {
-                load_bf16_row<DPL>(reinterpret_cast<const uint16_t*>(slot + (kKvTilePos + j) * row_bytes) + lane * DPL,
-                                   false, vf);
-              }
+              load_bf16_row<DPL>(reinterpret_cast<const uint16_t*>(slot + (kKvTilePos + j) * row_bytes) + lane * DPL,
+                                 false, vf);
 #pragma unroll
               for (int h = 0; h < G; ++h)
 #pragma unroll

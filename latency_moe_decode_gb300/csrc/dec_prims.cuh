@@ -128,6 +128,7 @@ __device__ __noinline__ int poll_all_geq(const unsigned* const* addr, const unsi
   const unsigned long long t0 = gtimer();
   for (unsigned it = 1;; ++it) {
     bool ok = true;
+#pragma unroll 1
     for (int i = lane; i < n; i += 32)
       if (addr[i] && ld_acquire(addr[i]) < want[i]) ok = false;
     if (__all_sync(0xffffffffu, ok)) return 1;
