@@ -498,7 +498,8 @@ struct Consumer {
       const int k = (tid + j * kConsumerWarps * 32) * 8;
       if (k < p.d) wv[j] = __ldg(reinterpret_cast<const uint4*>(w + k));
     }
-    for (int b = 0; b < p.B; ++b) {
+#pragma unroll 1
+    for (int b = 0; b < min(p.B, BM); ++b) {
       const uint16_t* src = direct ? direct + (size_t)b * p.d : x_in(l_src, b);
       uint4 v[MAXV];
 #pragma unroll
@@ -582,7 +583,8 @@ struct Consumer {
       if (lane == 0) m->rsum[warp][b] = ss;
     }
     cons_sync();
-    for (int b = 0; b < p.B; ++b) {
+#pragma unroll 1
+    for (int b = 0; b < min(p.B, BM); ++b) {
       float ss = 0.f;
 #pragma unroll
       for (int wi = 0; wi < kConsumerWarps; ++wi) ss += m->rsum[wi][b];
@@ -626,18 +628,28 @@ struct Consumer {
     }
   }
 
-  // xs[b][dst_off + 0..n) = f16(src[b][0..n)) for a bf16 activation written by other CTAs
+  // xs[b][dst_off + 0..n) = f16(src[b][0..n)) for a bf16 activation written by other CTAs; two
+  // 8-element chunks per thread and pass, both loads in flight before either is stored
   __device__ void stage_copy(const uint16_t* src, int n, size_t src_stride, int dst_off) {
-    for (int b = 0; b < p.B; ++b)
-#pragma unroll 4
-      for (int k = tid * 8; k < n; k += kConsumerWarps * 32 * 8) {
-        const uint4 v = ldcg4(src + (size_t)b * src_stride + k);
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
-        uint4 o;
-        uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
+    constexpr int P = kConsumerWarps * 32 * 8;
+#pragma unroll 1
+    for (int b = 0; b < min(p.B, BM); ++b)
+#pragma unroll 1
+      for (int k0 = tid * 8; k0 < n; k0 += 2 * P) {
+        uint4 v[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ou[q] = pack_f16x2(bf16lo(u[q]), bf16hi(u[q]));
-        *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k) = o;
+        for (int j = 0; j < 2; ++j)
+          if (k0 + j * P < n) v[j] = ldcg4(src + (size_t)b * src_stride + k0 + j * P);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (k0 + j * P >= n) break;
+          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[j]);
+          uint4 o;
+          uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ou[q] = pack_f16x2(bf16lo(u[q]), bf16hi(u[q]));
+          *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k0 + j * P) = o;
+        }
       }
     range_check();
   }
@@ -737,6 +749,7 @@ struct Consumer {
     const int a = seg * g.kbs;
     const int slot = contrib_slot(blockIdx.x, first_tile, a, g.T, gridDim.x);
     float* dst = part_base(kind) + ((size_t)seg * g.kbs + slot) * p.MB * kTileRows;
+    #pragma unroll 1
     for (int idx = tid; idx < p.B * kTileRows; idx += kConsumerWarps * 32) {
       const int b = idx / kTileRows, row = idx % kTileRows;
       dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
@@ -758,6 +771,7 @@ struct Consumer {
     if (kind != K_D) return n_contrib(grp * g.kbs, g.kbs, g.T, gridDim.x);
     int tot = 0;
     const int nv = g.T / g.tpe;
+#pragma unroll 1
     for (int v = 0; v < nv; ++v) {
       int seg = v * p.n_rb_d + grp;
       tot += n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
@@ -771,6 +785,7 @@ struct Consumer {
     const float* src = part_base(kind) + (size_t)seg * g.kbs * p.MB * kTileRows + (size_t)b * kTileRows + row;
     const size_t st = (size_t)p.MB * kTileRows;
     float s = 0.f;
+#pragma unroll 1
     for (int c0 = 0; c0 < nc; c0 += 8) {  // eight independent loads in flight, summed in slot order
       float v[8];
 #pragma unroll
@@ -1140,14 +1155,26 @@ struct Consumer {
           tmp[b * kTileRows + i] = v;
         }
         cons_sync();
-        if (tid < p.B) {
-          const int b = tid;
-          int best = 0;
-          for (int i = 1; i < kTileRows; ++i)
-            if (tmp[b * kTileRows + i] > tmp[b * kTileRows + best]) best = i;
-          unsigned long long key = ((unsigned long long)float_key(tmp[b * kTileRows + best]) << 32) |
-                                   (unsigned long long)(0xFFFFFFFFu - (unsigned)(grp * kTileRows + best));
-          atomicMax(p.amax + b, key);
+        // warp b: the block's largest logit of token b, ties to the lower row (each lane scans
+        // its rows in ascending order, the butterfly keeps the lower row of equal values)
+#pragma unroll 1
+        for (int b = warp; b < p.B; b += kConsumerWarps) {
+          float bv = tmp[b * kTileRows + lane];
+          int bi = lane;
+#pragma unroll
+          for (int j = 1; j < kTileRows / 32; ++j) {
+            const float x = tmp[b * kTileRows + lane + 32 * j];
+            if (x > bv) { bv = x; bi = lane + 32 * j; }
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+          }
+          if (lane == 0)
+            atomicMax(p.amax + b, ((unsigned long long)float_key(bv) << 32) |
+                                      (unsigned long long)(0xFFFFFFFFu - (unsigned)(grp * kTileRows + bi)));
         }
         cons_sync();
         if (tid == 0) {
@@ -1222,6 +1249,7 @@ struct Consumer {
         ok = 0;
       }
       if (ok) {
+#pragma unroll 1
         for (int i = lane; i < n; i += 32) {
           const WaitCond c = cond(i);
           m->wt_addr[i] = c.addr;
@@ -1324,11 +1352,20 @@ struct Consumer {
   __device__ void wait_o_groups(int l) {
     const StageGeo go = stage_geo(p, K_O, 0);
     const int t0 = range_lo(go.T, blockIdx.x, gridDim.x), t1 = range_lo(go.T, blockIdx.x + 1, gridDim.x);
+    // the tiles' k blocks (input columns) kb_a .. kb_b, wrapping at kbs, all of them when the
+    // range spans a whole row block; k block kb reads the heads of groups grp_lo(kb) .. grp_hi(kb)
+    auto grp_lo = [&](int kb) { return kb * kTileK / HD / G; };
+    auto grp_hi = [&](int kb) { return ((kb + 1) * kTileK - 1) / HD / G; };
+    auto bits = [](int lo, int hi) { return (2ull << hi) - (1ull << lo); };  // bits lo..hi, hi <= 63
     unsigned long long mask = 0;
-    const int span = min(t1 - t0, go.kbs);
-    for (int i = 0; i < span; ++i) {
-      const int kb = (t0 + i) % go.kbs;
-      for (int h = kb * kTileK / HD; h <= ((kb + 1) * kTileK - 1) / HD; ++h) mask |= 1ull << (h / G);
+    if (t1 > t0) {
+      const int kb_a = t0 % go.kbs, kb_b = (t1 - 1) % go.kbs;
+      if (t1 - t0 >= go.kbs)
+        mask = bits(0, grp_hi(go.kbs - 1));
+      else if (kb_a <= kb_b)
+        mask = bits(grp_lo(kb_a), grp_hi(kb_b));
+      else
+        mask = bits(grp_lo(kb_a), grp_hi(go.kbs - 1)) | bits(0, grp_hi(kb_b));
     }
     // condition i = (sequence b, KV head g) for the flagged groups; unflagged groups pass at once
     const unsigned* f = p.o_flag + (size_t)l * p.MB * p.hkv;
@@ -1532,6 +1569,7 @@ struct Consumer {
           for (int j = 0; j < kMergeBatch; ++j)
             mv[i][j] = (idx < G * HD && j < p.nch) ? ldcg(src + ((size_t)j * G + h) * (HD + 2) + d) : 0.f;
         }
+        #pragma unroll 1
         for (int idx = tid; idx < G * p.nch; idx += 256) {
           const int h = idx / p.nch, c = idx % p.nch;
           const float* r = src + ((size_t)c * G + h) * (HD + 2);
