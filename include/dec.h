@@ -117,7 +117,11 @@ dec_status dec_validate_cfg(const dec_model_cfg* cfg);
    KV cache [n_layers][max_batch][n_kv_heads][max_ctx][head_dim] bf16 x2 and the workspace, and
    checks that one CTA per SM can be co-resident. All sequence lengths start at 0. Work is
    queued on `stream` and synchronised before return. *out receives the engine (NULL on
-   failure). */
+   failure).
+   Environment, read here: DEC_TIMEOUT_MS bounds every device-side wait (default 1000);
+   DEC_EPOCH_LIMIT lowers the number of steps after which a step first zeroes the engine's
+   cross-step counters and flags (a cudaMemsetAsync on the step's stream) and restarts its epoch
+   (default 2^30 / the largest number of k blocks of a row block), so tests can make it happen. */
 dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* weights, void* stream,
                     dec_engine** out);
 

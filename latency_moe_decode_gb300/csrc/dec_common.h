@@ -18,6 +18,7 @@ constexpr int kTileBytes = kTileData + 16;     // 16400
 // 32 KB slots ~7.0 TB/s).
 constexpr int kSlotTiles = 2;
 constexpr int kSlotBytes = kSlotTiles * kTileBytes;  // 32800
+constexpr int kSlotsInFlight = 2;                     // copies a CTA keeps in flight (at most)
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kKvTilePos = 64;                       // KV positions per ring slot
@@ -60,6 +61,7 @@ struct KParams {
   int umax;       // most distinct routed experts one step can select
   int nch;        // attention chunks per (sequence, KV head)
   int ring;       // ring slots
+  int inflight;   // most slot copies of one CTA in flight at a time (1..ring)
   int xmax;       // elements per token of the shared-memory activation buffer
   // weights and tables
   const LayerDev* layers;

@@ -132,6 +132,11 @@ struct dec_engine {
   int nch_max = 1;
   std::vector<int32_t> lengths;
   unsigned epoch = 0;
+  // Counters that grow across steps (each arrival adds its tile count, at most kbs per row block
+  // and step) and flags that hold the step's epoch. They are zeroed and the epoch restarts at 1
+  // before a counter could leave the int range.
+  unsigned epoch_limit = 0;
+  std::vector<std::pair<void*, size_t>> epoch_bufs;
   bool poisoned = false;
   std::string err;
   int32_t* d_hist = nullptr;
@@ -563,6 +568,17 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d);
     Z(p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu);
     Z(p.cnt_router, sizeof(int) * c.n_layers);
+    e->epoch_bufs = {{p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv},
+                     {p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d},
+                     {p.cnt_router, sizeof(int) * c.n_layers},
+                     {p.o_flag, sizeof(unsigned) * (size_t)c.n_layers * MB * c.n_kv_heads},
+                     {p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d},
+                     {p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu}};
+    e->epoch_limit = (1u << 30) / (unsigned)std::max({p.kb_d, p.kb_o, 1});
+    if (const char* el = getenv("DEC_EPOCH_LIMIT")) {  // a smaller limit, for testing the restart
+      const long v = atol(el);
+      if (v >= 1 && (unsigned long)v < e->epoch_limit) e->epoch_limit = (unsigned)v;
+    }
     Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
     Z(p.cnt_rtgu, sizeof(int) * std::max(1, p.umax) * p.n_rb_gu);
     Z(p.cnt_d, sizeof(int) * p.n_rb_d);
@@ -655,10 +671,18 @@ dec_status dec_step_ex(dec_engine* e, const dec_step_args* a) {
   p.logits = a->logits;
   p.next_tokens = a->next_tokens;
   p.hidden_out = static_cast<uint16_t*>(a->hidden_out);
+  cudaStream_t s = a->stream ? static_cast<cudaStream_t>(a->stream) : e->stream;
+  if (e->epoch >= e->epoch_limit) {
+    for (const auto& b : e->epoch_bufs) {
+      cudaError_t me = cudaMemsetAsync(b.first, 0, b.second, s);
+      if (me != cudaSuccess) return cuda_fail(e, me, "epoch restart");
+    }
+    e->epoch = 0;
+  }
   p.epoch = ++e->epoch;
   p.ring = e->ring[bi];
+  p.inflight = std::min(p.ring, kSlotsInFlight);
   p.nch = std::max(1, std::min(e->nch_max, e->grid / (a->batch * c.n_kv_heads)));
-  cudaStream_t s = a->stream ? static_cast<cudaStream_t>(a->stream) : e->stream;
   void* args[] = {&p};
   cudaError_t ce = cudaLaunchCooperativeKernel((const void*)e->kern[bi], dim3(e->grid), dim3(kThreads), args,
                                                (size_t)e->smem[bi], s);

@@ -222,6 +222,9 @@ struct Producer {
   unsigned item = 0;  // slots issued so far in this step
   int pslot = 0;      // ring slot of the next item (item % ring, kept without divisions)
   unsigned plap = 0;  // times the ring has wrapped (item / ring)
+  unsigned landed = 0;  // issued slots seen to have landed, in issue order
+  int lslot = 0;        // ring slot of item `landed`
+  unsigned llap = 0;    // its lap (landed / ring)
   bool dead = false;
   int stamp = 0;
 
@@ -245,8 +248,26 @@ struct Producer {
     return a >= b && a + bytes <= b + extent && (a & 15u) == 0 && (bytes & 15u) == 0;
   }
 
-  // claim the next slot: wait until the consumers released it
+  // claim the next slot: wait until at most p.inflight - 1 of the CTA's copies are still in
+  // flight, then until the consumers released the slot.
+  // The cap matters when a stage starts: every CTA finds several free slots at the same moment,
+  // and the memory system serves all the copies it is handed interleaved, so a whole ring's
+  // worth from every CTA would make even each CTA's first slot land only when nearly all of it
+  // has. With a few copies per CTA in flight (enough to keep the memory busy), the first slots
+  // land after about one unloaded latency and the rest follow at the rate they are consumed.
+  // (p.inflight <= ring: the slot of item `landed` is never re-armed before it is checked.)
   __device__ bool claim(int& slot) {
+    while (item - landed >= (unsigned)p.inflight) {
+      if (!mbar_wait(&full[lslot], llap & 1, p, 12)) {
+        dead = true;
+        return false;
+      }
+      ++landed;
+      if (++lslot == p.ring) {
+        lslot = 0;
+        ++llap;
+      }
+    }
     slot = pslot;
     if (plap > 0) {
       if (!mbar_wait(&empty[slot], (plap - 1) & 1, p, 10)) {
@@ -488,7 +509,7 @@ struct Consumer {
     if (from_o) {
       const int* cnt = p.cnt_o + (size_t)l_src * p.n_rb_d;
       cta_wait_all(p.n_rb_d, [&](int rb) {
-        return count_reached(cnt + rb, (int)p.epoch * n_contrib(rb * go.kbs, go.kbs, go.T, gridDim.x));
+        return count_reached(cnt + rb, (int)p.epoch * go.kbs);
       }, 18);
     }
     // the norm weights of this thread's chunks, loaded once, in flight with the first activations
@@ -741,7 +762,7 @@ struct Consumer {
     return g.T / g.kbs;
   }
 
-  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, float (&acc)[BM]) {
+  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, int ntiles, float (&acc)[BM]) {
     // red[column half][row][b]: warp w holds row 32 * (w & 3) + lane of column half w >> 2
 #pragma unroll
     for (int b = 0; b < BM; ++b) red[((size_t)(warp >> 2) * kTileRows + (warp & 3) * 32 + lane) * BM + b] = acc[b];
@@ -755,28 +776,22 @@ struct Consumer {
       dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
     }
     // The CTA barrier orders every thread's partial before thread 0's releasing arrival; no
-    // thread waits for the arrival to complete.
+    // thread waits for the arrival to complete. An arrival adds the number of the segment's
+    // tiles the CTA summed, so a group is complete when its counter has grown by its tile count
+    // (kbs per segment), however the tiles were split among the CTAs.
     cons_sync();
     if (dead) return;
     if (kind == K_QKV || kind == K_O || kind == K_ROUTER) {
-      // published partials: the readers wait for every contributor of the row block
-      if (tid == 0) red_release_add(pub_counter(kind, l) + seg, 1);
+      // published partials: the readers wait for all of the row block's tiles
+      if (tid == 0) red_release_add(pub_counter(kind, l) + seg, ntiles);
       return;
     }
-    if (tid == 0) red_release_add(cnt_base(kind) + seg_group(kind, seg), 1);
+    if (tid == 0) red_release_add(cnt_base(kind) + seg_group(kind, seg), ntiles);
   }
 
-  // number of arrivals that complete an output group
+  // counter value that completes an output group: its tiles (D: one segment per expert)
   __device__ int group_expected(int kind, const StageGeo& g, int grp) const {
-    if (kind != K_D) return n_contrib(grp * g.kbs, g.kbs, g.T, gridDim.x);
-    int tot = 0;
-    const int nv = g.T / g.tpe;
-#pragma unroll 1
-    for (int v = 0; v < nv; ++v) {
-      int seg = v * p.n_rb_d + grp;
-      tot += n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
-    }
-    return tot;
+    return kind == K_D ? g.T / g.tpe * g.kbs : g.kbs;
   }
 
   // sum of the published partials of segment seg for (b, row)
@@ -879,7 +894,7 @@ struct Consumer {
           if (kind == K_RTGU || (kind == K_SHGU && p.dense)) cta_stamp(l, S_GU_TILES);
           if (kind == K_D) cta_stamp(l, S_D_TILES);
         }
-        if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, acc);
+        if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, t - seg_first, acc);
         if (t == t1) break;
         seg_cur = seg;
         seg_first = t;
@@ -906,20 +921,31 @@ struct Consumer {
     }
     // Finalise the output groups this CTA is designated for (groups spread evenly over the
     // CTAs, so no CTA finalises two while others finalise none): wait (acquire) until every
-    // contributor has arrived, finalise, and reset the counter for the next launch (nothing else
-    // touches it before then: every later arrival on it depends on this group's result). No
-    // contributor ever waits for the result of its own arrival.
-    const int ng = (kind == K_QKV || kind == K_O || kind == K_ROUTER) ? 0 : n_groups(kind, g);
+    // contributor has arrived, reset the counter for the next launch or layer (before the
+    // result is published, and nothing else touches it before then: every later arrival on it
+    // depends on this group's result), finalise. No contributor ever waits for the result of its
+    // own arrival.
+    // The SwiGLU groups of an MoE layer, routed experts' and shared experts' alike, are all
+    // finalised after the routed gate/up stage, together (see finalize_gu): a CTA designated for
+    // a shared-expert group then does not start its routed tiles late.
+    const bool gu = kind == K_RTGU || (kind == K_SHGU && p.dense);
+    int ng = 0;
+    if (kind == K_RTGU) ng = (U + (p.nsh ? 1 : 0)) * p.n_rb_gu;
+    else if (gu || kind == K_D || kind == K_LM) ng = n_groups(kind, g);
     const int f_lo = (int)(((long long)blockIdx.x * ng + G_ - 1) / G_);
     const int f_hi = (int)(((long long)(blockIdx.x + 1) * ng + G_ - 1) / G_);
-    for (int grp = f_lo; grp < f_hi && !dead; ++grp) {
-      const int* c = cnt_base(kind) + grp;
-      const int want = group_expected(kind, g, grp);
-      cta_wait_all(1, [&](int) { return count_reached(c, want); }, 21);
-      if (dead) break;
-      finalize(kind, l, g, grp, U);
-      cons_sync();
-      if (tid == 0) *const_cast<volatile int*>(c) = 0;
+    if (gu) {
+      if (f_hi > f_lo && !dead) finalize_gu(l, f_lo, f_hi, U);
+    } else {
+      for (int grp = f_lo; grp < f_hi && !dead; ++grp) {
+        const int* c = cnt_base(kind) + grp;
+        const int want = group_expected(kind, g, grp);
+        cta_wait_all(1, [&](int) { return count_reached(c, want); }, 21);
+        if (dead) break;
+        if (tid == 0) *const_cast<volatile int*>(c) = 0;
+        finalize(kind, l, g, grp, U);
+        cons_sync();
+      }
     }
     trace(kind << 4 | 2);
   }
@@ -936,7 +962,7 @@ struct Consumer {
     const StageGeo g = stage_geo(p, K_ROUTER, 0);
     const int nc = n_contrib(0, g.kbs, g.T, gridDim.x);
     const int* cnt = p.cnt_router + l;
-    cta_wait_all(1, [&](int) { return count_reached(cnt, (int)p.epoch * nc); }, 19);
+    cta_wait_all(1, [&](int) { return count_reached(cnt, (int)p.epoch * g.kbs); }, 19);
     float* tmp = red;                                        // [BM][128] logits
     int* mark = reinterpret_cast<int*>(tmp + BM * kTileRows);  // [128] rank + 1 of expert e
     int* sel = mark + kMaxExperts;                              // [BM][16]
@@ -1038,39 +1064,60 @@ struct Consumer {
     if (tid == 0) mbar_arrive(&m->rt_bar);  // the producer may now issue the routed experts
   }
 
-  // -------- finalisers (run by the CTA whose arrival completed an output group) --------
+  // -------- finalisers (run by the CTA designated for an output group) --------
+
+  // SwiGLU of the gate/up groups vlo..vhi-1 of layer l, all at once: one wait for all of their
+  // counters, one pass over their rows. Groups v < U * n_rb_gu are routed (expert slot
+  // v / n_rb_gu, row block v % n_rb_gu), the rest the shared experts' (or the dense FFN's) row
+  // blocks. Each row block holds 64 gate rows then the matching 64 up rows;
+  // h = bf16(silu(gate) * up) from the contributor partials summed in slot order.
+  __device__ void finalize_gu(int l, int vlo, int vhi, int U) {
+    const int half = kTileRows / 2;
+    const int nr = U * p.n_rb_gu;
+    const StageGeo gr = stage_geo(p, K_RTGU, U), gs = stage_geo(p, K_SHGU, 0);
+    cta_wait_all(vhi - vlo, [&](int i) {
+      const int v = vlo + i;
+      return v < nr ? count_reached(p.cnt_rtgu + v, group_expected(K_RTGU, gr, v))
+                    : count_reached(p.cnt_shgu + (v - nr), group_expected(K_SHGU, gs, v - nr));
+    }, 21);
+    if (dead) return;
+    if (tid == 0) {
+#pragma unroll 1
+      for (int v = vlo; v < vhi; ++v) *const_cast<volatile int*>(v < nr ? p.cnt_rtgu + v : p.cnt_shgu + (v - nr)) = 0;
+    }
+    const int per = p.B * half;
+#pragma unroll 1
+    for (int idx = tid; idx < (vhi - vlo) * per; idx += kConsumerWarps * 32) {
+      const int v = vlo + idx / per, r = idx % per;
+      const int b = r / half, i = r % half;
+      const bool sh = v >= nr;
+      const int grp = sh ? v - nr : v;
+      float gv, uv;
+      seg_sum2(sh ? K_SHGU : K_RTGU, sh ? gs : gr, grp, b, i, i + half, gv, uv);
+      const uint16_t h = f2bf((gv / (1.0f + expf(-gv))) * uv);
+      const int j = (sh ? grp : grp % p.n_rb_gu) * half + i;
+      if (sh)
+        p.hsh[(size_t)b * p.inter + j] = h;
+      else
+        p.hrt[((size_t)(grp / p.n_rb_gu) * p.MB + b) * p.inter + j] = h;
+    }
+    cons_sync();
+    if (tid == 0) {
+      __threadfence();
+      // flag of group v: h_flag[l][slot][rb], slot = v / n_rb_gu (the shared experts' slot umax
+      // after the routed ones), walked without divisions
+      unsigned* f = p.h_flag + (size_t)l * (p.umax + 1) * p.n_rb_gu;
+#pragma unroll 1
+      for (int v = vlo; v < vhi; ++v)
+        st_release(f + (v < nr ? v : p.umax * p.n_rb_gu + (v - nr)), p.epoch);
+    }
+  }
+
+  // Output-projection row block (D: residual + down projections) or LM-head block grp.
 
   __device__ void finalize(int kind, int l, const StageGeo& g, int grp, int U) {
     float* tmp = red;  // [BM][128]
     switch (kind) {
-      case K_SHGU:
-      case K_RTGU: {
-        const int half = kTileRows / 2;
-        int seg = grp;
-        int u = 0, rb = grp;
-        if (kind == K_RTGU) {
-          u = grp / p.n_rb_gu;
-          rb = grp % p.n_rb_gu;
-        }
-        for (int idx = tid; idx < p.B * half; idx += 256) {
-          int b = idx / half, i = idx % half;
-          float gv, uv;
-          seg_sum2(kind, g, seg, b, i, i + half, gv, uv);
-          float h = (gv / (1.0f + expf(-gv))) * uv;
-          int j = rb * half + i;
-          if (kind == K_SHGU)
-            p.hsh[(size_t)b * p.inter + j] = f2bf(h);
-          else
-            p.hrt[((size_t)u * p.MB + b) * p.inter + j] = f2bf(h);
-        }
-        cons_sync();
-        if (tid == 0) {
-          __threadfence();
-          const int slot = kind == K_SHGU ? p.umax : u;
-          st_release(p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch);
-        }
-        break;
-      }
       case K_D: {
         const int nv = g.T / g.tpe;
         // every expert's contributor slots for this row block, as offsets into the partials:
@@ -1283,7 +1330,7 @@ struct Consumer {
       const int* cnt = p.cnt_qkv + (size_t)l * p.n_rb_qkv;
       cta_wait_all(qn + kn + vn, [&](int i) {
         const int rb = i < qn ? qa + i : (i < qn + kn ? ka + i - qn : va + i - qn - kn);
-        return count_reached(cnt + rb, (int)p.epoch * n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x));
+        return count_reached(cnt + rb, (int)p.epoch * gq.kbs);
       }, 13);
     }
     // Each thread sums the contributor partials of its NPT values. All loads of a batch of eight
