@@ -90,13 +90,13 @@ struct KParams {
   // router partials: growing counter per layer [L]. Finalised outputs (SwiGLU h, down projection +
   // residual, logits): arrival counters that the group's designated finaliser waits on and resets
   int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
-  unsigned* o_flag;  // [L][MB][hkv] = epoch once the attention output of (sequence, KV head) is merged
+  int* o_cnt;  // [L][MB][hkv] chunk slices of the merged attention output written (zero between launches)
   unsigned* x_flag;  // [L][n_rb_d] = epoch once a row block of the layer's output is final
   unsigned* h_flag;  // [L][umax + 1][n_rb_gu] = epoch once an expert's 64 SwiGLU rows are final
                      // (slot umax: the shared / dense expert)
   // attention split-KV partials: [MB][hkv][nch][group][hd + 2], counters [MB][hkv]
   float* attn_part;
-  int* attn_cnt;
+  int* attn_cnt;  // [L][MB][hkv] chunk partials published (zero between launches)
   // routing of each layer, written by CTA 0 for inspection (every CTA computes it itself)
   int* rt_idx;        // [L][MB][topk] selections (score-descending)
   float* rt_topk_gate;// [L][MB][topk]

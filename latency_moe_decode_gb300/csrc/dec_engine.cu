@@ -564,21 +564,15 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.part_lm, fb * std::max(1, p.n_rb_lm) * p.kb_d);
     Z(p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv);
     Z(p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d);
-    Z(p.o_flag, sizeof(unsigned) * (size_t)c.n_layers * MB * c.n_kv_heads);
+    Z(p.o_cnt, sizeof(int) * (size_t)c.n_layers * MB * c.n_kv_heads);
     Z(p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d);
     Z(p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu);
     Z(p.cnt_router, sizeof(int) * c.n_layers);
     e->epoch_bufs = {{p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv},
                      {p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d},
                      {p.cnt_router, sizeof(int) * c.n_layers},
-                     {p.o_flag, sizeof(unsigned) * (size_t)c.n_layers * MB * c.n_kv_heads},
                      {p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d},
                      {p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu}};
-    e->epoch_limit = (1u << 30) / (unsigned)std::max({p.kb_d, p.kb_o, 1});
-    if (const char* el = getenv("DEC_EPOCH_LIMIT")) {  // a smaller limit, for testing the restart
-      const long v = atol(el);
-      if (v >= 1 && (unsigned long)v < e->epoch_limit) e->epoch_limit = (unsigned)v;
-    }
     Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
     Z(p.cnt_rtgu, sizeof(int) * std::max(1, p.umax) * p.n_rb_gu);
     Z(p.cnt_d, sizeof(int) * p.n_rb_d);
@@ -586,7 +580,13 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.cnt_lm_done, sizeof(int) * 32);
     e->nch_max = std::max(1, G / c.n_kv_heads);
     Z(p.attn_part, sizeof(float) * MB * c.n_kv_heads * e->nch_max * e->group * (c.head_dim + 2));
-    Z(p.attn_cnt, sizeof(int) * MB * c.n_kv_heads);
+    Z(p.attn_cnt, sizeof(int) * (size_t)c.n_layers * MB * c.n_kv_heads);
+    // per step a growing counter gains at most max(kb_d, kb_o)
+    e->epoch_limit = (1u << 30) / (unsigned)std::max({p.kb_d, p.kb_o, 1});
+    if (const char* el = getenv("DEC_EPOCH_LIMIT")) {  // a smaller limit, for testing the restart
+      const long v = atol(el);
+      if (v >= 1 && (unsigned long)v < e->epoch_limit) e->epoch_limit = (unsigned)v;
+    }
     Z(p.rt_idx, sizeof(int) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.amax, sizeof(unsigned long long) * MB);

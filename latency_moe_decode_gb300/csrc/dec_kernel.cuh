@@ -511,6 +511,15 @@ struct Consumer {
       cta_wait_all(p.n_rb_d, [&](int rb) {
         return count_reached(cnt + rb, (int)p.epoch * go.kbs);
       }, 18);
+      // Every output-projection tile has arrived, and each waited for the attention merges it
+      // reads (together: all of layer l_src's), each merge having waited for all of its chunks.
+      // So no CTA reads or adds to the layer's attention counters again in this launch: they
+      // are zeroed here for the next one.
+      if (tid == 0 && !dead)
+        for (int i = blockIdx.x; i < p.B * p.hkv; i += gridDim.x) {
+          p.attn_cnt[(size_t)l_src * p.MB * p.hkv + i] = 0;
+          p.o_cnt[(size_t)l_src * p.MB * p.hkv + i] = 0;
+        }
     }
     // the norm weights of this thread's chunks, loaded once, in flight with the first activations
     uint4 wv[MAXV];
@@ -1307,8 +1316,9 @@ struct Consumer {
       }
       if (lane == 0) m->flag = ok;
     }
-    cons_sync();
-    if (!m->flag) dead = true;
+    // every consumer thread leaves with the same verdict (one of them may have given up on a
+    // ring slot before), so branches on `dead` after a wait are uniform
+    dead = cons_any(dead) || !m->flag;
   }
 
   // a wait condition: a counter reaching target, or a flag reaching a value
@@ -1415,10 +1425,10 @@ struct Consumer {
         mask = bits(grp_lo(kb_a), grp_hi(go.kbs - 1)) | bits(0, grp_hi(kb_b));
     }
     // condition i = (sequence b, KV head g) for the flagged groups; unflagged groups pass at once
-    const unsigned* f = p.o_flag + (size_t)l * p.MB * p.hkv;
+    const int* f = p.o_cnt + (size_t)l * p.MB * p.hkv;
     cta_wait_all(p.B * p.hkv, [&](int i) {
       const int b = i / p.hkv, g = i % p.hkv;
-      return ((mask >> g) & 1ull) ? WaitCond{f + (size_t)b * p.hkv + g, p.epoch} : WaitCond{nullptr, 0u};
+      return ((mask >> g) & 1ull) ? count_reached(f + (size_t)b * p.hkv + g, p.nch) : WaitCond{nullptr, 0u};
     }, 16);
   }
 
@@ -1588,75 +1598,77 @@ struct Consumer {
           dst[(size_t)h * (HD + 2) + HD + 1] = Lsum;
         }
       }
-      // publish: the CTA barrier orders every thread's partial before thread 0's fence and
-      // arrival; the last arriver's acquiring arrival orders its reads after all chunks
+      // publish: the CTA barrier orders every thread's partial before thread 0's releasing
+      // arrival (the layer's counters start the launch at zero, see stage_rmsnorm)
       cons_sync();
-      int* cnt = p.attn_cnt + (size_t)a.b * p.hkv + a.g;
-      if (tid == 0 && !dead) red_release_add(cnt, 1);
-      // the unit of the last chunk merges (it waits for every chunk's arrival)
-      if (a.c == p.nch - 1 && !dead) {
-        cta_wait_all(1, [&](int) { return count_reached(cnt, p.nch); }, 23);
-      }
-      if (a.c == p.nch - 1 && !dead) {
-        const float* src = p.attn_part + (((size_t)a.b * p.hkv + a.g) * p.nch * G) * (HD + 2);
-        // Chunk merge. The chunk accumulators of the thread's (head, dim) pairs for the first
-        // kMergeBatch chunks are loaded first and the chunk maxima / sums after them, all in
-        // flight together; the weights exp2(m_c - M) / L go through shared memory.
-        constexpr int PER = (G * HD + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+      const size_t gi = ((size_t)l * p.MB + a.b) * p.hkv + a.g;
+      if (tid == 0 && !dead) red_release_add(p.attn_cnt + gi, 1);
+      // Chunk merge, shared by the group's nch units (with nch > 1 the host makes every unit a
+      // CTA of its own, so a CTA waits only for others' chunks): unit c merges the outputs
+      // [o_lo, o_hi) = [c * G*HD / nch, (c+1) * G*HD / nch) of the group's G*HD (head o / HD, dim
+      // o % HD) once every chunk has arrived, and arrives on the group's merged counter. Weights
+      // per head h: w_c = exp2(m_c - M) / L with M = max_c m_c, L = sum_c exp2(m_c - M) l_c (warp
+      // h - h_lo reduces them over the chunks, in a fixed order); output o = sum_c w_c acc_c[o],
+      // in chunk order.
+      cta_wait_all(1, [&](int) { return count_reached(p.attn_cnt + gi, p.nch); }, 23);
+      if (!dead) {  // (uniform across the CTA after a wait)
         constexpr int kMergeBatch = 24;
-        float* cm = red;                  // [G][nch]
-        float* cl = red + G * p.nch;      // [G][nch]
-        float* cw = red + 2 * G * p.nch;  // [G][nch] weights exp2(m_c - M) / L
-        float mv[PER][kMergeBatch];
+        const int o_lo = range_lo(G * HD, a.c, p.nch), o_hi = range_lo(G * HD, a.c + 1, p.nch);
+        const int h_lo = o_lo / HD, nh = o_hi > o_lo ? (o_hi - 1) / HD - h_lo + 1 : 0;
+        const float* src = p.attn_part + ((size_t)a.b * p.hkv + a.g) * p.nch * G * (HD + 2);
+        const size_t cst = (size_t)G * (HD + 2);  // chunk stride
+        float* cw = red;                          // [nh][nch] weights
+        // the first output of this thread: its chunk values are loaded before the weights are
+        // formed, all in flight together (one pass covers the slice unless nch is tiny)
+        int o = o_lo + tid;
+        const float* vsrc = src + (size_t)(o / HD) * (HD + 2) + o % HD;
+        float mv[kMergeBatch];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int idx = tid + i * kConsumerWarps * 32;
-          const int h = idx / HD, d = idx % HD;
+        for (int j = 0; j < kMergeBatch; ++j) mv[j] = (o < o_hi && j < p.nch) ? ldcg(vsrc + (size_t)j * cst) : 0.f;
+#pragma unroll 1
+        for (int hh = warp; hh < nh; hh += kConsumerWarps) {
+          const float* ms = src + (size_t)(h_lo + hh) * (HD + 2) + HD;  // (m, l) of chunk 0
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int c = lane; c < p.nch; c += 32) mx = fmaxf(mx, ldcg(ms + (size_t)c * cst));
 #pragma unroll
-          for (int j = 0; j < kMergeBatch; ++j)
-            mv[i][j] = (idx < G * HD && j < p.nch) ? ldcg(src + ((size_t)j * G + h) * (HD + 2) + d) : 0.f;
-        }
-        #pragma unroll 1
-        for (int idx = tid; idx < G * p.nch; idx += 256) {
-          const int h = idx / p.nch, c = idx % p.nch;
-          const float* r = src + ((size_t)c * G + h) * (HD + 2);
-          const float mm = ldcg(r + HD), ll = ldcg(r + HD + 1);
-          cm[idx] = mm;
-          cl[idx] = ll;
-        }
-        cons_sync();
-        for (int idx = tid; idx < G * p.nch; idx += 256) {
-          const int h = idx / p.nch;
-          float M = -INFINITY;
-          for (int c2 = 0; c2 < p.nch; ++c2) M = fmaxf(M, cm[h * p.nch + c2]);
-          float Lsum = 0.f;
-          for (int c2 = 0; c2 < p.nch; ++c2) {
-            const float mc = cm[h * p.nch + c2];
-            if (mc != -INFINITY) Lsum = fmaf(exp2f(mc - M), cl[h * p.nch + c2], Lsum);
+          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          float ls = 0.f;
+#pragma unroll 1
+          for (int c = lane; c < p.nch; c += 32) {
+            const float mc = ldcg(ms + (size_t)c * cst);
+            if (mc != -INFINITY) ls = fmaf(exp2f(mc - mx), ldcg(ms + (size_t)c * cst + 1), ls);
           }
-          const float mc = cm[idx];
-          cw[idx] = (mc == -INFINITY || !(Lsum > 0.f)) ? 0.f : exp2f(mc - M) / Lsum;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+#pragma unroll 1
+          for (int c = lane; c < p.nch; c += 32) {
+            const float mc = ldcg(ms + (size_t)c * cst);
+            cw[hh * p.nch + c] = (mc == -INFINITY || !(ls > 0.f)) ? 0.f : exp2f(mc - mx) / ls;
+          }
         }
         cons_sync();
+#pragma unroll 1
+        for (; o < o_hi; o += kConsumerWarps * 32) {
+          if (o != o_lo + tid) {
+            vsrc = src + (size_t)(o / HD) * (HD + 2) + o % HD;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int idx = tid + i * kConsumerWarps * 32;
-          if (idx >= G * HD) break;
-          const int h = idx / HD, d = idx % HD;
+            for (int j = 0; j < kMergeBatch; ++j) mv[j] = j < p.nch ? ldcg(vsrc + (size_t)j * cst) : 0.f;
+          }
+          const float* w = cw + (o / HD - h_lo) * p.nch;
           float A = 0.f;
 #pragma unroll
           for (int j = 0; j < kMergeBatch; ++j)
-            if (j < p.nch) A = fmaf(cw[h * p.nch + j], mv[i][j], A);
+            if (j < p.nch) A = fmaf(w[j], mv[j], A);
 #pragma unroll 1
           for (int c = kMergeBatch; c < p.nch; ++c)  // more chunks than one batch (small models)
-            A = fmaf(cw[h * p.nch + c], ldcg(src + ((size_t)c * G + h) * (HD + 2) + d), A);
-          p.obuf[(size_t)a.b * p.hq * HD + (size_t)(a.g * G + h) * HD + d] = f2bf(A);
+            A = fmaf(w[c], ldcg(vsrc + (size_t)c * cst), A);
+          p.obuf[(size_t)a.b * p.hq * HD + (size_t)a.g * G * HD + o] = f2bf(A);
         }
         cons_sync();
         if (tid == 0) {
-          *const_cast<volatile int*>(cnt) = 0;
           __threadfence();
-          st_release(p.o_flag + ((size_t)l * p.MB + a.b) * p.hkv + a.g, p.epoch);
+          red_release_add(p.o_cnt + gi, 1);
         }
       }
       cons_sync();

@@ -165,6 +165,19 @@ __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ uint4 ldcg4(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ uint16_t ldcg_u16(const uint16_t* p) { return __ldcg(p); }
 
+// Consumer-warp barrier (named barrier 1, 256 threads) that also returns whether v held in any
+// of the consumer threads.
+__device__ __forceinline__ bool cons_any(bool v) {
+  unsigned r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((unsigned)v), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
 // Consumer warps only (named barrier 1, 256 threads).
 __device__ __forceinline__ void cons_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
