@@ -598,15 +598,16 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   }
 
   // ---- activation buffer width: d, n_heads*head_dim, or the experts a CTA's down range spans
+  // (down tiles are row-block major: run s of kb_i tiles belongs to expert slot s % nv)
   {
     int xmax = std::max(c.hidden, c.n_heads * c.head_dim);
-    const int tpe = p.n_rb_d * p.kb_i;
     int span = 1;
     for (int U = 0; U <= p.umax; ++U) {
-      const int T = (U + p.nsh) * tpe;
+      const int nv = U + p.nsh;
+      const int T = p.n_rb_d * nv * p.kb_i;
       for (int cta = 0; cta < G; ++cta) {
         int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
-        if (t1 > t0) span = std::max(span, (t1 - 1) / tpe - t0 / tpe + 1);
+        if (t1 > t0) span = std::max(span, std::min((t1 - 1) / p.kb_i - t0 / p.kb_i + 1, nv));
       }
     }
     xmax = std::max(xmax, span * p.inter);

@@ -41,7 +41,6 @@ struct SmemLayout {
 };
 
 constexpr int kMaxExperts = 128;
-constexpr int kListCap = 1024;  // contributor slots one down-projection row block may gather
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
 constexpr int kWaitMax = 128;  // conditions one CTA-wide wait may span
@@ -53,7 +52,6 @@ struct Misc {
   int flag;
   int nfin;
   int U;
-  int v_lo;
   int len[kMaxBatch];
   int elist[kMaxExperts];
   float gate[kMaxBatch][kMaxExperts + 1];
@@ -77,7 +75,7 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   s.red_off = align_up(s.xs_off + bm * xmax * 2, 128);
   int red_gemv = 2 * kTileRows * bm * 4;
   int red_attn = kConsumerWarps * group * (hd + 2) * 4;
-  int red_fin = (bm * kTileRows + kListCap + 16) * 4;
+  int red_fin = (bm * kTileRows + 16) * 4;
   int red = red_gemv > red_attn ? red_gemv : red_attn;
   red = red > red_fin ? red : red_fin;
   s.misc_off = align_up(s.red_off + red, 128);
@@ -128,8 +126,8 @@ __device__ __forceinline__ int contrib_slot(int c, int f, int a, int T, int G) {
 
 struct StageGeo {
   int T;    // tiles
-  int kbs;  // tiles per segment
-  int tpe;  // tiles per expert (routed / down stages)
+  int kbs;  // tiles per segment (the k blocks one output row block sums)
+  int tpe;  // routed gate/up: tiles per expert; down: tiles per expert within a segment (kb_i)
 };
 
 __device__ __forceinline__ StageGeo stage_geo(const KParams& p, int kind, int U) {
@@ -141,18 +139,22 @@ __device__ __forceinline__ StageGeo stage_geo(const KParams& p, int kind, int U)
     case K_ROUTER: g.kbs = p.kb_d; g.T = p.n_rb_router * p.kb_d; break;
     case K_SHGU: g.kbs = p.kb_d; g.T = p.n_rb_gu * p.kb_d; break;
     case K_RTGU: g.kbs = p.kb_d; g.tpe = p.n_rb_gu * p.kb_d; g.T = U * g.tpe; break;
-    case K_D: g.kbs = p.kb_i; g.tpe = p.n_rb_d * p.kb_i; g.T = (U + p.nsh) * g.tpe; break;
+    // down projections, row-block major: segment rb holds the k blocks of every active expert
+    // (routed slots 0..U-1, then the shared one), kb_i each, so one output row block's tiles are
+    // contiguous and are split among few CTAs
+    case K_D: g.tpe = p.kb_i; g.kbs = (U + p.nsh) * p.kb_i; g.T = p.n_rb_d * g.kbs; break;
     default: g.kbs = p.kb_d; g.T = p.n_rb_lm * p.kb_d; break;
   }
   return g;
 }
 
 // Walks a stage's tiles in order (no divisions per tile). Plain stages are one contiguous run of
-// tiles; expert stages are a run of tpe tiles per expert slot u, at that expert's weights (the
-// shared / dense expert's after the routed ones for the down projections).
+// tiles; the routed gate/up stage is a run of tpe tiles per expert slot u, at that expert's
+// weights; the down stage is, per output row block rb, a run of kb_i tiles of each expert slot u
+// (the shared expert after the routed ones), at row block rb of that expert's weights.
 struct TileCursor {
   const uint8_t* addr;
-  int u, r;  // expert stages: expert slot and tile within it
+  int u, r, rb;  // expert stages: expert slot, tile within its run, (down) output row block
   __device__ __forceinline__ static const uint8_t* expert_base(const KParams& p, const LayerDev& Ld, int kind, int u,
                                                                int U, const int* elist) {
     if (kind == K_RTGU) return Ld.e_gu + (size_t)elist[u] * p.e_gu_stride;
@@ -160,10 +162,18 @@ struct TileCursor {
   }
   __device__ void init(const KParams& p, const LayerDev& Ld, int kind, int t, const StageGeo& g, int U,
                        const int* elist) {
-    if (kind == K_RTGU || kind == K_D) {
+    if (kind == K_RTGU) {
       u = t / g.tpe;
       r = t - u * g.tpe;
       addr = expert_base(p, Ld, kind, u, U, elist) + (size_t)r * kTileBytes;
+      return;
+    }
+    if (kind == K_D) {
+      rb = t / g.kbs;
+      const int k = t - rb * g.kbs;
+      u = k / g.tpe;
+      r = k - u * g.tpe;
+      addr = expert_base(p, Ld, kind, u, U, elist) + ((size_t)rb * g.tpe + r) * kTileBytes;
       return;
     }
     const uint8_t* base = kind == K_QKV ? Ld.qkv
@@ -179,10 +189,18 @@ struct TileCursor {
   __device__ __forceinline__ void next(const KParams& p, const LayerDev& Ld, int kind, const StageGeo& g, int U,
                                        const int* elist) {
     addr += kTileBytes;
-    if ((kind == K_RTGU || kind == K_D) && ++r == g.tpe) {
+    if (kind == K_RTGU && ++r == g.tpe) {
       r = 0;
       ++u;
       if (u * g.tpe < g.T) addr = expert_base(p, Ld, kind, u, U, elist);
+    }
+    if (kind == K_D && ++r == g.tpe) {
+      r = 0;
+      if (++u * g.tpe == g.kbs) {
+        u = 0;
+        ++rb;
+      }
+      if (rb < p.n_rb_d) addr = expert_base(p, Ld, kind, u, U, elist) + (size_t)rb * g.tpe * kTileBytes;
     }
   }
 };
@@ -752,10 +770,6 @@ struct Consumer {
       default: return p.cnt_lm;
     }
   }
-  // output group of a segment (D: the output row block shared by all experts)
-  __device__ __forceinline__ int seg_group(int kind, int seg) const {
-    return kind == K_D ? seg % p.n_rb_d : seg;
-  }
 
   // Cross-warp reduction of one segment's accumulators, publication of the CTA's partial sums,
   // and the arrival on the output group's counter (result kept for the end of the stage).
@@ -767,7 +781,6 @@ struct Consumer {
   // output groups of a finalised stage (SwiGLU row blocks of each expert, output row blocks,
   // vocabulary row blocks)
   __device__ __forceinline__ int n_groups(int kind, const StageGeo& g) const {
-    if (kind == K_D) return p.n_rb_d;
     return g.T / g.kbs;
   }
 
@@ -795,13 +808,11 @@ struct Consumer {
       if (tid == 0) red_release_add(pub_counter(kind, l) + seg, ntiles);
       return;
     }
-    if (tid == 0) red_release_add(cnt_base(kind) + seg_group(kind, seg), ntiles);
+    if (tid == 0) red_release_add(cnt_base(kind) + seg, ntiles);
   }
 
-  // counter value that completes an output group: its tiles (D: one segment per expert)
-  __device__ int group_expected(int kind, const StageGeo& g, int grp) const {
-    return kind == K_D ? g.T / g.tpe * g.kbs : g.kbs;
-  }
+  // counter value that completes an output group: its segment's tiles
+  __device__ int group_expected(int kind, const StageGeo& g, int grp) const { return g.kbs; }
 
   // sum of the published partials of segment seg for (b, row)
   __device__ __forceinline__ float seg_sum(int kind, const StageGeo& g, int seg, int b, int row) const {
@@ -879,15 +890,17 @@ struct Consumer {
     int seg_cur = -1, seg_first = 0;
     const uint8_t* slot_base = ring;
     // position of tile t, advanced without divisions: segment, k block within it, and for the
-    // down projection the expert (whose gates scale the tile) and the tile within the expert
+    // down projection the expert slot v (whose gates scale the tile), the k block kx within its
+    // run and the expert's place xj among the SwiGLU rows staged in xs (the CTA's runs in order,
+    // the first at 0, wrapping after nv)
     int seg = t1 > t0 ? t0 / g.kbs : 0, kb = t0 - seg * g.kbs;
-    int v = 0, rv = 0, xbase = 0;
+    int v = 0, kx = kb, xj = 0, xbase = 0;
+    const int nv = kind == K_D ? U + p.nsh : 1;
 #pragma unroll
     for (int b = 0; b < BM; ++b) gmul[b] = 1.f;
     if (kind == K_D && t1 > t0) {
-      v = t0 / g.tpe;
-      rv = t0 - v * g.tpe;
-      xbase = (v - m->v_lo) * p.inter;
+      v = kb / g.tpe;
+      kx = kb - v * g.tpe;
 #pragma unroll
       for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
     }
@@ -911,7 +924,7 @@ struct Consumer {
         for (int b = 0; b < BM; ++b) acc[b] = 0.f;
       }
       if (j == 0) slot_base = wait_item();
-      if (!dead) tile_dot(slot_base + (size_t)j * kTileBytes, xbase + kb * kTileK, gmul, acc);
+      if (!dead) tile_dot(slot_base + (size_t)j * kTileBytes, xbase + kx * kTileK, gmul, acc);
       if (++j == kSlotTiles || t == t1 - 1) {
         release_item();
         j = 0;
@@ -920,10 +933,13 @@ struct Consumer {
         kb = 0;
         ++seg;
       }
-      if (kind == K_D && ++rv == g.tpe) {
-        rv = 0;
-        ++v;
-        xbase = (v - m->v_lo) * p.inter;
+      if (kind != K_D) {
+        kx = kb;
+      } else if (++kx == g.tpe) {
+        kx = 0;
+        if (++v == nv) v = 0;
+        if (++xj == nv) xj = 0;
+        xbase = xj * p.inter;
 #pragma unroll
         for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
       }
@@ -1007,33 +1023,35 @@ struct Consumer {
     }
     if (tid < kMaxExperts) mark[tid] = 0;
     cons_sync();
-    if (warp < p.B) {
-      const int b = warp;
-      float v[kMaxExperts / 32];
-#pragma unroll
-      for (int j = 0; j < kMaxExperts / 32; ++j) v[j] = tmp[b * kTileRows + lane + 32 * j];
-      float ssum = 0.f;
-      for (int k = 0; k < p.topk; ++k) {
-        float bv = v[0];
-        int bi = lane;
-#pragma unroll
-        for (int j = 1; j < kMaxExperts / 32; ++j)
-          if (v[j] > bv) { bv = v[j]; bi = lane + 32 * j; }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) v[bi >> 5] = -INFINITY;
-        const float sc = 1.0f / (1.0f + expf(-bv));
-        ssum += sc;
-        if (lane == 0) {
-          sel[b * 16 + k] = bi;
-          sg[b * 16 + k] = sc;
-          mark[bi] = 1;
-        }
+    // top-k by rank: thread (b, e) counts the experts ahead of e (a larger logit, or an equal
+    // one at a lower index; a NaN logit counts as -inf, so the order is total and the ranks of a
+    // token are a permutation). Ranks 0..top_k-1 are the selection, in descending order.
+#pragma unroll 1
+    for (int idx = tid; idx < p.B * p.E; idx += kConsumerWarps * 32) {
+      const int b = idx / p.E, e = idx - b * p.E;
+      const float* row = tmp + b * kTileRows;
+      float v = row[e];
+      if (v != v) v = -INFINITY;
+      int rank = 0;
+#pragma unroll 4
+      for (int j = 0; j < p.E; ++j) {
+        float w = row[j];
+        if (w != w) w = -INFINITY;
+        rank += (w > v || (w == v && j < e)) ? 1 : 0;
       }
+      if (rank < p.topk) {
+        sel[b * 16 + rank] = e;
+        sg[b * 16 + rank] = 1.0f / (1.0f + expf(-v));
+        mark[e] = 1;
+      }
+    }
+    cons_sync();
+    if (warp < p.B) {
+      // gates: the selected scores over their sum (taken in rank order)
+      const int b = warp;
+      float ssum = 0.f;
+#pragma unroll 1
+      for (int k = 0; k < p.topk; ++k) ssum += sg[b * 16 + k];
       __syncwarp();
       if (lane < p.topk) {
         const float gt = sg[b * 16 + lane] / ssum;
@@ -1128,63 +1146,37 @@ struct Consumer {
     float* tmp = red;  // [BM][128]
     switch (kind) {
       case K_D: {
-        const int nv = g.T / g.tpe;
-        // every expert's contributor slots for this row block, as offsets into the partials:
-        // warp 0 lane v counts expert v's contributors, a prefix sum places them
-        int* list = reinterpret_cast<int*>(tmp + BM * kTileRows);
-        int* nlist = list + kListCap;
-        if (warp == 0) {
-          int base = 0;
-          for (int v0 = 0; v0 < nv; v0 += 32) {
-            const int v = v0 + lane;
-            const int seg = v * p.n_rb_d + grp;
-            const int nc = v < nv ? n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x) : 0;
-            int incl = nc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const int y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += y;
-            }
-            const int first = base + incl - nc;
-            for (int c = 0; c < nc; ++c)
-              if (first + c < kListCap) list[first + c] = (seg * g.kbs + c) * p.MB * kTileRows;
-            base += __shfl_sync(0xffffffffu, incl, 31);
-          }
-          if (lane == 0) {
-            if (base > kListCap) raise_err(p, kDevBadArg, 3);
-            *nlist = min(base, kListCap);
-          }
-        }
-        cons_sync();
-        const int nl = *nlist;
+        // the row block's contributor slots are consecutive (its tiles are one contiguous run)
+        const int nl = n_contrib(grp * g.kbs, g.kbs, g.T, gridDim.x);
         const StageGeo go = stage_geo(p, K_O, 0);
         const int nco = n_contrib(grp * go.kbs, go.kbs, go.T, gridDim.x);
-        const size_t ost = (size_t)p.MB * kTileRows;
+        const size_t st = (size_t)p.MB * kTileRows;
         for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
           int b = idx / kTileRows, i = idx % kTileRows;
           int r = grp * kTileRows + i;
-          const float* src = p.part_d + (size_t)b * kTileRows + i;
-          const float* osrc = p.part_o + (size_t)grp * go.kbs * ost + (size_t)b * kTileRows + i;
+          const float* src = p.part_d + (size_t)grp * g.kbs * st + (size_t)b * kTileRows + i;
+          const float* osrc = p.part_o + (size_t)grp * go.kbs * st + (size_t)b * kTileRows + i;
           // the residual input, the output projection's partials (x_mid, as the norm stage
-          // formed it) and the first sixteen down-projection partials, all in flight together
+          // formed it) and the first eight down-projection partials, all in flight together
           const uint16_t xin = ldcg_u16(x_in(l, b) + r);
-          float ov[8], v[16];
+          float ov[8], v[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) ov[j] = (j < nco) ? ldcg(osrc + (size_t)j * ost) : 0.f;
+          for (int j = 0; j < 8; ++j) {
+            ov[j] = (j < nco) ? ldcg(osrc + (size_t)j * st) : 0.f;
+            v[j] = (j < nl) ? ldcg(src + (size_t)j * st) : 0.f;
+          }
+          float y = 0.f, os = 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = (j < nl) ? ldcg(src + list[j]) : 0.f;
-          float y = 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) y += v[j];
+          for (int j = 0; j < 8; ++j) {
+            y += v[j];
+            os += ov[j];
+          }
           // more contributors than one batch (not at the sizes this kernel is tuned for): one
           // load at a time, in the same order
 #pragma unroll 1
-          for (int e = 16; e < nl; ++e) y += ldcg(src + list[e]);
-          float os = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) os += ov[j];
+          for (int e = 8; e < nl; ++e) y += ldcg(src + (size_t)e * st);
 #pragma unroll 1
-          for (int c = 8; c < nco; ++c) os += ldcg(osrc + (size_t)c * ost);
+          for (int c = 8; c < nco; ++c) os += ldcg(osrc + (size_t)c * st);
           const float xm = bf16f(f2bf(bf16f(xin) + os));
           uint16_t o = f2bf(xm + y);
           p.xbuf[((size_t)((l + 1) & 1) * p.MB + b) * p.d + r] = o;
@@ -1432,11 +1424,12 @@ struct Consumer {
     }, 16);
   }
 
-  // thread 0: wait for the final SwiGLU rows of the experts the CTA's down-projection tiles read
-  __device__ void wait_h(int l, int v_lo, int v_hi, int U) {
-    const int nv = v_hi >= v_lo ? v_hi - v_lo + 1 : 0;
-    cta_wait_all(nv * p.n_rb_gu, [&](int i) {
-      const int v = v_lo + i / p.n_rb_gu, rb = i % p.n_rb_gu;
+  // wait for the final SwiGLU rows of the n experts whose down-projection k blocks the CTA's
+  // tiles read: expert slots v0, v0 + 1, ... (wrapping after nv; slot U is the shared expert)
+  __device__ void wait_h(int l, int v0, int n, int nv, int U) {
+    cta_wait_all(n * p.n_rb_gu, [&](int i) {
+      const int j = i / p.n_rb_gu, rb = i - j * p.n_rb_gu;
+      const int v = (v0 + j) % nv;
       const int slot = v < U ? v : p.umax;
       return WaitCond{p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch};
     }, 17);
@@ -1693,10 +1686,10 @@ struct Consumer {
       for (int ph = 0; ph < 7; ++ph) {
         int kind = -1;
         // a norm stage or an activation copy runs right before the GEMV stage it feeds (one call
-        // site each, see below): the attention output, or the SwiGLU rows of experts cp_lo..cp_hi
+        // site each, see below): the attention output, or the SwiGLU rows of cp_n experts
         const uint16_t* norm_w = nullptr;
         bool norm_from_o = false;
-        int cp_lo = 0, cp_hi = -1;
+        int cp_v0 = 0, cp_n = 0, cp_nv = 1;  // experts cp_v0, cp_v0 + 1, ... (mod cp_nv)
         bool cp_obuf = false;
         if (lm) {
           if (ph == 0) {
@@ -1719,7 +1712,7 @@ struct Consumer {
               wait_o_groups(l);
               cta_stamp(l, S_OGRP_READY);
               cp_obuf = true;
-              cp_hi = 0;
+              cp_n = 1;
               kind = K_O;
               break;
             case 2:
@@ -1746,20 +1739,27 @@ struct Consumer {
             case 5: {
               cta_stamp(l, S_GU_DONE);
               // down projections of all active experts, gate-weighted, + residual
+              // (the CTA's tiles run through k-block runs s0 .. s1 of kb_i tiles, run s of
+              // expert slot s % nv: it stages the SwiGLU rows of the first min(runs, nv) of them)
               const StageGeo g = stage_geo(p, K_D, U);
               const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
-              int v_lo = 0, v_hi = -1;
+              const int nv = U + p.nsh;
+              int s0 = 0, nst = 0;
               if (t1 > t0) {
-                v_lo = t0 / g.tpe;
-                v_hi = (t1 - 1) / g.tpe;
+                s0 = t0 / g.tpe;
+                nst = min((t1 - 1) / g.tpe - s0 + 1, nv);
               }
-              if ((v_hi - v_lo + 1) * p.inter > p.xmax) raise_err(p, kDevBadArg, 6);
-              wait_h(l, v_lo, v_hi, U);
+              if (nst * p.inter > p.xmax) {
+                raise_err(p, kDevBadArg, 6);
+                nst = 0;
+              }
+              const int v0 = nv > 0 ? s0 % nv : 0;
+              wait_h(l, v0, nst, nv, U);
               cta_stamp(l, S_H_READY);
-              if (tid == 0) m->v_lo = v_lo;
               for (int i = tid; i < BM; i += 256) m->gate[i][U] = 1.f;  // shared / dense expert
-              cp_lo = v_lo;
-              cp_hi = (v_hi - v_lo + 1) * p.inter <= p.xmax ? v_hi : v_lo - 1;
+              cp_v0 = v0;
+              cp_n = nst;
+              cp_nv = nv;
               kind = K_D;
               break;
             }
@@ -1779,11 +1779,14 @@ struct Consumer {
           stage_rmsnorm(lm ? p.L : l, nullptr, norm_w, norm_from_o);
           if (norm_from_o) cta_stamp(l, S_XMID_READY);
         }
-        if (cp_hi >= cp_lo) {
-          for (int v = cp_lo; v <= cp_hi; ++v) {
+        if (cp_n > 0) {
+          int v = cp_v0;
+#pragma unroll 1
+          for (int j = 0; j < cp_n; ++j) {
             const uint16_t* src = cp_obuf ? p.obuf : (v < U ? p.hrt + (size_t)v * p.MB * p.inter : p.hsh);
             const int n = cp_obuf ? p.hq * HD : p.inter;
-            stage_copy(src, n, (size_t)n, (v - cp_lo) * n);
+            stage_copy(src, n, (size_t)n, j * n);
+            if (++v == cp_nv) v = 0;
           }
           cons_sync();
         }
