@@ -44,6 +44,10 @@ constexpr int kMaxExperts = 128;
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
 constexpr int kWaitMax = 128;  // conditions one CTA-wide wait may span
+// The consumer thread that publishes a CTA's results (releasing arrivals and flags, preceded by
+// a CTA barrier) and resets the counters it finalised: a thread of the last warp, so that warp 0,
+// which polls in every CTA-wide wait, does not stall on the release.
+constexpr int kPubThread = (kConsumerWarps - 1) * 32;
 
 struct Misc {
   const unsigned* wt_addr[kWaitMax];  // CTA-wide wait: *wt_addr[i] >= wt_want[i] for all i
@@ -556,7 +560,7 @@ struct Consumer {
         if (k < p.d) v[j] = ldcg4(src + k);
       }
       if (from_o) {
-        // the output projection's partials of this thread's chunks: two chunks at a time, four
+        // the output projection's partials of this thread's chunks: two chunks at a time, six
         // contributors per batch, every load of a batch in flight before any is added (one L2
         // round trip per batch); each row is summed in contributor order
         const size_t st = (size_t)p.MB * kTileRows;
@@ -576,12 +580,12 @@ struct Consumer {
             for (int e = 0; e < 8; ++e) o8[jj][e] = 0.f;
           }
           const int ncm = max(nc[0], nc[1]);
-          for (int c0 = 0; c0 < ncm; c0 += 4) {
-            float4 t[2][4][2];
+          for (int c0 = 0; c0 < ncm; c0 += 6) {
+            float4 t[2][6][2];
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
+              for (int c = 0; c < 6; ++c) {
                 if (c0 + c < nc[jj]) {
                   t[jj][c][0] = __ldcg(reinterpret_cast<const float4*>(base[jj] + (size_t)(c0 + c) * st));
                   t[jj][c][1] = __ldcg(reinterpret_cast<const float4*>(base[jj] + (size_t)(c0 + c) * st + 4));
@@ -592,7 +596,7 @@ struct Consumer {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
+              for (int c = 0; c < 6; ++c) {
                 o8[jj][0] += t[jj][c][0].x; o8[jj][1] += t[jj][c][0].y; o8[jj][2] += t[jj][c][0].z; o8[jj][3] += t[jj][c][0].w;
                 o8[jj][4] += t[jj][c][1].x; o8[jj][5] += t[jj][c][1].y; o8[jj][6] += t[jj][c][1].z; o8[jj][7] += t[jj][c][1].w;
               }
@@ -797,18 +801,18 @@ struct Consumer {
       const int b = idx / kTileRows, row = idx % kTileRows;
       dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
     }
-    // The CTA barrier orders every thread's partial before thread 0's releasing arrival; no
-    // thread waits for the arrival to complete. An arrival adds the number of the segment's
-    // tiles the CTA summed, so a group is complete when its counter has grown by its tile count
-    // (kbs per segment), however the tiles were split among the CTAs.
+    // The CTA barrier orders every thread's partial before the publishing thread's releasing
+    // arrival; no other thread waits for the arrival to complete. An arrival adds the number of
+    // the segment's tiles the CTA summed, so a group is complete when its counter has grown by
+    // its tile count (kbs per segment), however the tiles were split among the CTAs.
     cons_sync();
     if (dead) return;
     if (kind == K_QKV || kind == K_O || kind == K_ROUTER) {
       // published partials: the readers wait for all of the row block's tiles
-      if (tid == 0) red_release_add(pub_counter(kind, l) + seg, ntiles);
+      if (tid == kPubThread) red_release_add(pub_counter(kind, l) + seg, ntiles);
       return;
     }
-    if (tid == 0) red_release_add(cnt_base(kind) + seg, ntiles);
+    if (tid == kPubThread) red_release_add(cnt_base(kind) + seg, ntiles);
   }
 
   // counter value that completes an output group: its segment's tiles
@@ -967,7 +971,7 @@ struct Consumer {
         const int want = group_expected(kind, g, grp);
         cta_wait_all(1, [&](int) { return count_reached(c, want); }, 21);
         if (dead) break;
-        if (tid == 0) *const_cast<volatile int*>(c) = 0;
+        if (tid == kPubThread) *const_cast<volatile int*>(c) = 0;
         finalize(kind, l, g, grp, U);
         cons_sync();
       }
@@ -1108,7 +1112,7 @@ struct Consumer {
                     : count_reached(p.cnt_shgu + (v - nr), group_expected(K_SHGU, gs, v - nr));
     }, 21);
     if (dead) return;
-    if (tid == 0) {
+    if (tid == kPubThread) {
 #pragma unroll 1
       for (int v = vlo; v < vhi; ++v) *const_cast<volatile int*>(v < nr ? p.cnt_rtgu + v : p.cnt_shgu + (v - nr)) = 0;
     }
@@ -1129,8 +1133,7 @@ struct Consumer {
         p.hrt[((size_t)(grp / p.n_rb_gu) * p.MB + b) * p.inter + j] = h;
     }
     cons_sync();
-    if (tid == 0) {
-      __threadfence();
+    if (tid == kPubThread) {
       // flag of group v: h_flag[l][slot][rb], slot = v / n_rb_gu (the shared experts' slot umax
       // after the routed ones), walked without divisions
       unsigned* f = p.h_flag + (size_t)l * (p.umax + 1) * p.n_rb_gu;
@@ -1184,10 +1187,7 @@ struct Consumer {
         }
         // the next layer's input row block is final
         cons_sync();
-        if (tid == 0) {
-          __threadfence();
-          st_release(p.x_flag + (size_t)l * p.n_rb_d + grp, p.epoch);
-        }
+        if (tid == kPubThread) st_release(p.x_flag + (size_t)l * p.n_rb_d + grp, p.epoch);
         break;
       }
       default: {  // LM head
@@ -1225,7 +1225,7 @@ struct Consumer {
                                       (unsigned long long)(0xFFFFFFFFu - (unsigned)(grp * kTileRows + bi)));
         }
         cons_sync();
-        if (tid == 0) {
+        if (tid == kPubThread) {
           __threadfence();
           int old = atom_add_acqrel(p.cnt_lm_done, 1);
           if (old + 1 == p.n_rb_lm) {
@@ -1396,7 +1396,7 @@ struct Consumer {
     cons_sync();
   }
 
-  // thread 0: wait for the merged attention output of every (sequence, KV head) whose heads the
+  // wait for the merged attention output of every (sequence, KV head) whose heads the
   // CTA's output-projection tiles read
   __device__ void wait_o_groups(int l) {
     const StageGeo go = stage_geo(p, K_O, 0);
@@ -1591,11 +1591,11 @@ struct Consumer {
           dst[(size_t)h * (HD + 2) + HD + 1] = Lsum;
         }
       }
-      // publish: the CTA barrier orders every thread's partial before thread 0's releasing
-      // arrival (the layer's counters start the launch at zero, see stage_rmsnorm)
+      // publish: the CTA barrier orders every thread's partial before the publishing thread's
+      // releasing arrival (the layer's counters start the launch at zero, see stage_rmsnorm)
       cons_sync();
       const size_t gi = ((size_t)l * p.MB + a.b) * p.hkv + a.g;
-      if (tid == 0 && !dead) red_release_add(p.attn_cnt + gi, 1);
+      if (tid == kPubThread && !dead) red_release_add(p.attn_cnt + gi, 1);
       // Chunk merge, shared by the group's nch units (with nch > 1 the host makes every unit a
       // CTA of its own, so a CTA waits only for others' chunks): unit c merges the outputs
       // [o_lo, o_hi) = [c * G*HD / nch, (c+1) * G*HD / nch) of the group's G*HD (head o / HD, dim
@@ -1659,10 +1659,7 @@ struct Consumer {
           p.obuf[(size_t)a.b * p.hq * HD + (size_t)a.g * G * HD + o] = f2bf(A);
         }
         cons_sync();
-        if (tid == 0) {
-          __threadfence();
-          red_release_add(p.o_cnt + gi, 1);
-        }
+        if (tid == kPubThread) red_release_add(p.o_cnt + gi, 1);
       }
       cons_sync();
     }
