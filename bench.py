@@ -37,6 +37,10 @@ WORKLOADS = {
     "moe8_1k1k": ("MOE8", 1024, 1024, 1),
     "moe8_8k1k": ("MOE8", 8192, 1024, 1),
     "moe_layer_8k": ("MOE_LAYER", 8192, 256, 1),
+    # batch sweep of the 8-layer stack (each sequence its own seeded 1024-token history)
+    "moe8_1k_b2": ("MOE8", 1024, 256, 2),
+    "moe8_1k_b4": ("MOE8", 1024, 256, 4),
+    "moe8_1k_b8": ("MOE8", 1024, 256, 8),
     # small captures for ncu: two layers of the same stack + LM head
     "moe2_1k_prof": ("MOE2", 1024, 8, 1),
 }

@@ -90,9 +90,9 @@ struct KParams {
   // router partials: growing counter per layer [L]. Finalised outputs (SwiGLU h, down projection +
   // residual, logits): arrival counters that the group's designated finaliser waits on and resets
   int *cnt_router, *cnt_shgu, *cnt_rtgu, *cnt_d, *cnt_lm, *cnt_lm_done;
-  int* o_cnt;  // [L][MB][hkv] chunk slices of the merged attention output written (zero between launches)
+  int* o_cnt;  // [L][hkv] merged attention slices written, all sequences (zero between launches)
   unsigned* x_flag;  // [L][n_rb_d] = epoch once a row block of the layer's output is final
-  unsigned* h_flag;  // [L][umax + 1][n_rb_gu] = epoch once an expert's 64 SwiGLU rows are final
+  int* h_cnt;  // [L][umax + 1] grows by n_rb_gu per step: an expert slot's SwiGLU row blocks final
                      // (slot umax: the shared / dense expert)
   // attention split-KV partials: [MB][hkv][nch][group][hd + 2], counters [MB][hkv]
   float* attn_part;

@@ -564,15 +564,15 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.part_lm, fb * std::max(1, p.n_rb_lm) * p.kb_d);
     Z(p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv);
     Z(p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d);
-    Z(p.o_cnt, sizeof(int) * (size_t)c.n_layers * MB * c.n_kv_heads);
+    Z(p.o_cnt, sizeof(int) * (size_t)c.n_layers * c.n_kv_heads);
     Z(p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d);
-    Z(p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu);
+    Z(p.h_cnt, sizeof(int) * (size_t)c.n_layers * (p.umax + 1));
     Z(p.cnt_router, sizeof(int) * c.n_layers);
     e->epoch_bufs = {{p.cnt_qkv, sizeof(int) * (size_t)c.n_layers * p.n_rb_qkv},
                      {p.cnt_o, sizeof(int) * (size_t)c.n_layers * p.n_rb_d},
                      {p.cnt_router, sizeof(int) * c.n_layers},
                      {p.x_flag, sizeof(unsigned) * (size_t)c.n_layers * p.n_rb_d},
-                     {p.h_flag, sizeof(unsigned) * (size_t)c.n_layers * (p.umax + 1) * p.n_rb_gu}};
+                     {p.h_cnt, sizeof(int) * (size_t)c.n_layers * (p.umax + 1)}};
     Z(p.cnt_shgu, sizeof(int) * p.n_rb_gu);
     Z(p.cnt_rtgu, sizeof(int) * std::max(1, p.umax) * p.n_rb_gu);
     Z(p.cnt_d, sizeof(int) * p.n_rb_d);
@@ -581,8 +581,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     e->nch_max = std::max(1, G / c.n_kv_heads);
     Z(p.attn_part, sizeof(float) * MB * c.n_kv_heads * e->nch_max * e->group * (c.head_dim + 2));
     Z(p.attn_cnt, sizeof(int) * (size_t)c.n_layers * MB * c.n_kv_heads);
-    // per step a growing counter gains at most max(kb_d, kb_o)
-    e->epoch_limit = (1u << 30) / (unsigned)std::max({p.kb_d, p.kb_o, 1});
+    // per step a growing counter gains at most max(kb_d, kb_o, n_rb_gu)
+    e->epoch_limit = (1u << 30) / (unsigned)std::max({p.kb_d, p.kb_o, p.n_rb_gu, 1});
     if (const char* el = getenv("DEC_EPOCH_LIMIT")) {  // a smaller limit, for testing the restart
       const long v = atol(el);
       if (v >= 1 && (unsigned long)v < e->epoch_limit) e->epoch_limit = (unsigned)v;
@@ -598,16 +598,18 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   }
 
   // ---- activation buffer width: d, n_heads*head_dim, or the experts a CTA's down range spans
-  // (down tiles are row-block major: run s of kb_i tiles belongs to expert slot s % nv)
+  // (down tiles come in runs of one expert slot: kb_i tiles row-block major for at most
+  // kDRowMajorMax slots, run s belonging to slot s % nv; otherwise n_rb_d * kb_i tiles, one per slot)
   {
     int xmax = std::max(c.hidden, c.n_heads * c.head_dim);
     int span = 1;
     for (int U = 0; U <= p.umax; ++U) {
       const int nv = U + p.nsh;
       const int T = p.n_rb_d * nv * p.kb_i;
+      const int run = nv <= kDRowMajorMax ? p.kb_i : p.n_rb_d * p.kb_i;
       for (int cta = 0; cta < G; ++cta) {
         int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
-        if (t1 > t0) span = std::max(span, std::min((t1 - 1) / p.kb_i - t0 / p.kb_i + 1, nv));
+        if (t1 > t0) span = std::max(span, std::min((t1 - 1) / run - t0 / run + 1, nv));
       }
     }
     xmax = std::max(xmax, span * p.inter);

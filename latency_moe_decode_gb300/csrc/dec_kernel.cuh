@@ -43,7 +43,9 @@ struct SmemLayout {
 constexpr int kMaxExperts = 128;
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
-constexpr int kWaitMax = 128;  // conditions one CTA-wide wait may span
+constexpr int kWaitMax = 128;  // conditions one CTA-wide wait table holds
+constexpr int kDRowMajorMax = 12;  // down projections of at most this many expert slots: row-block major
+constexpr int kListCap = 1024;     // contributor slots one down-projection row block may gather
 // The consumer thread that publishes a CTA's results (releasing arrivals and flags, preceded by
 // a CTA barrier) and resets the counters it finalised: a thread of the last warp, so that warp 0,
 // which polls in every CTA-wide wait, does not stall on the release.
@@ -79,7 +81,7 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   s.red_off = align_up(s.xs_off + bm * xmax * 2, 128);
   int red_gemv = 2 * kTileRows * bm * 4;
   int red_attn = kConsumerWarps * group * (hd + 2) * 4;
-  int red_fin = (bm * kTileRows + 16) * 4;
+  int red_fin = (bm * kTileRows + kListCap + 16) * 4;
   int red = red_gemv > red_attn ? red_gemv : red_attn;
   red = red > red_fin ? red : red_fin;
   s.misc_off = align_up(s.red_off + red, 128);
@@ -131,22 +133,33 @@ __device__ __forceinline__ int contrib_slot(int c, int f, int a, int T, int G) {
 struct StageGeo {
   int T;    // tiles
   int kbs;  // tiles per segment (the k blocks one output row block sums)
-  int tpe;  // routed gate/up: tiles per expert; down: tiles per expert within a segment (kb_i)
+  int tpe;  // expert stages: tiles of one expert in a row (one run)
+  int rbm;  // down projections: row-block major (else expert major)
 };
 
 __device__ __forceinline__ StageGeo stage_geo(const KParams& p, int kind, int U) {
   StageGeo g;
   g.tpe = 0;
+  g.rbm = 0;
   switch (kind) {
     case K_QKV: g.kbs = p.kb_d; g.T = p.n_rb_qkv * p.kb_d; break;
     case K_O: g.kbs = p.kb_o; g.T = p.n_rb_d * p.kb_o; break;
     case K_ROUTER: g.kbs = p.kb_d; g.T = p.n_rb_router * p.kb_d; break;
     case K_SHGU: g.kbs = p.kb_d; g.T = p.n_rb_gu * p.kb_d; break;
     case K_RTGU: g.kbs = p.kb_d; g.tpe = p.n_rb_gu * p.kb_d; g.T = U * g.tpe; break;
-    // down projections, row-block major: segment rb holds the k blocks of every active expert
-    // (routed slots 0..U-1, then the shared one), kb_i each, so one output row block's tiles are
-    // contiguous and are split among few CTAs
-    case K_D: g.tpe = p.kb_i; g.kbs = (U + p.nsh) * p.kb_i; g.T = p.n_rb_d * g.kbs; break;
+    // Down projections of the nv = U + nsh active expert slots (routed, then the shared one).
+    // Few slots: row-block major, segment rb = the kb_i k blocks of row block rb of every slot in
+    // turn, so one output row block's tiles are contiguous and split among few CTAs. Many slots
+    // (large batches): expert major, one expert's row blocks after another (segments of kb_i),
+    // so a CTA's range spans few experts (whose SwiGLU rows it stages).
+    case K_D: {
+      const int nv = U + p.nsh;
+      g.rbm = nv <= kDRowMajorMax;
+      g.tpe = g.rbm ? p.kb_i : p.n_rb_d * p.kb_i;
+      g.kbs = g.rbm ? nv * p.kb_i : p.kb_i;
+      g.T = p.n_rb_d * nv * p.kb_i;
+      break;
+    }
     default: g.kbs = p.kb_d; g.T = p.n_rb_lm * p.kb_d; break;
   }
   return g;
@@ -166,7 +179,7 @@ struct TileCursor {
   }
   __device__ void init(const KParams& p, const LayerDev& Ld, int kind, int t, const StageGeo& g, int U,
                        const int* elist) {
-    if (kind == K_RTGU) {
+    if (kind == K_RTGU || (kind == K_D && !g.rbm)) {
       u = t / g.tpe;
       r = t - u * g.tpe;
       addr = expert_base(p, Ld, kind, u, U, elist) + (size_t)r * kTileBytes;
@@ -193,12 +206,12 @@ struct TileCursor {
   __device__ __forceinline__ void next(const KParams& p, const LayerDev& Ld, int kind, const StageGeo& g, int U,
                                        const int* elist) {
     addr += kTileBytes;
-    if (kind == K_RTGU && ++r == g.tpe) {
+    if ((kind == K_RTGU || (kind == K_D && !g.rbm)) && ++r == g.tpe) {
       r = 0;
       ++u;
       if (u * g.tpe < g.T) addr = expert_base(p, Ld, kind, u, U, elist);
     }
-    if (kind == K_D && ++r == g.tpe) {
+    if (kind == K_D && g.rbm && ++r == g.tpe) {
       r = 0;
       if (++u * g.tpe == g.kbs) {
         u = 0;
@@ -537,11 +550,10 @@ struct Consumer {
       // reads (together: all of layer l_src's), each merge having waited for all of its chunks.
       // So no CTA reads or adds to the layer's attention counters again in this launch: they
       // are zeroed here for the next one.
-      if (tid == 0 && !dead)
-        for (int i = blockIdx.x; i < p.B * p.hkv; i += gridDim.x) {
-          p.attn_cnt[(size_t)l_src * p.MB * p.hkv + i] = 0;
-          p.o_cnt[(size_t)l_src * p.MB * p.hkv + i] = 0;
-        }
+      if (tid == 0 && !dead) {
+        for (int i = blockIdx.x; i < p.B * p.hkv; i += gridDim.x) p.attn_cnt[(size_t)l_src * p.MB * p.hkv + i] = 0;
+        for (int g = blockIdx.x; g < p.hkv; g += gridDim.x) p.o_cnt[(size_t)l_src * p.hkv + g] = 0;
+      }
     }
     // the norm weights of this thread's chunks, loaded once, in flight with the first activations
     uint4 wv[MAXV];
@@ -785,7 +797,7 @@ struct Consumer {
   // output groups of a finalised stage (SwiGLU row blocks of each expert, output row blocks,
   // vocabulary row blocks)
   __device__ __forceinline__ int n_groups(int kind, const StageGeo& g) const {
-    return g.T / g.kbs;
+    return kind == K_D ? p.n_rb_d : g.T / g.kbs;  // down projections: the output row blocks
   }
 
   __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, int ntiles, float (&acc)[BM]) {
@@ -812,11 +824,15 @@ struct Consumer {
       if (tid == kPubThread) red_release_add(pub_counter(kind, l) + seg, ntiles);
       return;
     }
-    if (tid == kPubThread) red_release_add(cnt_base(kind) + seg, ntiles);
+    // (expert-major down projections: segment v * n_rb_d + rb adds to output row block rb)
+    if (tid == kPubThread) red_release_add(cnt_base(kind) + (kind == K_D && !g.rbm ? seg % p.n_rb_d : seg), ntiles);
   }
 
   // counter value that completes an output group: its segment's tiles
-  __device__ int group_expected(int kind, const StageGeo& g, int grp) const { return g.kbs; }
+  // (down projections: every expert slot's k blocks of the row block, in either tile order)
+  __device__ int group_expected(int kind, const StageGeo& g, int grp) const {
+    return kind == K_D ? g.T / p.n_rb_d : g.kbs;
+  }
 
   // sum of the published partials of segment seg for (b, row)
   __device__ __forceinline__ float seg_sum(int kind, const StageGeo& g, int seg, int b, int row) const {
@@ -898,13 +914,14 @@ struct Consumer {
     // run and the expert's place xj among the SwiGLU rows staged in xs (the CTA's runs in order,
     // the first at 0, wrapping after nv)
     int seg = t1 > t0 ? t0 / g.kbs : 0, kb = t0 - seg * g.kbs;
-    int v = 0, kx = kb, xj = 0, xbase = 0;
+    int v = 0, kx = kb, rv = 0, xj = 0, xbase = 0;
     const int nv = kind == K_D ? U + p.nsh : 1;
 #pragma unroll
     for (int b = 0; b < BM; ++b) gmul[b] = 1.f;
     if (kind == K_D && t1 > t0) {
-      v = kb / g.tpe;
-      kx = kb - v * g.tpe;
+      v = g.rbm ? kb / g.tpe : t0 / g.tpe;       // expert slot of the first tile
+      rv = g.rbm ? kb - v * g.tpe : t0 - v * g.tpe;  // its place in that expert's run
+      kx = rv % p.kb_i;                          // and in its k-block sweep
 #pragma unroll
       for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
     }
@@ -939,13 +956,16 @@ struct Consumer {
       }
       if (kind != K_D) {
         kx = kb;
-      } else if (++kx == g.tpe) {
-        kx = 0;
-        if (++v == nv) v = 0;
-        if (++xj == nv) xj = 0;
-        xbase = xj * p.inter;
+      } else {
+        if (++kx == p.kb_i) kx = 0;
+        if (++rv == g.tpe) {
+          rv = 0;
+          if (++v == nv) v = 0;
+          if (++xj == nv) xj = 0;
+          xbase = xj * p.inter;
 #pragma unroll
-        for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
+          for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
+        }
       }
     }
     // Finalise the output groups this CTA is designated for (groups spread evenly over the
@@ -1093,6 +1113,12 @@ struct Consumer {
     }
     cons_sync();
     if (tid == 0) mbar_arrive(&m->rt_bar);  // the producer may now issue the routed experts
+    // The SwiGLU counters h_cnt[l][slot] grow by n_rb_gu per step for every slot (so a wait's
+    // target is epoch * n_rb_gu whatever the slot did in earlier steps): the slots this step's
+    // routing leaves unused get their n_rb_gu here, spread over the CTAs.
+    if (tid == kPubThread)
+      for (int u = m->U + blockIdx.x; u < p.umax; u += gridDim.x)
+        red_relaxed_add(p.h_cnt + (size_t)l * (p.umax + 1) + u, p.n_rb_gu);
   }
 
   // -------- finalisers (run by the CTA designated for an output group) --------
@@ -1134,12 +1160,11 @@ struct Consumer {
     }
     cons_sync();
     if (tid == kPubThread) {
-      // flag of group v: h_flag[l][slot][rb], slot = v / n_rb_gu (the shared experts' slot umax
-      // after the routed ones), walked without divisions
-      unsigned* f = p.h_flag + (size_t)l * (p.umax + 1) * p.n_rb_gu;
+      // one arrival per group on its expert slot's counter h_cnt[l][slot] (slot v / n_rb_gu, the
+      // shared experts' umax), which grows by n_rb_gu per step
+      int* c = p.h_cnt + (size_t)l * (p.umax + 1);
 #pragma unroll 1
-      for (int v = vlo; v < vhi; ++v)
-        st_release(f + (v < nr ? v : p.umax * p.n_rb_gu + (v - nr)), p.epoch);
+      for (int v = vlo; v < vhi; ++v) red_release_add(c + (v < nr ? v / p.n_rb_gu : p.umax), 1);
     }
   }
 
@@ -1149,35 +1174,67 @@ struct Consumer {
     float* tmp = red;  // [BM][128]
     switch (kind) {
       case K_D: {
-        // the row block's contributor slots are consecutive (its tiles are one contiguous run)
-        const int nl = n_contrib(grp * g.kbs, g.kbs, g.T, gridDim.x);
+        // the row block's contributor slots (partial rows of part_d): one run of consecutive
+        // slots (row-block major), or one run per expert slot (expert major), listed by warp 0
+        // (lane v counts run v's contributors, a prefix sum places them)
+        int* list = reinterpret_cast<int*>(tmp + BM * kTileRows);
+        int* nlist = list + kListCap;
+        const int rb0 = grp * g.kbs;  // row-block major: the slots rb0 .. rb0 + nl - 1
+        if (!g.rbm && warp == 0) {
+          const int nseg = g.T / g.tpe;
+          int base = 0;
+#pragma unroll 1
+          for (int v0 = 0; v0 < nseg; v0 += 32) {
+            const int v = v0 + lane;
+            const int seg = v * p.n_rb_d + grp;
+            const int nc = v < nseg ? n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x) : 0;
+            int incl = nc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const int first = base + incl - nc;
+#pragma unroll 1
+            for (int c = 0; c < nc; ++c)
+              if (first + c < kListCap) list[first + c] = seg * g.kbs + c;
+            base += __shfl_sync(0xffffffffu, incl, 31);
+          }
+          if (lane == 0) {
+            if (base > kListCap) raise_err(p, kDevBadArg, 3);
+            *nlist = min(base, kListCap);
+          }
+        }
+        if (!g.rbm) cons_sync();
+        const int nl = g.rbm ? n_contrib(rb0, g.kbs, g.T, gridDim.x) : *nlist;
         const StageGeo go = stage_geo(p, K_O, 0);
         const int nco = n_contrib(grp * go.kbs, go.kbs, go.T, gridDim.x);
         const size_t st = (size_t)p.MB * kTileRows;
+#pragma unroll 1
         for (int idx = tid; idx < p.B * kTileRows; idx += 256) {
           int b = idx / kTileRows, i = idx % kTileRows;
           int r = grp * kTileRows + i;
-          const float* src = p.part_d + (size_t)grp * g.kbs * st + (size_t)b * kTileRows + i;
+          const float* src = p.part_d + (size_t)b * kTileRows + i;
           const float* osrc = p.part_o + (size_t)grp * go.kbs * st + (size_t)b * kTileRows + i;
           // the residual input, the output projection's partials (x_mid, as the norm stage
           // formed it) and the first eight down-projection partials, all in flight together
           const uint16_t xin = ldcg_u16(x_in(l, b) + r);
-          float ov[8], v[8];
+          float ov[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            ov[j] = (j < nco) ? ldcg(osrc + (size_t)j * st) : 0.f;
-            v[j] = (j < nl) ? ldcg(src + (size_t)j * st) : 0.f;
-          }
-          float y = 0.f, os = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            y += v[j];
-            os += ov[j];
-          }
-          // more contributors than one batch (not at the sizes this kernel is tuned for): one
-          // load at a time, in the same order
+          for (int j = 0; j < 8; ++j) ov[j] = (j < nco) ? ldcg(osrc + (size_t)j * st) : 0.f;
+          float y = 0.f;
 #pragma unroll 1
-          for (int e = 8; e < nl; ++e) y += ldcg(src + (size_t)e * st);
+          for (int e0 = 0; e0 < nl; e0 += 8) {  // eight contributors per batch, in list order
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[j] = (e0 + j < nl) ? ldcg(src + (size_t)(g.rbm ? rb0 + e0 + j : list[e0 + j]) * st) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y += v[j];
+          }
+          float os = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) os += ov[j];
 #pragma unroll 1
           for (int c = 8; c < nco; ++c) os += ldcg(osrc + (size_t)c * st);
           const float xm = bf16f(f2bf(bf16f(xin) + os));
@@ -1292,7 +1349,7 @@ struct Consumer {
   __device__ void cta_wait_all(int n, F cond, int where) {
     if (warp == 0) {
       int ok = dead ? 0 : 1;
-      if (n > kWaitMax) {
+      if (n > kWaitMax) {  // (no wait of the step spans more: at most max(64 KV heads, 32 row blocks))
         if (lane == 0) raise_err(p, kDevBadArg, 7);
         ok = 0;
       }
@@ -1416,22 +1473,21 @@ struct Consumer {
       else
         mask = bits(grp_lo(kb_a), grp_hi(go.kbs - 1)) | bits(0, grp_hi(kb_b));
     }
-    // condition i = (sequence b, KV head g) for the flagged groups; unflagged groups pass at once
-    const int* f = p.o_cnt + (size_t)l * p.MB * p.hkv;
-    cta_wait_all(p.B * p.hkv, [&](int i) {
-      const int b = i / p.hkv, g = i % p.hkv;
-      return ((mask >> g) & 1ull) ? count_reached(f + (size_t)b * p.hkv + g, p.nch) : WaitCond{nullptr, 0u};
+    // condition g = KV head g's merged slices of every sequence (B * nch of them) for the flagged
+    // heads; unflagged heads pass at once
+    const int* f = p.o_cnt + (size_t)l * p.hkv;
+    cta_wait_all(p.hkv, [&](int g) {
+      return ((mask >> g) & 1ull) ? count_reached(f + g, p.B * p.nch) : WaitCond{nullptr, 0u};
     }, 16);
   }
 
   // wait for the final SwiGLU rows of the n experts whose down-projection k blocks the CTA's
   // tiles read: expert slots v0, v0 + 1, ... (wrapping after nv; slot U is the shared expert)
   __device__ void wait_h(int l, int v0, int n, int nv, int U) {
-    cta_wait_all(n * p.n_rb_gu, [&](int i) {
-      const int j = i / p.n_rb_gu, rb = i - j * p.n_rb_gu;
+    cta_wait_all(n, [&](int j) {
       const int v = (v0 + j) % nv;
       const int slot = v < U ? v : p.umax;
-      return WaitCond{p.h_flag + ((size_t)l * (p.umax + 1) + slot) * p.n_rb_gu + rb, p.epoch};
+      return count_reached(p.h_cnt + (size_t)l * (p.umax + 1) + slot, (int)p.epoch * p.n_rb_gu);
     }, 17);
   }
 
@@ -1659,7 +1715,7 @@ struct Consumer {
           p.obuf[(size_t)a.b * p.hq * HD + (size_t)a.g * G * HD + o] = f2bf(A);
         }
         cons_sync();
-        if (tid == kPubThread) red_release_add(p.o_cnt + gi, 1);
+        if (tid == kPubThread) red_release_add(p.o_cnt + (size_t)l * p.hkv + a.g, 1);
       }
       cons_sync();
     }
@@ -1736,8 +1792,8 @@ struct Consumer {
             case 5: {
               cta_stamp(l, S_GU_DONE);
               // down projections of all active experts, gate-weighted, + residual
-              // (the CTA's tiles run through k-block runs s0 .. s1 of kb_i tiles, run s of
-              // expert slot s % nv: it stages the SwiGLU rows of the first min(runs, nv) of them)
+              // (the CTA's tiles run through expert runs s0 .. s1 of tpe tiles, run s of expert
+              // slot s % nv: it stages the SwiGLU rows of the first min(runs, nv) of them)
               const StageGeo g = stage_geo(p, K_D, U);
               const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
               const int nv = U + p.nsh;
