@@ -214,6 +214,34 @@ def test_moe_layer_kv8192_hidden_input(moe8):
     assert rel_l2(bf16_to_f64(t_bits(vg)), bf16_to_f64(kv["v"][0, :, 8192])) < 1e-2
 
 
+def test_moe_layer_batch4_expert_major_down(moe8):
+    """Full-size layer at batch 4 (up to 33 active expert slots: the expert-major order of the
+    down projections, and CTA-wide waits over every KV head of four sequences), each sequence
+    against the oracle with its own ragged KV history."""
+    m_cpu, m_gpu = moe8
+    cfg = synth.MOE_LAYER
+    B = 4
+    lens = [1024 + 77 * b for b in range(B)]
+    orc = oracle.Oracle(_one_layer(m_cpu))
+    eng = _engine(_one_layer(m_gpu), max_ctx=2048, max_batch=B)
+    x = synth.gen_hidden(B, cfg.hidden, seed=9, device="cuda")
+    outs = []
+    for b in range(B):
+        k, v = synth.gen_kv(cfg, lens[b], seed=40 + b, device="cuda")
+        eng.prefill_import(k, v, seq=b)
+        kv = orc.new_kv(2048)
+        orc.import_kv(kv, k.cpu(), v.cpu(), lens[b])
+        outs.append(orc.decode_step(kv, lens[b], hidden=t_bits(x)[b], want_trace=True))
+    _, _, g_hidden = _gpu_step(eng, hidden=x, batch=B)
+    gi, gg = eng.routing(0)
+    assert len(set(gi[:B].reshape(-1).tolist())) + 1 > 12  # the expert-major order was taken
+    for b, o in enumerate(outs):
+        assert topk_ok(gi[b], o["trace"]["topk_idx"][0], o["trace"]["router_score"][0], 8)
+        if set(gi[b]) == set(o["trace"]["topk_idx"][0]):
+            assert rel_l2(bf16_to_f64(g_hidden[b]), bf16_to_f64(o["hidden"])) <= 1e-2
+        assert eng.get_length(b) == lens[b] + 1
+
+
 def _bf16(x):
     return torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
 
