@@ -237,7 +237,8 @@ dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* 
    (or dense FFN) gate/up, 4 routed gate/up, 5 down projections, 6 LM head, 7 attention, 8 grid
    barrier, 9 routing wait, 10 step; event: 0 begin, 1 last tile consumed, 2 finalisers done
    (barrier: its site). Words [512 - 128, 512) hold CTA 0's producer trace in the same format.
-   Words from 512 on hold per-CTA %globaltimer stamps of the first 8 layers: word
+   In a library built with DEC_STAMPS=1, words from 512 on hold per-CTA %globaltimer stamps of
+   the first 8 layers (the default build leaves them zero): word
    512 + (layer * 16 + point) * grid + cta, for the points q/k/v tiles consumed (0), q/k/v done
    (1), attention merged (2), attention outputs ready (3), output-projection tiles consumed (4)
    and done (5), x_mid ready (6), router partials published (7), routing known (8), gate/up

@@ -25,6 +25,9 @@ constexpr int kKvTilePos = 64;                       // KV positions per ring sl
 constexpr int kMaxBatch = 8;
 constexpr int kMaxHidden = 4096;                     // hidden sizes the kernel handles
 constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
+#ifndef DEC_STAMPS
+#define DEC_STAMPS 0  // 1: record the per-CTA dependency stamps (diagnostics)
+#endif
 constexpr int kStampsPerLayer = 16;                  // per-CTA dependency time stamps of a layer
 constexpr int kStampLayers = 8;                      // layers whose stamps are kept
 constexpr int kBarTrace = kStampsPerLayer * kStampLayers;  // per-CTA stamp words per CTA

@@ -495,9 +495,10 @@ struct Consumer {
     }
   }
 
-  // every CTA's time at dependency point k (a Stamp) of layer l < kStampLayers
+  // every CTA's time at dependency point k (a Stamp) of layer l < kStampLayers; only in a
+  // library built with DEC_STAMPS=1 (the stores cost a few KB of code in every phase)
   __device__ void cta_stamp(int l, int k) {
-    if (tid == 0 && l < kStampLayers)
+    if (DEC_STAMPS && tid == 0 && l < kStampLayers)
       p.trace[kTraceSlots + ((size_t)l * kStampsPerLayer + k) * gridDim.x + blockIdx.x] = gtimer();
   }
 
