@@ -232,13 +232,16 @@ dec_status dec_get_info(dec_engine* eng, dec_info* out);
    gates [max_batch][top_k]; rows >= the step's batch are stale. Synchronises. */
 dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* gates);
 
-/* Per-step trace written by CTA 0: (event code, %globaltimer ns) pairs in host_buf[2i], [2i+1].
+/* Diagnostics of the last step, recorded only by a library built with DEC_TRACE=1 /
+   DEC_STAMPS=1 (`DEC_DIAG=1` when running latency_moe_decode_gb300/build.py; the default build
+   records nothing, its words stay zero: the stores cost the step ~4% in instruction fetch).
+   Per-step trace written by CTA 0: (event code, %globaltimer ns) pairs in host_buf[2i], [2i+1].
    code = what << 4 | event; what: 0 q/k/v GEMV, 1 output projection, 2 router, 3 shared-expert
    (or dense FFN) gate/up, 4 routed gate/up, 5 down projections, 6 LM head, 7 attention, 8 grid
    barrier, 9 routing wait, 10 step; event: 0 begin, 1 last tile consumed, 2 finalisers done
    (barrier: its site). Words [512 - 128, 512) hold CTA 0's producer trace in the same format.
-   In a library built with DEC_STAMPS=1, words from 512 on hold per-CTA %globaltimer stamps of
-   the first 8 layers (the default build leaves them zero): word
+   With DEC_STAMPS=1, words from 512 on hold per-CTA %globaltimer stamps of the first 8 layers:
+   word
    512 + (layer * 16 + point) * grid + cta, for the points q/k/v tiles consumed (0), q/k/v done
    (1), attention merged (2), attention outputs ready (3), output-projection tiles consumed (4)
    and done (5), x_mid ready (6), router partials published (7), routing known (8), gate/up

@@ -35,6 +35,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
            "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
+    if os.environ.get("DEC_DIAG") == "1":  # diagnostics build: event trace and per-CTA stamps
+        cmd += ["-DDEC_TRACE=1", "-DDEC_STAMPS=1"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

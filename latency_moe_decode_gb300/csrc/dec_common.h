@@ -28,6 +28,9 @@ constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace w
 #ifndef DEC_STAMPS
 #define DEC_STAMPS 0  // 1: record the per-CTA dependency stamps (diagnostics)
 #endif
+#ifndef DEC_TRACE
+#define DEC_TRACE 0  // 1: record CTA 0's event trace (diagnostics)
+#endif
 constexpr int kStampsPerLayer = 16;                  // per-CTA dependency time stamps of a layer
 constexpr int kStampLayers = 8;                      // layers whose stamps are kept
 constexpr int kBarTrace = kStampsPerLayer * kStampLayers;  // per-CTA stamp words per CTA

@@ -267,7 +267,7 @@ struct Producer {
   // code = what << 4 | event, event 0 = first copy of a stage issued, 1 = last copy issued
   // (what: GEMV kind, 7 attention, 9 routing wait with 0 = begin, 1 = flag seen).
   __device__ void trace(int code) {
-    if (blockIdx.x == 0 && stamp + 1 < kProducerTrace) {
+    if (DEC_TRACE && blockIdx.x == 0 && stamp + 1 < kProducerTrace) {
       p.trace[kTraceSlots - kProducerTrace + stamp] = (unsigned long long)code;
       p.trace[kTraceSlots - kProducerTrace + stamp + 1] = gtimer();
       stamp += 2;
@@ -488,7 +488,7 @@ struct Consumer {
   // GEMV kind (0..6), 7 attention, 8 grid barrier, 9 routing wait, 10 step start/end, and event
   // 0 = begin, 1 = last tile consumed, 2 = finalisers done (barrier: its site number).
   __device__ void trace(int code) {
-    if (blockIdx.x == 0 && tid == 0 && stamp + 1 < kTraceSlots - kProducerTrace) {
+    if (DEC_TRACE && blockIdx.x == 0 && tid == 0 && stamp + 1 < kTraceSlots - kProducerTrace) {
       p.trace[stamp] = (unsigned long long)code;
       p.trace[stamp + 1] = gtimer();
       stamp += 2;
