@@ -257,6 +257,11 @@ struct Producer {
   unsigned item = 0;  // slots issued so far in this step
   int pslot = 0;      // ring slot of the next item (item % ring, kept without divisions)
   unsigned plap = 0;  // times the ring has wrapped (item / ring)
+  // L2 eviction policies of the bulk copies. Weight tiles: evict first. They are read once per
+  // step (~1.9 GB go through L2 per step at the 8-layer stack); without the hint they push out
+  // the small exchange data (partial sums, counters, activations) that the CTAs' hops read back
+  // from L2, and the step is ~4% longer. KV rows: normal priority (measured marginally better).
+  uint64_t pol_stream = 0, pol_kv = 0;
   unsigned landed = 0;  // issued slots seen to have landed, in issue order
   int lslot = 0;        // ring slot of item `landed`
   unsigned llap = 0;    // its lap (landed / ring)
@@ -355,9 +360,10 @@ struct Producer {
       }
       mbar_arrive_expect_tx(&full[slot], (unsigned)n * kTileBytes);
       if (n == 2 && src[1] == src[0] + kTileBytes) {
-        bulk_g2s(dst, src[0], 2 * kTileBytes, &full[slot]);
+        bulk_g2s_hint(dst, src[0], 2 * kTileBytes, &full[slot], pol_stream);
       } else {
-        for (int j = 0; j < n; ++j) bulk_g2s(dst + (size_t)j * kTileBytes, src[j], kTileBytes, &full[slot]);
+        for (int j = 0; j < n; ++j)
+          bulk_g2s_hint(dst + (size_t)j * kTileBytes, src[j], kTileBytes, &full[slot], pol_stream);
       }
       advance();
     }
@@ -385,8 +391,8 @@ struct Producer {
           continue;
         }
         mbar_arrive_expect_tx(&full[slot], 2u * n * row_bytes);
-        bulk_g2s(dst, p.kc + r0, n * row_bytes, &full[slot]);
-        bulk_g2s(dst + kKvTilePos * row_bytes, p.vc + r0, n * row_bytes, &full[slot]);
+        bulk_g2s_hint(dst, p.kc + r0, n * row_bytes, &full[slot], pol_kv);
+        bulk_g2s_hint(dst + kKvTilePos * row_bytes, p.vc + r0, n * row_bytes, &full[slot], pol_kv);
         advance();
       }
     }
@@ -426,6 +432,8 @@ struct Producer {
   __device__ void run() {
     int elist[kMaxExperts];
     int U = 0;
+    pol_stream = l2_policy(true);
+    pol_kv = l2_policy(false);
 #pragma unroll 1
     for (int l = 0; l <= p.L && !dead; ++l) {
       const bool lm = l == p.L;

@@ -90,15 +90,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, const KP
 }
 
 // ---------------------------------------------------------------------------------------------
-// bulk copies (TMA, non-tensor): global -> this CTA's shared memory, completing on an mbarrier.
-// Addresses 16-byte aligned, size a multiple of 16.
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+// bulk copies (TMA, non-tensor): global -> this CTA's shared memory, completing on an mbarrier,
+// with an L2 eviction-priority hint (a policy made by createpolicy). Addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, unsigned bytes, uint64_t* bar,
+                                              uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
           smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+// every access of a copy gets the evict-first priority (its lines leave L2 before others) or
+// the normal one
+__device__ __forceinline__ uint64_t l2_policy(bool evict_first) {
+  uint64_t pol;
+  if (evict_first)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
