@@ -23,11 +23,13 @@
 //               the result of its own arrival).
 // Cross-CTA data flow of a layer: the q/k/v, output-projection and router partials are read
 // directly by every CTA that needs them (attention units, the x_mid norm, the routing, which
-// every CTA computes itself); the attention chunks are merged by the unit of the last chunk;
-// SwiGLU rows and the layer output row blocks are finalised by the owner of each group's last
-// tile, which waits for the group's counter and publishes an epoch flag. There is no grid
-// barrier: each consumer waits only for the data it reads. Every wait is bounded and turns into
-// an error status instead of a hang.
+// every CTA computes itself); the attention chunks of a (sequence, KV head) are merged in slices
+// by all of its chunks' CTAs; SwiGLU rows and the layer output row blocks are finalised by CTAs
+// designated per group (spread evenly over the grid), which wait for the group's counter and
+// publish a counter arrival (SwiGLU) or an epoch flag (layer output). There is no grid barrier:
+// each consumer waits only for the data it reads. Every wait is bounded and turns into an error
+// status instead of a hang. Weight copies carry an L2 evict-first hint, so the streamed weights
+// do not evict the small exchange data the hops read back.
 #pragma once
 #include "dec_prims.cuh"
 
