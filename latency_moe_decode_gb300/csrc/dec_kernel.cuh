@@ -1403,10 +1403,10 @@ struct Consumer {
         return count_reached(cnt + rb, (int)p.epoch * gq.kbs);
       }, 13);
     }
-    // Each thread sums the contributor partials of its NPT values. All loads of a batch of eight
+    // Each thread sums the contributor partials of its NPT values. All loads of a batch of five
     // contributors (for all NPT values, and the thread's RoPE angles) are issued before any is
-    // used, so the sums cost one L2 round trip per batch; each value is still summed in
-    // contributor order.
+    // used, so the sums cost one L2 round trip per batch (a q/k/v row block has at most five
+    // contributors on 152 SMs); each value is still summed in contributor order.
     constexpr int NV_ = (G + 2) * HD;
     constexpr int NPT = (NV_ + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
     float* raw = qkvn + NV_;
@@ -1428,16 +1428,16 @@ struct Consumer {
       psum[i] = 0.f;
       cs[i] = (idx < NV_ && t <= G) ? __ldg(p.rope + (size_t)pos * (HD / 2) + d % (HD / 2)) : make_float2(1.f, 0.f);
     }
-    for (int c0 = 0; c0 < ncmax; c0 += 8) {
-      float v[NPT][8];
+    for (int c0 = 0; c0 < ncmax; c0 += 5) {
+      float v[NPT][5];
 #pragma unroll
       for (int i = 0; i < NPT; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[i][j] = (c0 + j < pnc[i]) ? ldcg(pbase[i] + (size_t)(c0 + j) * pst) : 0.f;
+        for (int j = 0; j < 5; ++j) v[i][j] = (c0 + j < pnc[i]) ? ldcg(pbase[i] + (size_t)(c0 + j) * pst) : 0.f;
 #pragma unroll
       for (int i = 0; i < NPT; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) psum[i] += v[i][j];
+        for (int j = 0; j < 5; ++j) psum[i] += v[i][j];
     }
 #pragma unroll
     for (int i = 0; i < NPT; ++i) {
