@@ -123,6 +123,30 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+def ranks_barrier():
+    """Barrier over the ranks of a torchrun job (nothing on one rank)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def max_over_ranks(seconds: float, device: str) -> float:
+    """The longest timed region over the ranks (the job ends when its slowest rank does)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, seconds: float) -> float:
+    """Units all ranks processed (each rank the same fixed share: weak scaling) per second of
+    the slowest rank's timed region."""
+    return units_per_rank * world / seconds
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -200,9 +224,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         one_step()
     eng.sync()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    ranks_barrier()
     torch.cuda.synchronize()
     times = []
     with ClockSampler(local) as clk:
@@ -210,14 +232,9 @@ def run_ours(args):
             times.append(one_step())
     torch.cuda.synchronize()
     eng.sync()
-    total = sum(times)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-    tokens = n_dec * batch * args.steps * world
-    value = tokens / total
+    ranks_barrier()
+    total = max_over_ranks(sum(times), "cuda")
+    value = whole_job_rate(n_dec * batch * args.steps, world, total)
 
     # routing actually taken in the last step (distinct experts per layer) for the byte count
     distinct = []
