@@ -884,32 +884,6 @@ struct Consumer {
     }
   }
 
-  // eight consecutive rows of one segment, all contributor slots loaded together
-  __device__ __forceinline__ void seg_sum8(int kind, const StageGeo& g, int seg, int b, int row0, float (&o)[8]) const {
-    const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
-    const float* src = part_base(kind) + (size_t)seg * g.kbs * p.MB * kTileRows + (size_t)b * kTileRows + row0;
-    const size_t st = (size_t)p.MB * kTileRows;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = 0.f;
-    for (int c0 = 0; c0 < nc; c0 += 4) {
-      float4 v[4][2];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (c0 + j < nc) {
-          v[j][0] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * st));
-          v[j][1] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * st + 4));
-        } else {
-          v[j][0] = v[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        o[0] += v[j][0].x; o[1] += v[j][0].y; o[2] += v[j][0].z; o[3] += v[j][0].w;
-        o[4] += v[j][1].x; o[5] += v[j][1].y; o[6] += v[j][1].z; o[7] += v[j][1].w;
-      }
-    }
-  }
-
   __device__ void gemv_stage(int kind, int l, int U) {
     const StageGeo g = stage_geo(p, kind, U);
     const int G_ = gridDim.x;

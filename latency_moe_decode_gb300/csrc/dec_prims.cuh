@@ -112,9 +112,6 @@ __device__ __forceinline__ uint64_t l2_policy(bool evict_first) {
   return pol;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 // ---------------------------------------------------------------------------------------------
 // cross-CTA memory
