@@ -17,7 +17,14 @@
  *  - FP8 matrices are OCP E4M3 codes, row-major [rows][cols], with fp32 block scales
  *    [ceil(rows/128)][ceil(cols/128)]; element (r, c) means scale[r/128][c/128] * e4m3(W[r][c]).
  *  - A `stream` argument is a cudaStream_t; NULL means the engine's own (non-blocking) stream,
- *    so the legacy default stream must be passed as cudaStreamLegacy.
+ *    so the legacy default stream must be passed as cudaStreamLegacy. Consecutive steps of one
+ *    engine share its counters, exchange buffers and KV cache, so they must not overlap: when a
+ *    call queues work on a different stream than the engine's previous work, the library makes
+ *    the new stream wait for the old one (an event), so calls of one engine run in call order
+ *    whatever streams they are given. Work of other engines and other libraries is never waited
+ *    for: no entry point synchronises the whole device.
+ *  - Entry points that queue device work require the engine's device to be the current CUDA
+ *    device (DEC_ERR_ARG otherwise).
  *  - Every call returns a dec_status. Errors found on the device (a wait that ran out of time,
  *    a failed bounds check) are reported by the next call that synchronises (dec_sync,
  *    dec_generate, dec_prefill_kv, dec_export_kv) and POISON the engine: later calls return
@@ -119,6 +126,9 @@ dec_status dec_validate_cfg(const dec_model_cfg* cfg);
    queued on `stream` and synchronised before return. *out receives the engine (NULL on
    failure).
    Environment, read here: DEC_TIMEOUT_MS bounds every device-side wait (default 1000);
+   DEC_TEST_SKIP_ARRIVAL=1 (tests of the failure path only) makes the CTA holding the first
+   q/k/v tile withhold that partial sum's arrival in layer 0, so the waits for it run out after
+   DEC_TIMEOUT_MS and the step ends with DEC_ERR_TIMEOUT instead of hanging;
    DEC_EPOCH_LIMIT lowers the number of steps after which a step first zeroes the engine's
    cross-step counters and flags (a cudaMemsetAsync on the step's stream) and restarts its epoch
    (default 2^30 / the largest number of k blocks of a row block), so tests can make it happen. */
@@ -160,7 +170,9 @@ dec_status dec_prefill_kv(dec_engine* eng, const dec_ctx* ctx);
      any stream capture begins.
    - Nothing needs to start at zero: a call writes every id it reads before reading it.
    - The array is shared by all engines on a device: overlapping calls (two host threads, or two
-     engines on one device) race on it; the caller must serialise them.
+     engines on one device) race on it; the caller must serialise them. Within one engine the
+     call is stream-ordered after the engine's earlier work (no device-wide synchronisation).
+   - The engine's device must be the current device (DEC_ERR_ARG otherwise).
    Results, capacity checks and synchronisation are those of dec_prefill_kv's token mode. */
 #define DEC_NOALLOC_PREFILL_MAX_IDS 65536
 dec_status dec_prefill_kv_noalloc(dec_engine* eng, const dec_ctx* ctx);
@@ -232,6 +244,12 @@ dec_status dec_get_info(dec_engine* eng, dec_info* out);
    gates [max_batch][top_k]; rows >= the step's batch are stale. Synchronises. */
 dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* gates);
 
+/* The router logits (fp32, before the sigmoid) the most recent step selected from at one layer
+   (MoE models): host logits [max_batch][n_experts]; rows >= the step's batch are stale. With
+   dec_get_routing this lets a caller check that a selection is the top_k of its own logits
+   (ties to the lower expert index). Synchronises. */
+dec_status dec_get_router_logits(dec_engine* eng, int32_t layer, float* logits);
+
 /* Diagnostics of the last step, recorded only by a library built with DEC_TRACE=1 /
    DEC_STAMPS=1 (`DEC_DIAG=1` when running latency_moe_decode_gb300/build.py; the default build
    records nothing, its words stay zero: the stores cost the step ~4% in instruction fetch).
@@ -249,6 +267,15 @@ dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* 
    (13), layer barrier passed (14). Copies up to n words and returns the count in *n_written.
    Synchronises. */
 dec_status dec_get_trace(dec_engine* eng, uint64_t* host_buf, int32_t n, int32_t* n_written);
+
+/* Per-layer timing of the most recent step, recorded in every build by one thread of the first
+   CTA: host_buf[l] is the %globaltimer time (ns) at which the input of layer l was final, as
+   that CTA saw it (l = 0: the step start; l = n_layers: the final norm's input), and
+   host_buf[n_layers + 1] the time that CTA finished the step. So host_buf[l + 1] - host_buf[l]
+   is layer l's time on the critical path and the last difference the LM head's tail. Copies
+   min(n, n_layers + 2) words and returns the count in *n_written. Synchronises with the
+   engine's work. */
+dec_status dec_get_layer_times(dec_engine* eng, uint64_t* host_buf, int32_t n, int32_t* n_written);
 
 /* Reason for the last failing call on this engine ("" if none). Valid until the next call. */
 const char* dec_last_error(const dec_engine* eng);

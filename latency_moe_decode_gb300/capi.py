@@ -73,7 +73,9 @@ PROTOTYPES = {
     "dec_sync": (C.c_int, [C.c_void_p]),
     "dec_get_info": (C.c_int, [C.c_void_p, C.POINTER(DecInfo)]),
     "dec_get_routing": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
+    "dec_get_router_logits": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p]),
     "dec_get_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int32, C.POINTER(C.c_int32)]),
+    "dec_get_layer_times": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int32, C.POINTER(C.c_int32)]),
     "dec_last_error": (C.c_char_p, [C.c_void_p]),
     "dec_status_string": (C.c_char_p, [C.c_int]),
     "dec_destroy": (None, [C.c_void_p]),

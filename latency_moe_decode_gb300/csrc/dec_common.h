@@ -106,10 +106,15 @@ struct KParams {
   // routing of each layer, written by CTA 0 for inspection (every CTA computes it itself)
   int* rt_idx;        // [L][MB][topk] selections (score-descending)
   float* rt_topk_gate;// [L][MB][topk]
+  float* rt_logits;   // [L][MB][E] router logits the selection was made from
   unsigned long long* amax;  // [MB] packed (ordered logit, ~id) maxima
   int* err;           // device status word
   float* logits_ws;   // [MB][V] when the caller gives no logits buffer
   unsigned long long* trace;  // [kTraceSlots + kBarTrace * grid]
+  // CTA 0's %globaltimer when the input of layer l was ready (l = 0: step start; l = L: the
+  // final norm's input) and, at [L + 1], when CTA 0 finished the step: [L + 2], every build
+  unsigned long long* layer_ts;
+  int test_skip;  // nonzero only in tests: the first q/k/v tile's arrival of layer 0 is withheld
   // this step
   const int32_t* tokens;
   const uint16_t* hidden_in;

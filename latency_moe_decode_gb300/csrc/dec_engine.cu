@@ -122,6 +122,10 @@ struct dec_engine {
   dec_model_cfg cfg{};
   int device = 0, sms = 0, grid = 0;
   cudaStream_t stream = nullptr;
+  // The stream of the engine's most recent work. Consecutive steps share counters, exchange
+  // buffers and the KV cache, so work on another stream is ordered after it (order_on).
+  cudaStream_t last_stream = nullptr;
+  cudaEvent_t order_ev = nullptr;
   KParams base{};
   std::vector<void*> allocs;
   LayerDev* d_layers = nullptr;
@@ -232,9 +236,38 @@ dec_status copy_bf16(dec_engine* e, const void* src, size_t n, uint16_t** out) {
 
 int range_lo_h(int T, int c, int G) { return (int)((long long)T * c / G); }
 
+// Order work about to be queued on stream s after everything the engine queued before (on
+// whichever stream that was): an event on the previous stream that s waits for, only when the
+// stream changes. Steps of one engine therefore never overlap, whatever streams they are given.
+dec_status order_on(dec_engine* e, cudaStream_t s) {
+  if (e->last_stream != s) {
+    DEC_CUDA(cudaEventRecord(e->order_ev, e->last_stream));
+    DEC_CUDA(cudaStreamWaitEvent(s, e->order_ev, 0));
+    e->last_stream = s;
+  }
+  return DEC_OK;
+}
+
+// Wait on the host for all of the engine's queued work (and nothing else on the device).
+dec_status quiesce(dec_engine* e) {
+  dec_status st = order_on(e, e->stream);
+  if (st != DEC_OK) return st;
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
+  return DEC_OK;
+}
+
+// Entry points that queue work need the engine's device to be the current one.
+dec_status check_device(dec_engine* e) {
+  int cur = -1;
+  DEC_CUDA(cudaGetDevice(&cur));
+  if (cur != e->device) return fail(e, DEC_ERR_ARG, "the engine's device is not the current CUDA device");
+  return DEC_OK;
+}
+
 dec_status check_device_status(dec_engine* e) {
   int code = 0;
-  DEC_CUDA(cudaMemcpy(&code, e->base.err, sizeof(int), cudaMemcpyDeviceToHost));
+  DEC_CUDA(cudaMemcpyAsync(&code, e->base.err, sizeof(int), cudaMemcpyDeviceToHost, e->stream));
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
   if (code == 0) return DEC_OK;
   e->poisoned = true;
   char buf[160];
@@ -360,6 +393,9 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   if (!prop.cooperativeLaunch) return bail(DEC_ERR_UNSUPPORTED);
   ce = cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking);
   if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaStreamCreate"));
+  e->last_stream = e->stream;
+  ce = cudaEventCreateWithFlags(&e->order_ev, cudaEventDisableTiming);
+  if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaEventCreate"));
   cudaStream_t user = stream ? static_cast<cudaStream_t>(stream) : e->stream;
   // weights are read on the engine's stream: order after the caller's pending work
   {
@@ -589,10 +625,12 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     }
     Z(p.rt_idx, sizeof(int) * c.n_layers * MB * std::max(1, c.top_k));
     Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
+    Z(p.rt_logits, sizeof(float) * c.n_layers * MB * std::max(1, c.n_experts));
     Z(p.amax, sizeof(unsigned long long) * MB);
     Z(p.err, sizeof(int) * 32);
     Z(p.logits_ws, sizeof(float) * MB * std::max(1, c.vocab));
     Z(p.trace, sizeof(unsigned long long) * (kTraceSlots + (size_t)kBarTrace * G));
+    Z(p.layer_ts, sizeof(unsigned long long) * (c.n_layers + 2));
     Z(e->d_hist, sizeof(int32_t) * (size_t)(c.max_ctx + 1) * MB);
 #undef Z
   }
@@ -643,6 +681,9 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     double ms = tm ? atof(tm) : 1000.0;
     if (!(ms > 0)) ms = 1000.0;
     p.timeout_ns = (unsigned long long)(ms * 1e6);
+    // tests only: the first q/k/v tile's layer-0 arrival is withheld, so the waits for it run out
+    const char* sk = getenv("DEC_TEST_SKIP_ARRIVAL");
+    p.test_skip = (sk && atoi(sk) == 1) ? 1 : 0;
   }
   e->lengths.assign(c.max_batch, 0);
   ce = cudaStreamSynchronize(e->stream);
@@ -654,6 +695,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
 dec_status dec_step_ex(dec_engine* e, const dec_step_args* a) {
   if (!e || !a) return DEC_ERR_ARG;
   if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  if (dec_status ds = check_device(e)) return ds;
   const dec_model_cfg& c = e->cfg;
   if (a->batch == 0) return DEC_OK;
   if (a->batch < 0 || a->seq0 < 0 || a->seq0 + a->batch > c.max_batch) return fail(e, DEC_ERR_ARG, "batch/seq0 out of range");
@@ -675,6 +717,7 @@ dec_status dec_step_ex(dec_engine* e, const dec_step_args* a) {
   p.next_tokens = a->next_tokens;
   p.hidden_out = static_cast<uint16_t*>(a->hidden_out);
   cudaStream_t s = a->stream ? static_cast<cudaStream_t>(a->stream) : e->stream;
+  if (dec_status os = order_on(e, s)) return os;
   if (e->epoch >= e->epoch_limit) {
     for (const auto& b : e->epoch_bufs) {
       cudaError_t me = cudaMemsetAsync(b.first, 0, b.second, s);
@@ -708,8 +751,7 @@ dec_status dec_step(dec_engine* e, const int32_t* token_ids, int32_t batch, floa
 
 dec_status dec_sync(dec_engine* e) {
   if (!e) return DEC_ERR_ARG;
-  DEC_CUDA(cudaStreamSynchronize(e->stream));
-  DEC_CUDA(cudaDeviceSynchronize());
+  if (dec_status qs = quiesce(e)) return qs;
   if (e->poisoned) return fail(e, DEC_ERR_POISONED, e->err.empty() ? "engine poisoned" : e->err);
   return check_device_status(e);
 }
@@ -721,7 +763,8 @@ dec_status dec_prefill_kv(dec_engine* e, const dec_ctx* x) {
   if (x->n_seq < 1 || x->seq < 0 || x->seq + x->n_seq > c.max_batch || x->n_tokens < 0)
     return fail(e, DEC_ERR_ARG, "bad slot range");
   if (x->n_tokens == 0) return DEC_OK;
-  DEC_CUDA(cudaDeviceSynchronize());  // earlier steps may be queued on a caller stream
+  if (dec_status ds = check_device(e)) return ds;
+  if (dec_status os = order_on(e, e->stream)) return os;  // after earlier steps, on any stream
   if (x->k_import) {
     if (!x->v_import) return fail(e, DEC_ERR_ARG, "v_import missing");
     if (x->n_tokens > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "import longer than max_ctx");
@@ -793,10 +836,14 @@ dec_status dec_prefill_kv_noalloc(dec_engine* e, const dec_ctx* x) {
   if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "token prefill needs an embedding");
   for (int s = x->seq; s < x->seq + x->n_seq; ++s)
     if (e->lengths[s] + x->n_tokens > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "prefill exceeds max_ctx");
+  if (dec_status ds = check_device(e)) return ds;
   int32_t* tt = nullptr;
   dec_status st = prefill_ids_scratch(e, &tt);
   if (st != DEC_OK) return st;
-  DEC_CUDA(cudaDeviceSynchronize());  // earlier steps (or an earlier call) may still read the ids
+  // Stream order, not a device-wide wait: the transpose that overwrites the ids runs on the
+  // engine's stream after the engine's earlier work (an earlier call of this engine ended with
+  // its steps synchronised; other engines on the device are the caller's to serialise).
+  if (dec_status os = order_on(e, e->stream)) return os;
   const int n = x->n_seq * x->n_tokens;
   transpose_tokens_kernel<<<(n + 255) / 256, 256, 0, e->stream>>>(x->token_ids, x->n_seq, x->n_tokens, tt);
   DEC_CUDA(cudaGetLastError());
@@ -820,7 +867,9 @@ dec_status dec_generate(dec_engine* e, const int32_t* first, int32_t batch, int3
   const dec_model_cfg& c = e->cfg;
   if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "generate needs an LM head");
   if (batch > c.max_batch || n_steps > c.max_ctx) return fail(e, DEC_ERR_ARG, "batch or n_steps too large");
+  if (dec_status ds = check_device(e)) return ds;
   cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
+  if (dec_status os = order_on(e, s)) return os;  // d_hist may still be read by earlier steps
   const int MB = c.max_batch;
   DEC_CUDA(cudaMemcpyAsync(e->d_hist, first, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s));
   for (int i = 0; i < n_steps; ++i) {
@@ -831,13 +880,14 @@ dec_status dec_generate(dec_engine* e, const int32_t* first, int32_t batch, int3
     DEC_CUDA(cudaMemcpy2DAsync(out, sizeof(int32_t) * batch, e->d_hist + MB, sizeof(int32_t) * MB,
                                sizeof(int32_t) * batch, n_steps, cudaMemcpyDeviceToHost, s));
   DEC_CUDA(cudaStreamSynchronize(s));
+  if (dec_status qs = quiesce(e)) return qs;
   return check_device_status(e);
 }
 
 dec_status dec_set_length(dec_engine* e, int32_t seq, int32_t length) {
   if (!e) return DEC_ERR_ARG;
   if (seq < 0 || seq >= e->cfg.max_batch || length < 0 || length > e->cfg.max_ctx) return fail(e, DEC_ERR_ARG, "bad length");
-  DEC_CUDA(cudaDeviceSynchronize());  // steps may be queued on any stream
+  if (dec_status qs = quiesce(e)) return qs;  // steps may be queued on any stream
   e->lengths[seq] = length;
   DEC_CUDA(cudaMemcpyAsync(e->base.lengths + seq, &e->lengths[seq], sizeof(int32_t), cudaMemcpyHostToDevice, e->stream));
   DEC_CUDA(cudaStreamSynchronize(e->stream));
@@ -855,15 +905,18 @@ dec_status dec_export_kv(dec_engine* e, int32_t seq, int32_t layer, int32_t pos0
   const dec_model_cfg& c = e->cfg;
   if (seq < 0 || seq >= c.max_batch || layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > c.max_ctx)
     return fail(e, DEC_ERR_ARG, "export range");
-  DEC_CUDA(cudaDeviceSynchronize());
+  if (dec_status os = order_on(e, e->stream)) return os;
   const size_t row = (size_t)c.head_dim * 2;
   for (int g = 0; g < c.n_kv_heads; ++g) {
     size_t src = ((((size_t)layer * c.max_batch + seq) * c.n_kv_heads + g) * c.max_ctx + pos0) * row;
-    DEC_CUDA(cudaMemcpy(static_cast<uint8_t*>(k_out) + (size_t)g * n * row,
-                        reinterpret_cast<const uint8_t*>(e->base.kc) + src, n * row, cudaMemcpyDeviceToDevice));
-    DEC_CUDA(cudaMemcpy(static_cast<uint8_t*>(v_out) + (size_t)g * n * row,
-                        reinterpret_cast<const uint8_t*>(e->base.vc) + src, n * row, cudaMemcpyDeviceToDevice));
+    DEC_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(k_out) + (size_t)g * n * row,
+                             reinterpret_cast<const uint8_t*>(e->base.kc) + src, n * row, cudaMemcpyDeviceToDevice,
+                             e->stream));
+    DEC_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(v_out) + (size_t)g * n * row,
+                             reinterpret_cast<const uint8_t*>(e->base.vc) + src, n * row, cudaMemcpyDeviceToDevice,
+                             e->stream));
   }
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
   return DEC_OK;
 }
 
@@ -885,18 +938,42 @@ dec_status dec_get_routing(dec_engine* e, int32_t layer, int32_t* idx, float* ga
   if (!e || !idx || !gates) return DEC_ERR_ARG;
   const dec_model_cfg& c = e->cfg;
   if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
-  DEC_CUDA(cudaDeviceSynchronize());
+  if (dec_status os = order_on(e, e->stream)) return os;
   const size_t n = (size_t)c.max_batch * c.top_k, off = (size_t)layer * n;
-  DEC_CUDA(cudaMemcpy(idx, e->base.rt_idx + off, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
-  DEC_CUDA(cudaMemcpy(gates, e->base.rt_topk_gate + off, sizeof(float) * n, cudaMemcpyDeviceToHost));
+  DEC_CUDA(cudaMemcpyAsync(idx, e->base.rt_idx + off, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, e->stream));
+  DEC_CUDA(cudaMemcpyAsync(gates, e->base.rt_topk_gate + off, sizeof(float) * n, cudaMemcpyDeviceToHost, e->stream));
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
+  return DEC_OK;
+}
+
+dec_status dec_get_router_logits(dec_engine* e, int32_t layer, float* logits) {
+  if (!e || !logits) return DEC_ERR_ARG;
+  const dec_model_cfg& c = e->cfg;
+  if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
+  if (dec_status os = order_on(e, e->stream)) return os;
+  const size_t n = (size_t)c.max_batch * c.n_experts;
+  DEC_CUDA(cudaMemcpyAsync(logits, e->base.rt_logits + (size_t)layer * n, sizeof(float) * n, cudaMemcpyDeviceToHost,
+                           e->stream));
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
   return DEC_OK;
 }
 
 dec_status dec_get_trace(dec_engine* e, uint64_t* host_buf, int32_t n, int32_t* n_written) {
   if (!e || !host_buf || n < 0) return DEC_ERR_ARG;
-  DEC_CUDA(cudaDeviceSynchronize());
+  if (dec_status os = order_on(e, e->stream)) return os;
   const int m = std::min(n, kTraceSlots + kBarTrace * e->grid);
-  DEC_CUDA(cudaMemcpy(host_buf, e->base.trace, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost));
+  DEC_CUDA(cudaMemcpyAsync(host_buf, e->base.trace, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost, e->stream));
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
+  if (n_written) *n_written = m;
+  return DEC_OK;
+}
+
+dec_status dec_get_layer_times(dec_engine* e, uint64_t* host_buf, int32_t n, int32_t* n_written) {
+  if (!e || !host_buf || n < 0) return DEC_ERR_ARG;
+  if (dec_status os = order_on(e, e->stream)) return os;
+  const int m = std::min(n, e->cfg.n_layers + 2);
+  DEC_CUDA(cudaMemcpyAsync(host_buf, e->base.layer_ts, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost, e->stream));
+  DEC_CUDA(cudaStreamSynchronize(e->stream));
   if (n_written) *n_written = m;
   return DEC_OK;
 }
@@ -905,8 +982,9 @@ const char* dec_last_error(const dec_engine* e) { return e ? e->err.c_str() : "n
 
 void dec_destroy(dec_engine* e) {
   if (!e) return;
-  if (e->stream) cudaStreamSynchronize(e->stream);
+  if (e->stream && e->order_ev) quiesce(e);
   for (void* p : e->allocs) cudaFree(p);
+  if (e->order_ev) cudaEventDestroy(e->order_ev);
   if (e->stream) cudaStreamDestroy(e->stream);
   delete e;
 }

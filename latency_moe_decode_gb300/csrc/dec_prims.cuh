@@ -197,39 +197,6 @@ __device__ __forceinline__ void cons_sync() {
 }
 
 
-// Wait until a published flag reaches `want` (acquire); one thread polls.
-__device__ __forceinline__ bool wait_flag(const KParams& p, const unsigned* f, unsigned want, int where) {
-  if (ld_acquire(f) == want) return true;
-  const unsigned long long t0 = gtimer();
-  for (unsigned it = 1; ld_acquire(f) != want; ++it) {
-    if ((it & 15u) == 0) {
-      if (aborted(p)) return false;
-      if (gtimer() - t0 > p.timeout_ns) {
-        raise_err(p, kDevTimeout, where);
-        return false;
-      }
-    }
-  }
-  return true;
-}
-
-// Wait until a counter that only grows reaches `target` (acquire); one thread polls.
-__device__ __forceinline__ bool wait_at_least(const KParams& p, const int* c, int target, int where) {
-  const unsigned* u = reinterpret_cast<const unsigned*>(c);
-  if ((int)ld_acquire(u) >= target) return true;
-  const unsigned long long t0 = gtimer();
-  for (unsigned it = 1; (int)ld_acquire(u) < target; ++it) {
-    if ((it & 15u) == 0) {
-      if (aborted(p)) return false;
-      if (gtimer() - t0 > p.timeout_ns) {
-        raise_err(p, kDevTimeout, where);
-        return false;
-      }
-    }
-  }
-  return true;
-}
-
 // ---------------------------------------------------------------------------------------------
 // conversions (CUDA's own FP8 conversion instruction; bf16 -> fp32 is a shift)
 

@@ -183,6 +183,21 @@ class Engine:
         self._check(self.lib.dec_get_routing(self.h, layer, idx.ctypes.data, gates.ctypes.data), "dec_get_routing")
         return idx, gates
 
+    def router_logits(self, layer: int) -> np.ndarray:
+        c = self.cfg
+        out = np.zeros((c.max_batch, c.n_experts), np.float32)
+        self._check(self.lib.dec_get_router_logits(self.h, layer, out.ctypes.data), "dec_get_router_logits")
+        return out
+
+    def layer_times(self) -> np.ndarray:
+        """Timestamps (ns) of the most recent step: input of layer l final, l = 0..n_layers, then
+        the step's end (first CTA's view)."""
+        n = self.cfg.n_layers + 2
+        buf = (C.c_uint64 * n)()
+        got = C.c_int32()
+        self._check(self.lib.dec_get_layer_times(self.h, buf, n, C.byref(got)), "dec_get_layer_times")
+        return np.array(buf[:got.value], dtype=np.uint64)
+
     def trace(self, n: int = 64) -> np.ndarray:
         buf = (C.c_uint64 * n)()
         got = C.c_int32()

@@ -1,0 +1,85 @@
+"""The failure path of the decode step, made to happen without faulting the GPU.
+
+* A wait that runs out: the engine is built with DEC_TEST_SKIP_ARRIVAL=1, so the CTA holding
+  the first q/k/v tile withholds that partial sum's arrival in layer 0 (a counter that nothing
+  completes), and with
+  DEC_TIMEOUT_MS=20 every wait of the step is bounded by 20 ms. The step must end by itself, the
+  next synchronising call must report DEC_ERR_TIMEOUT and poison the engine (later calls give
+  DEC_ERR_POISONED), and the CUDA context must stay usable: a fresh engine on the same device
+  then decodes exactly like one that never failed.
+* A device-side range check: an RMSNorm weight of 30000 makes the normalised GEMV input leave
+  the f16 range of its shared-memory staging; the kernel reports it (DEC_ERR_DEVICE) instead of
+  computing with infinities.
+"""
+import numpy as np
+import pytest
+import torch
+
+from latency_moe_decode_gb300 import capi, synth
+
+pytestmark = pytest.mark.gpu
+
+CFG = synth.ModelCfg(n_layers=2, hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, n_experts=8, top_k=2,
+                     moe_inter=128, n_shared=1, vocab=512, max_ctx=64, max_batch=2)
+DEC_ERR_TIMEOUT, DEC_ERR_POISONED, DEC_ERR_DEVICE = -4, -6, -7
+
+
+def _model(seed):
+    return synth.model_to(synth.gen_model(CFG, seed=seed, device="cpu"), "cuda")
+
+
+def _decode(eng, steps=3):
+    out = []
+    tok = torch.tensor([5, 9], dtype=torch.int32, device="cuda")
+    for _ in range(steps):
+        logits = torch.empty(2, CFG.vocab, device="cuda")
+        nxt = torch.empty(2, dtype=torch.int32, device="cuda")
+        eng.step(tokens=tok, batch=2, logits=logits, next_tokens=nxt)
+        eng.sync()
+        out.append((logits.cpu().numpy(), nxt.cpu().numpy()))
+        tok = nxt
+    return out
+
+
+def test_withheld_arrival_times_out_and_poisons(monkeypatch):
+    from latency_moe_decode_gb300.engine import Engine
+    m = _model(51)
+    monkeypatch.setenv("DEC_TEST_SKIP_ARRIVAL", "1")
+    monkeypatch.setenv("DEC_TIMEOUT_MS", "20")
+    bad = Engine(m)
+    monkeypatch.delenv("DEC_TEST_SKIP_ARRIVAL")
+    monkeypatch.delenv("DEC_TIMEOUT_MS")
+    tok = torch.tensor([5, 9], dtype=torch.int32, device="cuda")
+    bad.step(tokens=tok, batch=2)  # the launch itself succeeds; the device wait runs out
+    with pytest.raises(capi.DecError) as ei:
+        bad.sync()
+    assert ei.value.status == DEC_ERR_TIMEOUT, str(ei.value)
+    assert "timed out" in str(ei.value)
+    with pytest.raises(capi.DecError) as ei:
+        bad.step(tokens=tok, batch=2)
+    assert ei.value.status == DEC_ERR_POISONED
+    bad.close()
+    # the context is intact: two fresh engines decode, bit for bit alike
+    a, b = Engine(m), Engine(m)
+    ra, rb = _decode(a), _decode(b)
+    for (la, ta), (lb, tb) in zip(ra, rb):
+        assert np.isfinite(la).all() and np.array_equal(la, lb) and np.array_equal(ta, tb)
+    a.close()
+    b.close()
+
+
+def test_f16_staging_range_is_checked():
+    from latency_moe_decode_gb300.engine import Engine
+    m = _model(52)
+    m["layers"][0]["attn_norm"] = torch.full_like(m["layers"][0]["attn_norm"], 30000.0)
+    eng = Engine(m)
+    tok = torch.tensor([5, 9], dtype=torch.int32, device="cuda")
+    eng.step(tokens=tok, batch=2)
+    with pytest.raises(capi.DecError) as ei:
+        eng.sync()
+    assert ei.value.status == DEC_ERR_DEVICE, str(ei.value)
+    assert "f16 staging range" in str(ei.value)
+    with pytest.raises(capi.DecError) as ei:
+        eng.step(tokens=tok, batch=2)
+    assert ei.value.status == DEC_ERR_POISONED
+    eng.close()
