@@ -1,7 +1,7 @@
 """CPU oracle of the MoE decode step (ctypes binding of oracle.c).
 
 TEST INFRASTRUCTURE ONLY: imported by the test suite, by the smoke check and by the benchmark's
-CPU-baseline leg. The GPU engine never imports it. Inputs are numpy arrays (or CPU torch tensors)
+CPU-baseline and reference legs. The GPU engine never imports it. Inputs are numpy arrays (or CPU torch tensors)
 of the storage formats the decode step consumes: FP8-E4M3 codes (uint8) with fp32 block scales,
 bf16 values as uint16 bit patterns, int32 token ids. All arithmetic is in oracle.c (double).
 """
@@ -49,6 +49,8 @@ def lib():
         L.orc_full_recompute.argtypes = [C.POINTER(OrcModel), C.c_void_p, C.c_int32, C.c_void_p]
         L.orc_argmax.restype = C.c_int32
         L.orc_argmax.argtypes = [C.c_void_p, C.c_int32]
+        L.orc_set_threads.argtypes = [C.c_int32]
+        L.orc_max_threads.restype = C.c_int32
         _lib = L
     return _lib
 
@@ -197,6 +199,15 @@ class Oracle:
         logits = np.zeros(self.cfg.vocab, np.float64)
         tok = lib().orc_full_recompute(C.byref(self.model), _ptr(t), len(t), _ptr(logits))
         return tok, logits
+
+
+def set_threads(n: int) -> None:
+    """Host threads for the rows of each matrix-vector product (results do not depend on it)."""
+    lib().orc_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().orc_max_threads())
 
 
 # ---- small helpers over the building blocks (used by the pin tests) ----

@@ -1,12 +1,35 @@
 /*
  * CPU oracle for the latency-oriented MoE decode step. TEST INFRASTRUCTURE ONLY: see oracle.h.
- * Plain C, single-threaded, double arithmetic; bf16 rounding only at the stored activations.
+ * Plain C, double arithmetic; bf16 rounding only at the stored activations. The rows of a
+ * matrix-vector product may run on several host threads (OpenMP), with bit-identical results.
  */
 #include "oracle.h"
 
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Host threads for the independent rows of a matrix-vector product (1 unless the library was
+   built with OpenMP). Each row's sum runs in the same order on one thread, so every result is
+   bit-identical for any thread count. */
+void orc_set_threads(int32_t n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : 1);
+#else
+  (void)n;
+#endif
+}
+
+int32_t orc_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------------------------------ */
 /* Element codecs                                                                              */
@@ -83,6 +106,7 @@ static void e4m3_table(void) {
 void orc_gemv(const orc_mat* m, const double* x, double* y) {
   e4m3_table();
   int kb_n = (m->k + 127) / 128;
+#pragma omp parallel for schedule(static) if (m->n >= 256)
   for (int r = 0; r < m->n; ++r) {
     const uint8_t* row = m->w + (size_t)r * m->k;
     double acc = 0.0;

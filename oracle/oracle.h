@@ -1,7 +1,7 @@
 /*
  * CPU oracle for the latency-oriented MoE decode step.
  *
- * TEST INFRASTRUCTURE ONLY. This is a plain, slow, single-threaded restatement of what one
+ * TEST INFRASTRUCTURE ONLY. This is a plain, slow restatement of what one
  * decode step of a pre-norm MoE transformer computes, written so that a reader can check it
  * against its definition by eye. Only the test suite, the smoke check and the benchmark's CPU
  * baseline may call it. The GPU engine never links, loads or calls it, and the two share no
@@ -121,6 +121,11 @@ int32_t orc_decode_step(const orc_model* m, int32_t token, const uint16_t* hidde
 int32_t orc_full_recompute(const orc_model* m, const int32_t* tokens, int32_t n, double* logits);
 /* argmax with ties to the lowest index */
 int32_t orc_argmax(const double* v, int32_t n);
+
+/* Host threads for the rows of a matrix-vector product (bit-identical results for any count;
+   1 when built without OpenMP). */
+void orc_set_threads(int32_t n);
+int32_t orc_max_threads(void);
 
 #ifdef __cplusplus
 }

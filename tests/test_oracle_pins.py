@@ -350,3 +350,17 @@ def test_zero_sublayers_keep_the_residual_stream():
     o0 = oracle.Oracle(m0)
     out0 = o0.decode_step(o0.new_kv(8), 0, token=11)
     assert np.array_equal(out["logits"], out0["logits"])
+
+
+def test_oracle_threads_do_not_change_results():
+    """The matrix-vector rows may run on several host threads; every result is bit-identical."""
+    m = synth.gen_model(TINY_MOE, seed=8)
+    orc = oracle.Oracle(m)
+    outs = []
+    for threads in (1, 3):
+        oracle.set_threads(threads)
+        kv = orc.new_kv(16)
+        outs.append(orc.prefill(kv, synth.gen_tokens(5, TINY_MOE.vocab, seed=8)))
+    oracle.set_threads(oracle.max_threads())
+    assert np.array_equal(outs[0]["logits"], outs[1]["logits"])
+    assert np.array_equal(outs[0]["hidden"], outs[1]["hidden"])
