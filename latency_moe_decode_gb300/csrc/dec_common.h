@@ -20,7 +20,7 @@ constexpr int kSlotTiles = 2;
 constexpr int kSlotBytes = kSlotTiles * kTileBytes;  // 32800
 constexpr int kSlotsInFlight = 2;                     // copies a CTA keeps in flight (at most)
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + the producer warp and the MMA warp
 constexpr int kKvTilePos = 64;                       // KV positions per ring slot
 constexpr int kMaxBatch = 8;
 constexpr int kMaxHidden = 4096;                     // hidden sizes the kernel handles
@@ -40,7 +40,7 @@ enum : int {
   kDevOk = 0,
   kDevTimeout = 1,
   kDevBadArg = 2,
-  kDevRange = 3,  // an activation outside the f16 range of the GEMV input staging
+  kDevRange = 3,  // an activation outside the f16 range of the CUDA-core GEMV input staging
 };
 
 struct LayerDev {

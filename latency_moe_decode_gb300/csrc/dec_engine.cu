@@ -37,9 +37,11 @@ __global__ void repack_kernel(const RepackDesc d, uint8_t* dst) {
   const int rb = tile / kbn, kb = tile % kbn;
   uint8_t* out = dst + (size_t)tile * kTileBytes;
   for (int q = threadIdx.x; q < kTileData / 16; q += blockDim.x) {
-    // consumer order: 16-byte chunk c of tile row 32r + l sits at unit (4c + r) * 32 + l
-    const int l = q & 31, r = (q >> 5) & 3, c = q >> 7;
-    const int row = r * 32 + l;  // row inside the tile
+    // the tensor cores' canonical K-major layout without swizzling: 16-byte chunk c of tile row
+    // 8g + r sits at unit (8g + c) * 8 + r (core matrices of 8 rows x 16 bytes, 128 bytes apart
+    // along K, 1024 bytes apart along the rows)
+    const int r = q & 7, c = (q >> 3) & 7, g8 = q >> 6;
+    const int row = g8 * 8 + r;  // row inside the tile
     const int h = rb * 2 + row / 64;
     int src = -1, srow = 0;
     if (d.interleave) {
@@ -651,6 +653,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
       }
     }
     xmax = std::max(xmax, span * p.inter);
+    if (xmax > kMaxKb * kTileK) return bail(fail(e, DEC_ERR_UNSUPPORTED, "a stage input wider than the B operand table"));
     p.xmax = xmax;
   }
 

@@ -17,10 +17,12 @@
 //               ahead across stage boundaries (the fix named on the vLLM page, section "Agent-
 //               written kernels face evidence gates": only static weights are loaded ahead of a
 //               synchronisation wait).
-//   warps 0..7  consumers: dequantise E4M3 tiles (CUDA's cvt), multiply by the bf16 activations
-//               held in shared memory, accumulate in fp32, reduce across warps, and publish
-//               split-K partial sums with a releasing counter arrival (no CTA ever waits for
-//               the result of its own arrival).
+//   warps 0..7  consumers: hand each weight tile to the tensor cores (thread 0 issues
+//               tcgen05.mma on the raw E4M3 tile and the activations split into E4M3 pieces,
+//               accumulating in TMEM), add the tiles' products into fp32 registers with their
+//               block scales, and publish split-K partial sums with a releasing counter arrival
+//               (no CTA ever waits for the result of its own arrival); attention runs on the
+//               CUDA cores.
 // Cross-CTA data flow of a layer: the q/k/v, output-projection and router partials are read
 // directly by every CTA that needs them (attention units, the x_mid norm, the routing, which
 // every CTA computes itself); the attention chunks of a (sequence, KV head) are merged in slices
@@ -43,6 +45,28 @@ struct SmemLayout {
 };
 
 constexpr int kMaxExperts = 128;
+// Tensor-core tiles: kNB TMEM accumulators of kMmaN fp32 columns each, so the MMA warp can run
+// kNB tiles ahead of the epilogue; activation k blocks per stage at most kMaxKb.
+constexpr int kNB = 4;
+constexpr int kMmaN = 16;
+constexpr int kTmemCols = kNB * kMmaN;  // a power of two >= 32
+constexpr int kMaxKb = 64;
+
+// Layout of the B operand (a stage's activations as E4M3 pieces, the canonical K-major layout
+// of 8-row x 16-byte core matrices) for a step of B tokens: each k block of 128 activations
+// takes rpad rows (2B: rows 2b, 2b + 1 are token b's two pieces; 3 tokens pad to 8, 5..8 to 16),
+// and pk consecutive k blocks share one block of nrb rows (8, or 16 for B > 4), whose MMA (N = 16)
+// yields their columns side by side. With nrb = 8 the second 8-row group of N aliases the first.
+struct BGeo {
+  int rpad, pk, nrb;
+};
+__host__ __device__ inline BGeo bgeo(int B) {
+  BGeo g;
+  g.rpad = B <= 1 ? 2 : B <= 2 ? 4 : B <= 4 ? 8 : 16;
+  g.nrb = g.rpad <= 8 ? 8 : 16;
+  g.pk = g.rpad <= 8 ? 8 / g.rpad : 1;
+  return g;
+}
 constexpr int kProducerTrace = 128;  // trace words reserved for CTA 0's producer
 
 constexpr int kWaitMax = 128;  // conditions one CTA-wide wait table holds
@@ -65,6 +89,14 @@ struct Misc {
   float gate[kMaxBatch][kMaxExperts + 1];
   float rsum[kConsumerWarps][kMaxBatch];
   int tok[kMaxBatch];
+  // tensor-core tiles: the scale exponent a of each token's staged k block (its pieces encode
+  // x * 2^a), the consumers -> MMA warp "stage operand ready" barrier (one phase per GEMV stage),
+  // the MMA warp's "done" barrier, per TMEM accumulator a "product ready" (MMA commit) and a
+  // "product read" (one arrival per consumer warp) barrier, and the TMEM base address
+  int8_t xexp[kMaxBatch][kMaxKb];
+  uint64_t b_ready, mma_done;
+  uint64_t tfull[kNB], tempty[kNB];
+  uint32_t tmem_base;
 };
 
 struct WaitCond {
@@ -80,7 +112,14 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   s.full_off = align_up(ring * kSlotBytes, 128);
   s.empty_off = s.full_off + ring * 8;
   s.xs_off = align_up(s.empty_off + ring * 8, 128);
-  s.red_off = align_up(s.xs_off + bm * xmax * 2, 128);
+  // the stage's activations as tensor-core B operand blocks, for any step batch up to bm
+  int xs_bytes = 0;
+  for (int b = 1; b <= bm; ++b) {
+    const BGeo g = bgeo(b);
+    const int bytes = (xmax / 128 + g.pk - 1) / g.pk * g.nrb * 128;
+    xs_bytes = bytes > xs_bytes ? bytes : xs_bytes;
+  }
+  s.red_off = align_up(s.xs_off + xs_bytes, 128);
   int red_gemv = 2 * kTileRows * bm * 4;
   int red_attn = kConsumerWarps * group * (hd + 2) * 4;
   int red_fin = (bm * kTileRows + kListCap + 16) * 4;
@@ -222,6 +261,43 @@ struct TileCursor {
       if (rb < p.n_rb_d) addr = expert_base(p, Ld, kind, u, U, elist) + (size_t)rb * g.tpe * kTileBytes;
     }
   }
+};
+
+// Position of a GEMV stage's tile, advanced without divisions (consumers and the MMA warp walk
+// the same sequence): segment, k block within it, and for the down projection the expert slot v,
+// the k block kx within the expert's run and the run's place xj among the staged SwiGLU rows.
+struct TilePos {
+  int seg, kb, kx, v, rv, xj;
+  __device__ void init(const KParams& p, const StageGeo& g, int kind, int t0, int t1) {
+    seg = kb = kx = v = rv = xj = 0;
+    if (t1 <= t0) return;
+    seg = t0 / g.kbs;
+    kb = t0 - seg * g.kbs;
+    kx = kb;
+    if (kind == K_D) {
+      v = g.rbm ? kb / g.tpe : t0 / g.tpe;          // expert slot of the first tile
+      rv = g.rbm ? kb - v * g.tpe : t0 - v * g.tpe;  // its place in that expert's run
+      kx = rv % p.kb_i;                              // and in its k-block sweep
+    }
+  }
+  __device__ __forceinline__ void next(const KParams& p, const StageGeo& g, int kind, int nv) {
+    if (++kb == g.kbs) {
+      kb = 0;
+      ++seg;
+    }
+    if (kind != K_D) {
+      kx = kb;
+    } else {
+      if (++kx == p.kb_i) kx = 0;
+      if (++rv == g.tpe) {
+        rv = 0;
+        if (++v == nv) v = 0;
+        if (++xj == nv) xj = 0;
+      }
+    }
+  }
+  // k block of the staged activations the tile multiplies
+  __device__ __forceinline__ int kbi(const KParams& p, int kind) const { return kind == K_D ? xj * p.kb_i + kx : kx; }
 };
 
 // attention work units: (sequence b, KV head g, context chunk c)
@@ -486,7 +562,16 @@ struct Consumer {
   bool dead = false;
   int warp, lane, tid;
   int stamp = 0;
-  bool range_bad = false;  // an activation staged as f16 was outside its range
+  // Tile arithmetic: the tensor cores for steps of two or more tokens; at one token the CUDA
+  // cores (a tensor-core MMA of M = 128 costs a fixed ~50 ns per K = 32 slice for any N <= 128,
+  // so a 128 x 128 tile takes ~200 ns there, more than the ~160 ns of the CUDA-core product).
+  static constexpr bool kTC = BM >= 2;
+  bool range_bad = false;  // (CUDA-core path) an activation staged as f16 was outside its range
+  // tensor-core tiles: tiles whose products were added so far in this step (the sequence picks
+  // the TMEM accumulator and its barriers' phases), the TMEM base, the B operand layout
+  unsigned tseq = 0;
+  uint32_t tmem = 0;
+  BGeo bg;
 
   __device__ Consumer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint16_t* x, float* rd,
                       Misc* m_)
@@ -494,6 +579,7 @@ struct Consumer {
     tid = threadIdx.x;
     warp = tid >> 5;
     lane = tid & 31;
+    bg = bgeo(p.B);
   }
 
   // CTA 0 records (event code, %globaltimer) pairs: code = what << 4 | event, where `what` is a
@@ -653,7 +739,8 @@ struct Consumer {
             ss = fmaf(a, a, ss);
             ss = fmaf(c, c, ss);
           }
-          *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) = v[j];
+          if constexpr (kTC) park(b, k, v[j]);
+          else *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) = v[j];
         }
       }
 #pragma unroll
@@ -670,30 +757,37 @@ struct Consumer {
 #pragma unroll
       for (int j = 0; j < MAXV; ++j) {
         const int k = (tid + j * kConsumerWarps * 32) * 8;
-        if (k >= p.d) break;
-        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)b * p.xmax + k);
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(&xv);
-        const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv[j]);
-        uint4 o;
-        uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
+        const bool in = k < p.d;  // (whole half-warps: d is a multiple of 128)
+        float f[8];
+        if (in) {
+          const uint4 xv = kTC ? unpark(b, k) : *reinterpret_cast<const uint4*>(xs + (size_t)b * p.xmax + k);
+          const uint32_t* u = reinterpret_cast<const uint32_t*>(&xv);
+          const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv[j]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = bf16f(f2bf((bf16lo(u[q]) * inv) * bf16lo(wu[q])));
-          const float hi = bf16f(f2bf((bf16hi(u[q]) * inv) * bf16hi(wu[q])));
-          ou[q] = pack_f16x2(lo, hi);
+          for (int q = 0; q < 4; ++q) {
+            f[2 * q] = bf16f(f2bf((bf16lo(u[q]) * inv) * bf16lo(wu[q])));
+            f[2 * q + 1] = bf16f(f2bf((bf16hi(u[q]) * inv) * bf16hi(wu[q])));
+          }
         }
-        *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) = o;
+        if constexpr (kTC) {
+          pieces(b, k, f, in);
+        } else if (in) {
+          *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + k) =
+              make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]), pack_f16x2(f[6], f[7]));
+        }
       }
     }
-    range_check();
+    if constexpr (kTC) fence_proxy_async_smem();
+    else range_check();
     cons_sync();
   }
 
-  // The GEMV input is staged in shared memory as f16: every bf16 value with magnitude in
-  // [2^-17, 65504] converts exactly (8 significant bits fit in f16's 11); smaller ones round with
-  // an absolute error below 2^-25, far under the fp32 accumulation error of the sums they feed.
-  // A value beyond the f16 range would become infinite, so it is reported as a device error.
-  // (The range test only sets a per-thread flag; range_check() reports it once per staging.)
+  // (CUDA-core path) The GEMV input is staged in shared memory as f16: every bf16 value with
+  // magnitude in [2^-17, 65504] converts exactly (8 significant bits fit in f16's 11); smaller
+  // ones round with an absolute error below 2^-25, far under the fp32 accumulation error of the
+  // sums they feed. A value beyond the f16 range would become infinite, so it is reported as a
+  // device error. (The range test only sets a per-thread flag; range_check() reports it once per
+  // staging.)
   __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     range_bad |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -706,45 +800,121 @@ struct Consumer {
     }
   }
 
-  // xs[b][dst_off + 0..n) = f16(src[b][0..n)) for a bf16 activation written by other CTAs; two
-  // 8-element chunks per thread and pass, both loads in flight before either is stored
+  // ---- the tensor cores' B operand (the stage's activations as E4M3 pieces)
+
+  // byte of activation k (of the stage's input) of token b, piece r, in the B operand layout
+  __device__ __forceinline__ uint8_t* bpos(int b, int k, int r) const {
+    const int kb = k >> 7, c = k & 127;
+    const int row = (kb % bg.pk) * bg.rpad + 2 * b + r;
+    return reinterpret_cast<uint8_t*>(xs) + (size_t)(kb / bg.pk) * bg.nrb * 128 + (row >> 3) * 1024 + (c >> 4) * 128 +
+           (row & 7) * 16 + (c & 15);
+  }
+  // Park 8 bf16 activations k .. k + 7 of token b where their pieces will go: low bytes at piece
+  // 0's place, high bytes at piece 1's (so converting them later in place touches no other
+  // thread's data); unpark reads them back.
+  __device__ __forceinline__ void park(int b, int k, const uint4 v) {
+    *reinterpret_cast<uint2*>(bpos(b, k, 0)) = make_uint2(__byte_perm(v.x, v.y, 0x6420), __byte_perm(v.z, v.w, 0x6420));
+    *reinterpret_cast<uint2*>(bpos(b, k, 1)) = make_uint2(__byte_perm(v.x, v.y, 0x7531), __byte_perm(v.z, v.w, 0x7531));
+  }
+  __device__ __forceinline__ uint4 unpark(int b, int k) const {
+    const uint2 lo = *reinterpret_cast<const uint2*>(bpos(b, k, 0));
+    const uint2 hi = *reinterpret_cast<const uint2*>(bpos(b, k, 1));
+    return make_uint4(__byte_perm(lo.x, hi.x, 0x5140), __byte_perm(lo.x, hi.x, 0x7362), __byte_perm(lo.y, hi.y, 0x5140),
+                      __byte_perm(lo.y, hi.y, 0x7362));
+  }
+  // Activations k .. k + 7 of token b (bf16 values in f) as two E4M3 pieces each: with 2^a
+  // putting the largest |x| of their k block (the 16 chunks of a half-warp) in [128, 256),
+  // x * 2^a = p1 + p2 / 16, p1 = E4M3(x * 2^a), p2 = E4M3(16 (x * 2^a - p1)); exact for
+  // |x| >= 2^-13 max|x| (the residual has at most 4 significant bits), an error below
+  // 2^-21 max|x| under it. Called by whole warps (the maximum is a half-warp shuffle).
+  __device__ __forceinline__ void pieces(int b, int k, const float (&f)[8], bool in) {
+    float mx = 0.f;
+    if (in)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (!in) return;
+    const int e = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 7;
+    const int a = max(-120, min(120, 7 - e));
+    const float sa = __int_as_float((127 + a) << 23);
+    uint32_t w1[2], w2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float x0 = f[4 * i] * sa, x1 = f[4 * i + 1] * sa, x2 = f[4 * i + 2] * sa, x3 = f[4 * i + 3] * sa;
+      const uint16_t q01 = float2_to_e4m3x2(x0, x1), q23 = float2_to_e4m3x2(x2, x3);
+      const float2 g01 = e4m3x2_to_float2(q01), g23 = e4m3x2_to_float2(q23);
+      const uint16_t r01 = float2_to_e4m3x2((x0 - g01.x) * 16.f, (x1 - g01.y) * 16.f);
+      const uint16_t r23 = float2_to_e4m3x2((x2 - g23.x) * 16.f, (x3 - g23.y) * 16.f);
+      w1[i] = (uint32_t)q01 | ((uint32_t)q23 << 16);
+      w2[i] = (uint32_t)r01 | ((uint32_t)r23 << 16);
+    }
+    *reinterpret_cast<uint2*>(bpos(b, k, 0)) = make_uint2(w1[0], w1[1]);
+    *reinterpret_cast<uint2*>(bpos(b, k, 1)) = make_uint2(w2[0], w2[1]);
+    if ((lane & 15) == 0) m->xexp[b][k >> 7] = (int8_t)a;
+  }
+
+  // Stage activations dst_off .. dst_off + n of the stage's input (as B operand pieces) from a
+  // bf16 activation src[b][0..n) written by other CTAs; two 8-element chunks per thread and
+  // pass, both loads in flight before either is converted. n and dst_off are multiples of 128.
   __device__ void stage_copy(const uint16_t* src, int n, size_t src_stride, int dst_off) {
     constexpr int P = kConsumerWarps * 32 * 8;
 #pragma unroll 1
-    for (int b = 0; b < min(p.B, BM); ++b)
+    for (int b = 0; b < min(p.B, BM); ++b) {
 #pragma unroll 1
-      for (int k0 = tid * 8; k0 < n; k0 += 2 * P) {
+      for (int k0 = (tid & ~31) * 8; k0 < n; k0 += 2 * P) {  // (whole warps take part)
+        const int k = k0 + lane * 8;
         uint4 v[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-          if (k0 + j * P < n) v[j] = ldcg4(src + (size_t)b * src_stride + k0 + j * P);
+          if (k + j * P < n) v[j] = ldcg4(src + (size_t)b * src_stride + k + j * P);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          if (k0 + j * P >= n) break;
-          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[j]);
-          uint4 o;
-          uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
+          const bool in = k + j * P < n;
+          float f[8];
+          if (in) {
+            const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[j]);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) ou[q] = pack_f16x2(bf16lo(u[q]), bf16hi(u[q]));
-          *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k0 + j * P) = o;
+            for (int q = 0; q < 4; ++q) {
+              f[2 * q] = bf16lo(u[q]);
+              f[2 * q + 1] = bf16hi(u[q]);
+            }
+          }
+          if constexpr (kTC) {
+            pieces(b, dst_off + k + j * P, f, in);
+          } else if (in) {
+            *reinterpret_cast<uint4*>(xs + (size_t)b * p.xmax + dst_off + k + j * P) =
+                make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                           pack_f16x2(f[6], f[7]));
+          }
         }
       }
-    range_check();
+    }
+    if constexpr (kTC) fence_proxy_async_smem();
+    else range_check();
   }
 
-  // -------- split-K GEMV over one stage --------
+  // -------- split-K GEMV over one stage, on the tensor cores --------
 
-  // All eight consumer warps share each 128x128 tile, so a slot is held for an eighth of the
-  // time one warp would need and most of the ring stays in flight. Warp w takes rows
-  // 32 * (w & 3) + lane (lane = its row) and the column chunks 4 * (w >> 2) .. + 3 (the repacked
-  // tile stores the 16-byte chunk c of row 32r + l at 16 * ((4c + r) * 32 + l): each load of a
-  // warp reads 512 contiguous bytes, conflict-free). The activation chunk is the same for all
-  // lanes (a broadcast load). E4M3 pairs become f16 pairs exactly (CUDA's cvt); each product is
-  // then formed and accumulated in fp32 by one mixed-precision FMA (f16 x f16 + f32, one
-  // rounding, as converting both operands to fp32 first would give). The tile's block scale
-  // (rows 0..63 / 64..127) multiplies the tile sum.
-  __device__ __forceinline__ void tile_dot(const uint8_t* tile, int xoff, const float* gmul, float (&acc)[BM]) {
-    const int r = warp & 3, c0 = (warp >> 2) * 4;
+  // A tile (128 weight rows x 128 E4M3 columns, repacked in the canonical K-major layout: 8-row x
+  // 16-byte core matrices, 128 bytes apart along K and 1024 apart along the rows) is multiplied
+  // straight from its ring slot by tcgen05.mma kind::f8f6f4 (issued by the MMA warp): A = the raw
+  // E4M3 codes, B = the stage's bf16 activations split exactly into two E4M3 pieces per value
+  // (see pieces()), D = 128 rows x 16 fp32 columns in one of kNB TMEM accumulators. Products of
+  // 8-bit values are exact and the sums are fp32. The consumer warps add each tile's product
+  // into fp32 registers, applying the pieces' scales, the tile's block scale and the expert gate
+  // (a k block per tile, so the block scale cannot stay in TMEM). The tensor cores replace the
+  // E4M3 conversions that bound a CUDA-core dot product.
+
+  // (CUDA-core path, one token) All eight consumer warps share each tile: warp w takes row
+  // R = 32 (w & 3) + lane and the 16-byte column chunks 4 (w >> 2) .. + 3 (chunk c of row R sits
+  // at 16 ((R / 8 * 8 + c) * 8 + R % 8) in the tensor cores' layout: each load of a warp reads
+  // four 128-byte runs, no bank conflict beyond the 512 bytes' minimum). E4M3 pairs become f16
+  // pairs exactly (CUDA's cvt); each product is formed and accumulated in fp32 by one mixed-
+  // precision FMA (f16 x f16 + f32, one rounding). The block scale of the row's half multiplies
+  // the tile sum. The activation chunk is the same for all lanes (a broadcast load).
+  __device__ __forceinline__ void tile_dot(const uint8_t* tile, int xoff, const float* gmul, float (&acc)[4]) {
+    const int r = warp & 3, c0 = (warp >> 2) * 4, R = 32 * r + lane;
     const float2 sc = *reinterpret_cast<const float2*>(tile + kTileData);
     const float s_r = r < 2 ? sc.x : sc.y;
     float part[BM][2];  // two FMA chains per token
@@ -752,7 +922,8 @@ struct Consumer {
     for (int b = 0; b < BM; ++b) part[b][0] = part[b][1] = 0.f;
     uint4 wv[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(tile + ((((c0 + c) * 4 + r) * 32 + lane) << 4));
+    for (int c = 0; c < 4; ++c)
+      wv[c] = *reinterpret_cast<const uint4*>(tile + ((((R >> 3) * 8 + c0 + c) * 8 + (R & 7)) << 4));
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t* u = reinterpret_cast<const uint32_t*>(&wv[c]);
@@ -775,7 +946,40 @@ struct Consumer {
       }
     }
 #pragma unroll
-    for (int b = 0; b < BM; ++b) acc[b] = fmaf(s_r * gmul[b], part[b][0] + part[b][1], acc[b]);
+    for (int b = 0; b < BM && b < 4; ++b) acc[b] = fmaf(s_r * gmul[b], part[b][0] + part[b][1], acc[b]);
+  }
+
+  // Add tile seq's product into the thread's accumulators: thread (warp w, lane) holds row
+  // 32 (w & 3) + lane of tokens 4 (w >> 2) .. 4 (w >> 2) + 3 (TMEM lane quadrant w & 3; token b's
+  // pieces are columns cb + 2b, cb + 2b + 1 for k block kbi, cb = (kbi mod pk) rpad); `tile` = the
+  // tile in its slot (block scales in its header), gate multipliers gm. Every consumer warp then
+  // hands the accumulator back to the MMA warp.
+  __device__ void epilogue(unsigned seq, const uint8_t* tile, const float* gm, int kbi, float (&acc)[4]) {
+    const int buf = seq % kNB;
+    if (!dead && !mbar_wait(&m->tfull[buf], (seq / kNB) & 1, p, 25)) dead = true;
+    const int q = warp & 3, h = warp >> 2;
+    if (!dead && 4 * h < p.B) {  // (warp-uniform)
+      tc_fence_after();
+      const int row = 32 * q + lane;
+      const float2 sc = *reinterpret_cast<const float2*>(tile + kTileData);
+      const float s_r = row < 64 ? sc.x : sc.y;
+      const int cb = (kbi % bg.pk) * bg.rpad + 8 * h;
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + buf * kMmaN + cb;
+      float d[8];
+      constexpr int NC = BM >= 4 ? 8 : 2 * BM;
+      tmem_ld<NC>(ta, d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int b = 4 * h + i;
+        if (b < p.B && 2 * i < NC) {
+          const float inv = __int_as_float((127 - (int)m->xexp[b][kbi]) << 23);  // 2^-a
+          acc[i] = fmaf(s_r * gm[b] * inv, fmaf(d[2 * i + 1], 0.0625f, d[2 * i]), acc[i]);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&m->tempty[buf]);
   }
 
   __device__ float* part_base(int kind) const {
@@ -814,10 +1018,18 @@ struct Consumer {
     return kind == K_D ? p.n_rb_d : g.T / g.kbs;  // down projections: the output row blocks
   }
 
-  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, int ntiles, float (&acc)[BM]) {
-    // red[column half][row][b]: warp w holds row 32 * (w & 3) + lane of column half w >> 2
+  __device__ void flush(int kind, int l, const StageGeo& g, int seg, int first_tile, int ntiles, float (&acc)[4]) {
+    const int row_t = 32 * (warp & 3) + lane, h = warp >> 2;
+    if constexpr (kTC) {
+      // red[row][b]: thread (warp w, lane) holds row 32 (w & 3) + lane of tokens 4 (w >> 2) + i
 #pragma unroll
-    for (int b = 0; b < BM; ++b) red[((size_t)(warp >> 2) * kTileRows + (warp & 3) * 32 + lane) * BM + b] = acc[b];
+      for (int i = 0; i < 4; ++i)
+        if (4 * h + i < BM) red[(size_t)row_t * BM + 4 * h + i] = acc[i];
+    } else {
+      // red[column half][row][b]: the two column halves of a row are summed below
+#pragma unroll
+      for (int b = 0; b < BM && b < 4; ++b) red[((size_t)h * kTileRows + row_t) * BM + b] = acc[b];
+    }
     cons_sync();
     const int a = seg * g.kbs;
     const int slot = contrib_slot(blockIdx.x, first_tile, a, g.T, gridDim.x);
@@ -825,7 +1037,8 @@ struct Consumer {
     #pragma unroll 1
     for (int idx = tid; idx < p.B * kTileRows; idx += kConsumerWarps * 32) {
       const int b = idx / kTileRows, row = idx % kTileRows;
-      dst[(size_t)b * kTileRows + row] = red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
+      dst[(size_t)b * kTileRows + row] = kTC ? red[(size_t)row * BM + b]
+                                             : red[(size_t)row * BM + b] + red[((size_t)kTileRows + row) * BM + b];
     }
     // The CTA barrier orders every thread's partial before the publishing thread's releasing
     // arrival; no other thread waits for the arrival to complete. An arrival adds the number of
@@ -893,35 +1106,27 @@ struct Consumer {
     const StageGeo g = stage_geo(p, kind, U);
     const int G_ = gridDim.x;
     const int t0 = range_lo(g.T, blockIdx.x, G_), t1 = range_lo(g.T, blockIdx.x + 1, G_);
-    cons_sync();
+    cons_sync();  // the stage's activations are staged (and fenced for the tensor cores)
+    if (kTC && tid == 0) mbar_arrive(&m->b_ready);
     trace(kind << 4);
     float gmul[BM];
-    float acc[BM];
+    float acc[4];
     int seg_cur = -1, seg_first = 0;
-    const uint8_t* slot_base = ring;
-    // position of tile t, advanced without divisions: segment, k block within it, and for the
+    // Position of tile t, advanced without divisions: segment, k block within it, and for the
     // down projection the expert slot v (whose gates scale the tile), the k block kx within its
-    // run and the expert's place xj among the SwiGLU rows staged in xs (the CTA's runs in order,
-    // the first at 0, wrapping after nv)
-    int seg = t1 > t0 ? t0 / g.kbs : 0, kb = t0 - seg * g.kbs;
-    int v = 0, kx = kb, rv = 0, xj = 0, xbase = 0;
+    // run and the expert's place xj among the SwiGLU rows staged (the CTA's runs in order, the
+    // first at 0, wrapping after nv). The MMA warp walks the same positions.
     const int nv = kind == K_D ? U + p.nsh : 1;
-#pragma unroll
-    for (int b = 0; b < BM; ++b) gmul[b] = 1.f;
-    if (kind == K_D && t1 > t0) {
-      v = g.rbm ? kb / g.tpe : t0 / g.tpe;       // expert slot of the first tile
-      rv = g.rbm ? kb - v * g.tpe : t0 - v * g.tpe;  // its place in that expert's run
-      kx = rv % p.kb_i;                          // and in its k-block sweep
-#pragma unroll
-      for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
-    }
+    TilePos pe;
+    pe.init(p, g, kind, t0, t1);
     int j = 0;  // tile j of the current slot (the producer packs kSlotTiles consecutive tiles per slot)
+    const uint8_t* slot_base = ring;
     for (int t = t0;; ++t) {
       // a segment ends at a segment boundary or at the end of the range (one flush call site)
-      if (t == t1 || seg != seg_cur) {
+      if (t == t1 || pe.seg != seg_cur) {
         if (t == t1) {
-          // one verdict for the whole CTA: a thread may have given up on a ring slot that
-          // another thread saw land, and the finalisers below branch on it around barriers
+          // one verdict for the whole CTA: a thread may have given up on a wait that another
+          // thread saw end, and the finalisers below branch on it around barriers
           dead = cons_any(dead);
           trace(kind << 4 | 1);
           if (kind == K_QKV) cta_stamp(l, S_QKV_TILES);
@@ -931,34 +1136,24 @@ struct Consumer {
         }
         if (seg_cur >= 0) flush(kind, l, g, seg_cur, seg_first, t - seg_first, acc);
         if (t == t1) break;
-        seg_cur = seg;
+        seg_cur = pe.seg;
         seg_first = t;
 #pragma unroll
-        for (int b = 0; b < BM; ++b) acc[b] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[i] = 0.f;
       }
-      if (j == 0) slot_base = wait_item();
-      if (!dead) tile_dot(slot_base + (size_t)j * kTileBytes, xbase + kx * kTileK, gmul, acc);
+#pragma unroll
+      for (int b = 0; b < BM; ++b) gmul[b] = kind == K_D ? m->gate[b][min(pe.v, kMaxExperts)] : 1.f;
+      if constexpr (kTC) {
+        epilogue(tseq++, ring + (size_t)rslot * kSlotBytes + (size_t)j * kTileBytes, gmul, pe.kbi(p, kind), acc);
+      } else {
+        if (j == 0) slot_base = wait_item();
+        if (!dead) tile_dot(slot_base + (size_t)j * kTileBytes, pe.kbi(p, kind) * kTileK, gmul, acc);
+      }
       if (++j == kSlotTiles || t == t1 - 1) {
         release_item();
         j = 0;
       }
-      if (++kb == g.kbs) {
-        kb = 0;
-        ++seg;
-      }
-      if (kind != K_D) {
-        kx = kb;
-      } else {
-        if (++kx == p.kb_i) kx = 0;
-        if (++rv == g.tpe) {
-          rv = 0;
-          if (++v == nv) v = 0;
-          if (++xj == nv) xj = 0;
-          xbase = xj * p.inter;
-#pragma unroll
-          for (int b = 0; b < BM; ++b) gmul[b] = m->gate[b][min(v, kMaxExperts)];
-        }
-      }
+      pe.next(p, g, kind, nv);
     }
     // Finalise the output groups this CTA is designated for (groups spread evenly over the
     // CTAs, so no CTA finalises two while others finalise none): wait (acquire) until every
@@ -1725,6 +1920,14 @@ struct Consumer {
   __device__ void run() {
     trace(10 << 4);
     if (blockIdx.x == 0 && tid == 0) p.layer_ts[0] = gtimer();
+    // the TMEM accumulators of the tensor-core tiles (warp 0 allocates and frees them)
+    if constexpr (kTC) {
+      if (warp == 0) tmem_alloc(&m->tmem_base, kTmemCols);
+      tc_fence_before();
+      cons_sync();
+      tc_fence_after();
+      tmem = m->tmem_base;
+    }
     int U = 0;
 #pragma unroll 1
     for (int l = 0; l <= p.L; ++l) {
@@ -1843,6 +2046,132 @@ struct Consumer {
     }
     trace(10 << 4 | 1);
     if (blockIdx.x == 0 && tid == 0) p.layer_ts[p.L + 1] = gtimer();
+    // Free TMEM once the MMA warp has finished (it waits for its last MMAs before saying so);
+    // the wait is bounded whatever the status word says.
+    if (kTC && warp == 0) {
+      if (lane == 0) {
+        const unsigned long long t0 = gtimer();
+        while (!mbar_try_wait(&m->mma_done, 0) && gtimer() - t0 < p.timeout_ns) {
+        }
+      }
+      __syncwarp();
+      tc_fence_after();
+      tmem_free(tmem, kTmemCols);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------------------------
+// MMA warp: one thread walks the CTA's GEMV tiles in the consumers' order and hands each to the
+// tensor cores once its ring slot has landed, its stage's activations are staged and a TMEM
+// accumulator is free, up to kNB tiles ahead of the consumers.
+
+template <int BM, int HD, int G>
+struct MmaIssuer {
+  const KParams& p;
+  uint8_t* ring;
+  uint64_t* full;
+  Misc* m;
+  const uint8_t* xsb;  // the B operand region
+  int slot = 0;        // ring slot of the next item (items: GEMV slots and the attention's KV tiles)
+  unsigned lap = 0;
+  unsigned tseq = 0, stage = 0;
+  bool dead = false;
+  uint32_t tmem = 0;
+  BGeo bg;
+
+  __device__ MmaIssuer(const KParams& p_, uint8_t* r, uint64_t* f, Misc* m_, const uint8_t* x)
+      : p(p_), ring(r), full(f), m(m_), xsb(x) {
+    bg = bgeo(p.B);
+  }
+
+  __device__ __forceinline__ void skip(int n) {
+    for (int i = 0; i < n; ++i)
+      if (++slot == p.ring) {
+        slot = 0;
+        ++lap;
+      }
+  }
+
+  __device__ void gemv(int kind, int U) {
+    if (!dead && !mbar_wait(&m->b_ready, stage & 1, p, 26)) dead = true;
+    ++stage;
+    tc_fence_after();
+    tmem = m->tmem_base;
+    const StageGeo g = stage_geo(p, kind, U);
+    const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
+    const int nv = kind == K_D ? U + p.nsh : 1;
+    TilePos pos;
+    pos.init(p, g, kind, t0, t1);
+    constexpr uint32_t idesc = idesc_e4m3_f32(kTileRows, kMmaN);
+    const uint32_t sbo = bg.nrb == 16 ? 1024u : 0u;  // 8-row blocks: the second row group aliases the first
+    int j = 0;
+#pragma unroll 1
+    for (int t = t0; t < t1; ++t) {
+      if (!dead) {
+        const int buf = tseq % kNB;
+        if (j == 0 && !mbar_wait(&full[slot], lap & 1, p, 27)) dead = true;
+        if (!dead && tseq >= (unsigned)kNB && !mbar_wait(&m->tempty[buf], (tseq / kNB - 1) & 1, p, 28)) dead = true;
+        if (!dead) {
+          tc_fence_after();
+          const int kbi = pos.kbi(p, kind);
+          const uint8_t* a = ring + (size_t)slot * kSlotBytes + (size_t)j * kTileBytes;
+          const uint8_t* b = xsb + (size_t)(kbi / bg.pk) * bg.nrb * 128;
+          const uint64_t ad = smem_desc(a, 128, 1024), bd = smem_desc(b, 128, sbo);
+          const uint32_t d = tmem + buf * kMmaN;
+#pragma unroll
+          for (int k = 0; k < kTileK / 32; ++k)  // 32 bytes of K per MMA: two core matrices (256 B)
+            mma_e4m3(d, ad + (uint64_t)(k * 16), bd + (uint64_t)(k * 16), idesc, k > 0 ? 1u : 0u);
+          mma_commit(&m->tfull[buf]);
+        }
+      }
+      ++tseq;
+      pos.next(p, g, kind, nv);
+      if (++j == kSlotTiles || t == t1 - 1) {
+        j = 0;
+        skip(1);
+      }
+    }
+  }
+
+  // the same stage sequence as the consumers (and the producer): per layer q/k/v, attention (its
+  // KV tiles pass through the ring), output projection, router or dense FFN, routing, shared
+  // expert, routed gate/up, down projections; then the LM head
+  __device__ void run() {
+#pragma unroll 1
+    for (int l = 0; l <= p.L; ++l) {
+      if (l == p.L) {
+        if (p.V > 0) gemv(K_LM, 0);
+        break;
+      }
+      gemv(K_QKV, 0);
+      int items = 0;
+      for (int u = blockIdx.x; u < p.B * p.hkv * p.nch; u += gridDim.x) {
+        const AttnUnit a = attn_unit(p, m, u);
+        items += a.tile1 - a.tile0;
+      }
+      skip(items);
+      gemv(K_O, 0);
+      int U = 0;
+      if (p.dense) {
+        gemv(K_SHGU, 0);
+      } else {
+        gemv(K_ROUTER, 0);
+        if (!dead && !mbar_wait(&m->rt_bar, (unsigned)l & 1u, p, 29)) dead = true;
+        U = min(max(m->U, 0), p.umax);
+        if (p.nsh) gemv(K_SHGU, 0);
+        gemv(K_RTGU, U);
+      }
+      gemv(K_D, U);
+    }
+    // the last MMAs complete before the consumers may free TMEM (bounded wait)
+    if (tseq > 0) {
+      const unsigned last = tseq - 1;
+      const unsigned long long t0 = gtimer();
+      while (!mbar_try_wait(&m->tfull[last % kNB], (last / kNB) & 1) && gtimer() - t0 < p.timeout_ns) {
+      }
+    }
+    mbar_arrive(&m->mma_done);
   }
 };
 
@@ -1866,8 +2195,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
       mbar_init(&empty[s], kConsumerWarps);
     }
     mbar_init(&m->rt_bar, 1);
+    mbar_init(&m->b_ready, 1);
+    mbar_init(&m->mma_done, 1);
+    for (int i = 0; i < kNB; ++i) {
+      mbar_init(&m->tfull[i], 1);
+      mbar_init(&m->tempty[i], kConsumerWarps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // the B operand region starts zero: rows beyond the step's tokens are never written
+  for (int i = tid; i < (L.red_off - L.xs_off) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + L.xs_off)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid < kMaxBatch) {
     int len = 0, tok = 0;
     if (tid < p.B) {
@@ -1893,6 +2231,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (tid == kConsumerWarps * 32) {
       Producer<BM, HD, G> prod(p, ring, full, empty, m);
       prod.run();
+    } else if (BM >= 2 && tid == (kConsumerWarps + 1) * 32) {  // (tensor-core tiles: steps of 2+ tokens)
+      MmaIssuer<BM, HD, G> mma(p, ring, full, m, smem + L.xs_off);
+      mma.run();
     }
     return;
   }

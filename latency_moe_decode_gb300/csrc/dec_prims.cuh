@@ -198,6 +198,81 @@ __device__ __forceinline__ void cons_sync() {
 
 
 // ---------------------------------------------------------------------------------------------
+// 5th-generation tensor cores (tcgen05): tensor memory (TMEM) accumulators, MMAs issued by one
+// thread with operands described in shared memory, completion signalled on an mbarrier.
+
+// Allocate ncols TMEM columns (a power of two >= 32) for this CTA; the base address is written to
+// *dst (shared). Executed by one whole warp, which must also free them.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Ordering of tensor-core operations across a thread synchronisation (barrier or mbarrier).
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Generic-proxy shared-memory writes (st.shared) made visible to the tensor cores' reads.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand without swizzling: 8-row x 16-byte core
+// matrices, lbo bytes between core matrices adjacent in K, sbo bytes between 8-row groups.
+__device__ __forceinline__ uint64_t smem_desc(const void* base, uint32_t lbo, uint32_t sbo) {
+  const uint32_t a = smem_u32(base);
+  return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46);  // descriptor version 1 (tcgen05); base offset 0; no swizzle
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (both K-major) and an fp32 D of
+// shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                          // D format: f32
+         | (0u << 7) | (0u << 10)           // A, B format: E4M3
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// D[tmem] (+)= A * B^T for one K = 32 slice of 8-bit operands.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on an mbarrier when every tensor-core operation this thread issued so far is done.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Each thread of a warp reads its TMEM lane (lane quadrant = warp % 4), NC consecutive columns.
+template <int NC>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&d)[8]) {
+  uint32_t r[8];
+  if constexpr (NC == 2) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+  } else if constexpr (NC == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+  } else {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d[i] = i < NC ? __uint_as_float(r[i]) : 0.f;
+}
+
+// ---------------------------------------------------------------------------------------------
 // conversions (CUDA's own FP8 conversion instruction; bf16 -> fp32 is a shift)
 
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
@@ -220,6 +295,11 @@ __device__ __forceinline__ void fma_f16x2_f32(uint32_t w2, uint32_t x2, float& a
       "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
       : "+f"(acc0), "+f"(acc1)
       : "r"(w2), "r"(x2));
+}
+
+// two floats -> two E4M3 codes (round to nearest even, saturating to +-448), low code first
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
