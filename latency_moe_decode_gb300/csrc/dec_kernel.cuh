@@ -41,16 +41,20 @@ namespace dec {
 // shared-memory layout (identical on host and device)
 
 struct SmemLayout {
-  int ring_off, full_off, empty_off, xs_off, red_off, misc_off, total;
+  int ring_off, full_off, empty_off, mempty_off, xs_off, red_off, misc_off, total;
 };
 
 constexpr int kMaxExperts = 128;
-// Tensor-core tiles: kNB TMEM accumulators of kMmaN fp32 columns each, so the MMA warp can run
-// kNB tiles ahead of the epilogue; activation k blocks per stage at most kMaxKb.
-constexpr int kNB = 4;
+// Tensor-core tiles: every tile's product gets its own kMmaN-column TMEM slice; tiles are handed
+// to the consumers in groups of up to kGT (consecutive tiles of one segment), kNG groups in
+// flight (all 512 TMEM columns), so the consumers synchronise with the MMA warp once per group.
+// Activation k blocks per stage at most kMaxKb.
 constexpr int kMmaN = 16;
-constexpr int kTmemCols = kNB * kMmaN;  // a power of two >= 32
+constexpr int kGT = 8;
+constexpr int kNG = 4;
+constexpr int kTmemCols = kNG * kGT * kMmaN;  // 512
 constexpr int kMaxKb = 64;
+constexpr int kMaxRing = 16;
 
 // Layout of the B operand (a stage's activations as E4M3 pieces, the canonical K-major layout
 // of 8-row x 16-byte core matrices) for a step of B tokens: each k block of 128 activations
@@ -91,11 +95,12 @@ struct Misc {
   int tok[kMaxBatch];
   // tensor-core tiles: the scale exponent a of each token's staged k block (its pieces encode
   // x * 2^a), the consumers -> MMA warp "stage operand ready" barrier (one phase per GEMV stage),
-  // the MMA warp's "done" barrier, per TMEM accumulator a "product ready" (MMA commit) and a
-  // "product read" (one arrival per consumer warp) barrier, and the TMEM base address
+  // the MMA warp's "done" barrier, per group of TMEM slices a "products ready" (MMA commit) and
+  // a "products read" (one arrival per consumer warp) barrier, and the TMEM base address
   int8_t xexp[kMaxBatch][kMaxKb];
   uint64_t b_ready, mma_done;
-  uint64_t tfull[kNB], tempty[kNB];
+  uint64_t tfull[kNG], tempty[kNG];
+  float2 hdr[kNG][kGT];  // the block scales of each group's tiles (their slots may be refilled first)
   uint32_t tmem_base;
 };
 
@@ -111,7 +116,8 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   s.ring_off = 0;
   s.full_off = align_up(ring * kSlotBytes, 128);
   s.empty_off = s.full_off + ring * 8;
-  s.xs_off = align_up(s.empty_off + ring * 8, 128);
+  s.mempty_off = s.empty_off + ring * 8;  // a slot's tiles read by the tensor cores (MMA commit)
+  s.xs_off = align_up(s.mempty_off + ring * 8, 128);
   // the stage's activations as tensor-core B operand blocks, for any step batch up to bm
   int xs_bytes = 0;
   for (int b = 1; b <= bm; ++b) {
@@ -357,8 +363,15 @@ struct Producer {
     }
   }
 
-  __device__ Producer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, Misc* m_)
-      : p(p_), ring(r), full(f), empty(e), m(m_) {}
+  // Slots are released by the consumer warps (count kConsumerWarps on `empty`), or, for weight
+  // tiles of the tensor-core kernels, by the MMA warp's commit once the MMAs reading them are
+  // done (count 1 on `mempty`). One bit per slot (ring <= kMaxRing <= 32): whether its last use
+  // completes `mempty`, and the parity of the number of uses of each kind so far.
+  uint64_t* mempty;
+  uint32_t last_mma = 0, ne_par = 0, nm_par = 0;
+
+  __device__ Producer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* e, uint64_t* me, Misc* m_)
+      : p(p_), ring(r), full(f), empty(e), m(m_), mempty(me) {}
 
   // every bulk copy source must lie inside its allocation (checked before the copy is issued)
   __device__ __forceinline__ static bool within(const void* src, size_t bytes, const void* base, size_t extent) {
@@ -374,7 +387,7 @@ struct Producer {
   // has. With a few copies per CTA in flight (enough to keep the memory busy), the first slots
   // land after about one unloaded latency and the rest follow at the rate they are consumed.
   // (p.inflight <= ring: the slot of item `landed` is never re-armed before it is checked.)
-  __device__ bool claim(int& slot) {
+  __device__ bool claim(int& slot, bool mma_use) {
     while (item - landed >= (unsigned)p.inflight) {
       if (!mbar_wait(&full[lslot], llap & 1, p, 12)) {
         dead = true;
@@ -387,11 +400,22 @@ struct Producer {
       }
     }
     slot = pslot;
+    const uint32_t bit = 1u << slot;
     if (plap > 0) {
-      if (!mbar_wait(&empty[slot], (plap - 1) & 1, p, 10)) {
+      // the previous use's phase: the (count - 1)-th completion, parity = count's parity flipped
+      const bool pm = (last_mma & bit) != 0;
+      const unsigned par = (((pm ? nm_par : ne_par) >> slot) & 1u) ^ 1u;
+      if (!mbar_wait(pm ? &mempty[slot] : &empty[slot], par, p, 10)) {
         dead = true;
         return false;
       }
+    }
+    if (mma_use) {
+      last_mma |= bit;
+      nm_par ^= bit;
+    } else {
+      last_mma &= ~bit;
+      ne_par ^= bit;
     }
     return true;
   }
@@ -417,7 +441,7 @@ struct Producer {
     if (t1 > t0) cur.init(p, Ld, kind, t0, g, U, elist);
     for (int t = t0; t < t1; t += kSlotTiles) {
       int slot;
-      if (!claim(slot)) return;
+      if (!claim(slot, BM >= 2)) return;  // (tensor-core kernels: the MMA warp frees weight slots)
       const int n = min(kSlotTiles, t1 - t);
       const uint8_t* src[kSlotTiles];
       bool ok = true;
@@ -456,7 +480,7 @@ struct Producer {
       AttnUnit a = attn_unit(p, m, u);
       for (int t = a.tile0; t < a.tile1; ++t) {
         int slot;
-        if (!claim(slot)) return;
+        if (!claim(slot, false)) return;
         int p0 = t * kKvTilePos;
         int n = min(kKvTilePos, a.T - p0);
         uint8_t* dst = ring + (size_t)slot * kSlotBytes;
@@ -569,7 +593,7 @@ struct Consumer {
   bool range_bad = false;  // (CUDA-core path) an activation staged as f16 was outside its range
   // tensor-core tiles: tiles whose products were added so far in this step (the sequence picks
   // the TMEM accumulator and its barriers' phases), the TMEM base, the B operand layout
-  unsigned tseq = 0;
+  unsigned gseq = 0;  // groups of tiles handed over so far (slot of TMEM slices, barrier phases)
   uint32_t tmem = 0;
   BGeo bg;
 
@@ -900,7 +924,7 @@ struct Consumer {
   // 16-byte core matrices, 128 bytes apart along K and 1024 apart along the rows) is multiplied
   // straight from its ring slot by tcgen05.mma kind::f8f6f4 (issued by the MMA warp): A = the raw
   // E4M3 codes, B = the stage's bf16 activations split exactly into two E4M3 pieces per value
-  // (see pieces()), D = 128 rows x 16 fp32 columns in one of kNB TMEM accumulators. Products of
+  // (see pieces()), D = 128 rows x 16 fp32 columns in the tile's own TMEM slice. Products of
   // 8-bit values are exact and the sums are fp32. The consumer warps add each tile's product
   // into fp32 registers, applying the pieces' scales, the tile's block scale and the expert gate
   // (a k block per tile, so the block scale cannot stay in TMEM). The tensor cores replace the
@@ -949,37 +973,45 @@ struct Consumer {
     for (int b = 0; b < BM && b < 4; ++b) acc[b] = fmaf(s_r * gmul[b], part[b][0] + part[b][1], acc[b]);
   }
 
-  // Add tile seq's product into the thread's accumulators: thread (warp w, lane) holds row
-  // 32 (w & 3) + lane of tokens 4 (w >> 2) .. 4 (w >> 2) + 3 (TMEM lane quadrant w & 3; token b's
-  // pieces are columns cb + 2b, cb + 2b + 1 for k block kbi, cb = (kbi mod pk) rpad); `tile` = the
-  // tile in its slot (block scales in its header), gate multipliers gm. Every consumer warp then
-  // hands the accumulator back to the MMA warp.
-  __device__ void epilogue(unsigned seq, const uint8_t* tile, const float* gm, int kbi, float (&acc)[4]) {
-    const int buf = seq % kNB;
-    if (!dead && !mbar_wait(&m->tfull[buf], (seq / kNB) & 1, p, 25)) dead = true;
+  // Add the products of group gs (n consecutive tiles of one segment, from position pos) into the
+  // thread's accumulators. Thread (warp w, lane) holds row 32 (w & 3) + lane of tokens
+  // 4 (w >> 2) .. 4 (w >> 2) + 3 (TMEM lane quadrant w & 3; tile i's product is slice
+  // (group slot) * kGT + i, where token b's pieces are columns cb + 2b, cb + 2b + 1 for its k
+  // block kbi, cb = (kbi mod pk) rpad), scaled by the pieces' 2^-a, the tile's block scale (copied
+  // by the MMA warp) and the expert gate. Every consumer warp then hands the slices back.
+  __device__ void group_epilogue(unsigned gs, int n, TilePos pos, int kind, int nv, const StageGeo& g,
+                                 float (&acc)[4]) {
+    const int gsl = gs % kNG;
+    if (!dead && !mbar_wait(&m->tfull[gsl], (gs / kNG) & 1, p, 25)) dead = true;
     const int q = warp & 3, h = warp >> 2;
     if (!dead && 4 * h < p.B) {  // (warp-uniform)
       tc_fence_after();
       const int row = 32 * q + lane;
-      const float2 sc = *reinterpret_cast<const float2*>(tile + kTileData);
-      const float s_r = row < 64 ? sc.x : sc.y;
-      const int cb = (kbi % bg.pk) * bg.rpad + 8 * h;
-      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + buf * kMmaN + cb;
-      float d[8];
       constexpr int NC = BM >= 4 ? 8 : 2 * BM;
-      tmem_ld<NC>(ta, d);
+#pragma unroll 1
+      for (int i = 0; i < n; ++i) {
+        const int kbi = pos.kbi(p, kind);
+        const float2 sc = m->hdr[gsl][i];
+        const float s_r = row < 64 ? sc.x : sc.y;
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((gsl * kGT + i) * kMmaN) +
+                            (uint32_t)((kbi % bg.pk) * bg.rpad + 8 * h);
+        float d[8];
+        tmem_ld<NC>(ta, d);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int b = 4 * h + i;
-        if (b < p.B && 2 * i < NC) {
-          const float inv = __int_as_float((127 - (int)m->xexp[b][kbi]) << 23);  // 2^-a
-          acc[i] = fmaf(s_r * gm[b] * inv, fmaf(d[2 * i + 1], 0.0625f, d[2 * i]), acc[i]);
+        for (int j = 0; j < 4; ++j) {
+          const int b = 4 * h + j;
+          if (b < p.B && 2 * j < NC) {
+            const float gm = kind == K_D ? m->gate[b][min(pos.v, kMaxExperts)] : 1.f;
+            const float inv = __int_as_float((127 - (int)m->xexp[b][kbi]) << 23);  // 2^-a
+            acc[j] = fmaf(s_r * gm * inv, fmaf(d[2 * j + 1], 0.0625f, d[2 * j]), acc[j]);
+          }
         }
+        pos.next(p, g, kind, nv);
       }
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&m->tempty[buf]);
+    if (lane == 0) mbar_arrive(&m->tempty[gsl]);
   }
 
   __device__ float* part_base(int kind) const {
@@ -1121,7 +1153,7 @@ struct Consumer {
     pe.init(p, g, kind, t0, t1);
     int j = 0;  // tile j of the current slot (the producer packs kSlotTiles consecutive tiles per slot)
     const uint8_t* slot_base = ring;
-    for (int t = t0;; ++t) {
+    for (int t = t0;;) {
       // a segment ends at a segment boundary or at the end of the range (one flush call site)
       if (t == t1 || pe.seg != seg_cur) {
         if (t == t1) {
@@ -1141,19 +1173,34 @@ struct Consumer {
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] = 0.f;
       }
-#pragma unroll
-      for (int b = 0; b < BM; ++b) gmul[b] = kind == K_D ? m->gate[b][min(pe.v, kMaxExperts)] : 1.f;
       if constexpr (kTC) {
-        epilogue(tseq++, ring + (size_t)rslot * kSlotBytes + (size_t)j * kTileBytes, gmul, pe.kbi(p, kind), acc);
+        // a group: up to kGT tiles of this segment (the MMA warp forms the same groups)
+        const int n = min(kGT, min(t1, (pe.seg + 1) * g.kbs) - t);
+        group_epilogue(gseq++, n, pe, kind, nv, g, acc);
+        for (int i = 0; i < n; ++i) pe.next(p, g, kind, nv);
+        t += n;
       } else {
+#pragma unroll
+        for (int b = 0; b < BM; ++b) gmul[b] = kind == K_D ? m->gate[b][min(pe.v, kMaxExperts)] : 1.f;
         if (j == 0) slot_base = wait_item();
         if (!dead) tile_dot(slot_base + (size_t)j * kTileBytes, pe.kbi(p, kind) * kTileK, gmul, acc);
+        if (++j == kSlotTiles || t == t1 - 1) {
+          release_item();
+          j = 0;
+        }
+        pe.next(p, g, kind, nv);
+        ++t;
       }
-      if (++j == kSlotTiles || t == t1 - 1) {
-        release_item();
-        j = 0;
+    }
+    if constexpr (kTC) {
+      // the stage's weight slots were freed by the MMA warp; keep the ring position in step
+      for (int k = 0; k < (t1 - t0 + kSlotTiles - 1) / kSlotTiles; ++k) {
+        ++item;
+        if (++rslot == p.ring) {
+          rslot = 0;
+          rpar ^= 1;
+        }
       }
-      pe.next(p, g, kind, nv);
     }
     // Finalise the output groups this CTA is designated for (groups spread evenly over the
     // CTAs, so no CTA finalises two while others finalise none): wait (acquire) until every
@@ -2063,25 +2110,26 @@ struct Consumer {
 
 // ---------------------------------------------------------------------------------------------
 // MMA warp: one thread walks the CTA's GEMV tiles in the consumers' order and hands each to the
-// tensor cores once its ring slot has landed, its stage's activations are staged and a TMEM
-// accumulator is free, up to kNB tiles ahead of the consumers.
+// tensor cores once its ring slot has landed, its stage's activations are staged and its group
+// of TMEM slices is free, up to kNG groups ahead of the consumers.
 
 template <int BM, int HD, int G>
 struct MmaIssuer {
   const KParams& p;
   uint8_t* ring;
   uint64_t* full;
+  uint64_t* mempty;
   Misc* m;
   const uint8_t* xsb;  // the B operand region
   int slot = 0;        // ring slot of the next item (items: GEMV slots and the attention's KV tiles)
   unsigned lap = 0;
-  unsigned tseq = 0, stage = 0;
+  unsigned gseq = 0, stage = 0;
   bool dead = false;
   uint32_t tmem = 0;
   BGeo bg;
 
-  __device__ MmaIssuer(const KParams& p_, uint8_t* r, uint64_t* f, Misc* m_, const uint8_t* x)
-      : p(p_), ring(r), full(f), m(m_), xsb(x) {
+  __device__ MmaIssuer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* me, Misc* m_, const uint8_t* x)
+      : p(p_), ring(r), full(f), mempty(me), m(m_), xsb(x) {
     bg = bgeo(p.B);
   }
 
@@ -2093,6 +2141,9 @@ struct MmaIssuer {
       }
   }
 
+  // The stage's tiles in groups of up to kGT per segment (as the consumers take them): each tile
+  // gets TMEM slice (group slot) * kGT + i; a slot is freed (commit on its mempty barrier) after
+  // its last tile's MMAs, a group announced (commit on tfull) after its last tile's.
   __device__ void gemv(int kind, int U) {
     if (!dead && !mbar_wait(&m->b_ready, stage & 1, p, 26)) dead = true;
     ++stage;
@@ -2107,30 +2158,39 @@ struct MmaIssuer {
     const uint32_t sbo = bg.nrb == 16 ? 1024u : 0u;  // 8-row blocks: the second row group aliases the first
     int j = 0;
 #pragma unroll 1
-    for (int t = t0; t < t1; ++t) {
-      if (!dead) {
-        const int buf = tseq % kNB;
-        if (j == 0 && !mbar_wait(&full[slot], lap & 1, p, 27)) dead = true;
-        if (!dead && tseq >= (unsigned)kNB && !mbar_wait(&m->tempty[buf], (tseq / kNB - 1) & 1, p, 28)) dead = true;
+    for (int t = t0; t < t1;) {
+      const int n = min(kGT, min(t1, (pos.seg + 1) * g.kbs) - t);
+      const int gsl = gseq % kNG;
+      if (!dead && gseq >= (unsigned)kNG && !mbar_wait(&m->tempty[gsl], (gseq / kNG - 1) & 1, p, 28)) dead = true;
+#pragma unroll 1
+      for (int i = 0; i < n; ++i, ++t) {
+        if (!dead && j == 0 && !mbar_wait(&full[slot], lap & 1, p, 27)) dead = true;
+        const uint8_t* a = ring + (size_t)slot * kSlotBytes + (size_t)j * kTileBytes;
         if (!dead) {
           tc_fence_after();
+          m->hdr[gsl][i] = *reinterpret_cast<const float2*>(a + kTileData);
           const int kbi = pos.kbi(p, kind);
-          const uint8_t* a = ring + (size_t)slot * kSlotBytes + (size_t)j * kTileBytes;
           const uint8_t* b = xsb + (size_t)(kbi / bg.pk) * bg.nrb * 128;
           const uint64_t ad = smem_desc(a, 128, 1024), bd = smem_desc(b, 128, sbo);
-          const uint32_t d = tmem + buf * kMmaN;
+          const uint32_t d = tmem + (uint32_t)((gsl * kGT + i) * kMmaN);
 #pragma unroll
           for (int k = 0; k < kTileK / 32; ++k)  // 32 bytes of K per MMA: two core matrices (256 B)
             mma_e4m3(d, ad + (uint64_t)(k * 16), bd + (uint64_t)(k * 16), idesc, k > 0 ? 1u : 0u);
-          mma_commit(&m->tfull[buf]);
+        }
+        pos.next(p, g, kind, nv);
+        if (++j == kSlotTiles || t == t1 - 1) {
+          if (!dead) mma_commit(&mempty[slot]);  // the slot's tiles are read once these MMAs are done
+          j = 0;
+          skip(1);
         }
       }
-      ++tseq;
-      pos.next(p, g, kind, nv);
-      if (++j == kSlotTiles || t == t1 - 1) {
-        j = 0;
-        skip(1);
+      if (!dead) {
+        // the group's products are ready once both arrivals are in: the commit (MMAs done) and
+        // this thread's own (a release that orders its header copies before the consumers' reads)
+        mma_commit(&m->tfull[gsl]);
+        mbar_arrive(&m->tfull[gsl]);
       }
+      ++gseq;
     }
   }
 
@@ -2165,10 +2225,10 @@ struct MmaIssuer {
       gemv(K_D, U);
     }
     // the last MMAs complete before the consumers may free TMEM (bounded wait)
-    if (tseq > 0) {
-      const unsigned last = tseq - 1;
+    if (gseq > 0) {
+      const unsigned last = gseq - 1;
       const unsigned long long t0 = gtimer();
-      while (!mbar_try_wait(&m->tfull[last % kNB], (last / kNB) & 1) && gtimer() - t0 < p.timeout_ns) {
+      while (!mbar_try_wait(&m->tfull[last % kNG], (last / kNG) & 1) && gtimer() - t0 < p.timeout_ns) {
       }
     }
     mbar_arrive(&m->mma_done);
@@ -2184,6 +2244,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
   uint8_t* ring = smem + L.ring_off;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
+  uint64_t* mempty = reinterpret_cast<uint64_t*>(smem + L.mempty_off);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs_off);
   float* red = reinterpret_cast<float*>(smem + L.red_off);
   Misc* m = reinterpret_cast<Misc*>(smem + L.misc_off);
@@ -2193,12 +2254,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     for (int s = 0; s < p.ring; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&mempty[s], 1);
     }
     mbar_init(&m->rt_bar, 1);
     mbar_init(&m->b_ready, 1);
     mbar_init(&m->mma_done, 1);
-    for (int i = 0; i < kNB; ++i) {
-      mbar_init(&m->tfull[i], 1);
+    for (int i = 0; i < kNG; ++i) {
+      mbar_init(&m->tfull[i], 2);  // MMA commit + the MMA thread's release of the headers
       mbar_init(&m->tempty[i], kConsumerWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -2229,10 +2291,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
   if (tid >= kConsumerWarps * 32) {
     if (tid == kConsumerWarps * 32) {
-      Producer<BM, HD, G> prod(p, ring, full, empty, m);
+      Producer<BM, HD, G> prod(p, ring, full, empty, mempty, m);
       prod.run();
     } else if (BM >= 2 && tid == (kConsumerWarps + 1) * 32) {  // (tensor-core tiles: steps of 2+ tokens)
-      MmaIssuer<BM, HD, G> mma(p, ring, full, m, smem + L.xs_off);
+      MmaIssuer<BM, HD, G> mma(p, ring, full, mempty, m, smem + L.xs_off);
       mma.run();
     }
     return;
