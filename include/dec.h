@@ -136,10 +136,13 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* weights, void* 
                     dec_engine** out);
 
 /* Fill the KV cache of sequence slots [seq, seq + n_seq).
-   Token mode (k_import == NULL): token_ids is device int32 [n_seq][n_tokens]; the engine runs
-   n_tokens batched decode steps (slots decoded together), appending to each slot's current
-   length, and discards the logits. This is decode-engine prefill as on the pages' prefill/decode
-   split; it is not a fast prefill path.
+   Token mode (k_import == NULL): token_ids is device int32 [n_seq][n_tokens]; appending to each
+   slot's current length, the engine runs the decode kernel over the prompt and discards the
+   logits: for one slot (n_seq == 1) in launches of up to DEC_MAX_STEP_TOKENS consecutive
+   positions each (as dec_step_positions: every launch streams the weights once for all of its
+   positions), for several slots one launch per position with the slots side by side. This is
+   decode-engine prefill as on the pages' prefill/decode split, not a compute-bound prefill
+   engine.
    Import mode (k_import != NULL): copies an external KV state, device bf16
    [n_layers][n_kv_heads][n_tokens][head_dim] for K (post-RoPE) and V, into positions
    0..n_tokens of every slot in the range and sets their length to n_tokens (the handoff of a KV
@@ -201,6 +204,29 @@ typedef struct {
 } dec_step_args;
 dec_status dec_step_ex(dec_engine* eng, const dec_step_args* args);
 
+/* The most tokens one launch takes (sequences side by side, or positions of one sequence). */
+#define DEC_MAX_STEP_TOKENS 8
+
+/* Several consecutive positions of ONE sequence in one launch ("vLLM's Kimi K3 Backend Hits 842
+   Tokens per Second", section "Throughput holds across the tested range": verifying speculative
+   drafts; also chunked prefill). tokens is device int32 [n], 1 <= n <= DEC_MAX_STEP_TOKENS;
+   token j is written at position length[seq] + j and attends over positions 0 .. length + j
+   (causal: the keys and values of the earlier tokens of the same launch included); the slot's
+   length grows by n. logits device fp32 [n][vocab] and next_tokens device int32 [n] (the argmax
+   after each position) are optional. One launch on `stream`; nothing is synchronised.
+   Requires vocab > 0. Errors: DEC_ERR_ARG, DEC_ERR_CAPACITY, DEC_ERR_POISONED, DEC_ERR_CUDA. */
+dec_status dec_step_positions(dec_engine* eng, int32_t seq, const int32_t* tokens, int32_t n,
+                              float* logits, int32_t* next_tokens, void* stream);
+
+/* Speculative-decoding verify step: as dec_step_positions with tokens = [t0, d1, .., d(n-1)], t0
+   the sequence's next input token and d the draft. The kernel accepts draft d(j+1) while it equals
+   the argmax after position length + j, writes the accepted count m (0 <= m < n) to the host
+   int *n_accepted, and keeps the positions length .. length + m in the cache: the slot's length
+   becomes length + m + 1, and next_tokens[m] (if given) is the next input token. Synchronises
+   with `stream` (the caller needs m to go on). */
+dec_status dec_verify(dec_engine* eng, int32_t seq, const int32_t* tokens, int32_t n, float* logits,
+                      int32_t* next_tokens, int32_t* n_accepted, void* stream);
+
 /* The plain form: slots [0, batch), token input, logits/next_tokens outputs (may be NULL). */
 dec_status dec_step(dec_engine* eng, const int32_t* token_ids, int32_t batch, float* logits,
                     int32_t* next_tokens, void* stream);
@@ -240,12 +266,14 @@ typedef struct {
 dec_status dec_get_info(dec_engine* eng, dec_info* out);
 
 /* Routing of the most recent step at one layer (MoE models): copies the selected experts
-   (score-descending) into host idx [max_batch][top_k] and their normalised gates into host
-   gates [max_batch][top_k]; rows >= the step's batch are stale. Synchronises. */
+   (score-descending) into host idx [DEC_MAX_STEP_TOKENS][top_k] and their normalised gates into
+   host gates [DEC_MAX_STEP_TOKENS][top_k], one row per token of the step; rows >= the step's
+   token count are stale. Synchronises. */
 dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* gates);
 
 /* The router logits (fp32, before the sigmoid) the most recent step selected from at one layer
-   (MoE models): host logits [max_batch][n_experts]; rows >= the step's batch are stale. With
+   (MoE models): host logits [DEC_MAX_STEP_TOKENS][n_experts]; rows >= the step's token count
+   are stale. With
    dec_get_routing this lets a caller check that a selection is the top_k of its own logits
    (ties to the lower expert index). Synchronises. */
 dec_status dec_get_router_logits(dec_engine* eng, int32_t layer, float* logits);

@@ -13,6 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdec.so")
 
 DEC_OK = 0
+DEC_MAX_STEP_TOKENS = 8  # include/dec.h
 STATUS = {0: "DEC_OK", -1: "DEC_ERR_ARG", -2: "DEC_ERR_CUDA", -3: "DEC_ERR_OOM", -4: "DEC_ERR_TIMEOUT",
           -5: "DEC_ERR_UNSUPPORTED", -6: "DEC_ERR_POISONED", -7: "DEC_ERR_DEVICE", -8: "DEC_ERR_CAPACITY"}
 
@@ -66,6 +67,10 @@ PROTOTYPES = {
     "dec_prefill_kv_noalloc": (C.c_int, [C.c_void_p, C.POINTER(DecCtx)]),
     "dec_step_ex": (C.c_int, [C.c_void_p, C.POINTER(DecStepArgs)]),
     "dec_step": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "dec_step_positions": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
+                                     C.c_void_p]),
+    "dec_verify": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
+                             C.POINTER(C.c_int32), C.c_void_p]),
     "dec_generate": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "dec_set_length": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "dec_get_length": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int32)]),

@@ -80,7 +80,8 @@ struct KParams {
   const float2* rope;  // [max_ctx][hd/2] (cos, sin)
   uint16_t* kc;        // [L][MB][hkv][max_ctx][hd]
   uint16_t* vc;
-  int32_t* lengths;    // [MB]
+  int32_t* lengths;    // [slots]
+  int slots;           // KV cache slots (sequences); MB is the token capacity of one step
   // activations
   uint16_t* xbuf;   // [2][MB][d]
   uint16_t* xmid;   // [MB][d]
@@ -119,6 +120,12 @@ struct KParams {
   const int32_t* tokens;
   const uint16_t* hidden_in;
   int B, seq0;
+  // 1: the B tokens are consecutive positions length[seq0] .. + B - 1 of slot seq0 (a verify or
+  // prefill step), each attending over the cache and the step's earlier new keys (causal)
+  int mpos;
+  // verify steps: the number of draft tokens accepted (tokens[j + 1] == argmax after position j
+  // for j < m) is written here and the slot's length set to length + m + 1
+  int32_t* accepted;
   float* logits;
   int32_t* next_tokens;
   uint16_t* hidden_out;

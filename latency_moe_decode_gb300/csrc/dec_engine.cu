@@ -146,6 +146,7 @@ struct dec_engine {
   bool poisoned = false;
   std::string err;
   int32_t* d_hist = nullptr;
+  int32_t* d_accepted = nullptr;  // verify steps: the accepted draft count
   int64_t launches = 0, weight_bytes = 0, kv_bytes = 0, ws_bytes = 0;
   uint8_t* arena = nullptr;  // all repacked weight tiles (one allocation the kernel bounds-checks)
   size_t arena_size = 0, arena_used = 0;
@@ -424,7 +425,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   p.dense = dense ? 1 : 0;
   p.V = c.vocab;
   p.max_ctx = c.max_ctx;
-  p.MB = c.max_batch;
+  p.MB = kMaxBatch;  // tokens one step can take: sequences side by side, or positions of one
+  p.slots = c.max_batch;
   p.eps = c.rms_eps;
   p.kb_d = c.hidden / kTileK;
   p.kb_o = c.n_heads * c.head_dim / kTileK;
@@ -436,7 +438,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   p.n_rb_lm = (c.vocab + kTileRows - 1) / kTileRows;
   p.e_gu_stride = (long long)p.n_rb_gu * p.kb_d * kTileBytes;
   p.e_d_stride = (long long)p.n_rb_d * p.kb_i * kTileBytes;
-  p.umax = dense ? 0 : std::min(c.n_experts, c.max_batch * c.top_k);
+  p.umax = dense ? 0 : std::min(c.n_experts, p.MB * c.top_k);
   e->grid = e->sms;
   const int G = e->grid;
   {
@@ -576,7 +578,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
 
   // ---- workspace
   {
-    const int MB = c.max_batch, d = c.hidden, qd = c.n_heads * c.head_dim;
+    const int MB = p.MB, d = c.hidden, qd = c.n_heads * c.head_dim;
     const size_t rows = kTileRows;
     auto zalloc = [&](auto** ptr, size_t bytes) -> dec_status {
       dec_status s2 = dalloc(e, ptr, bytes, &e->ws_bytes);
@@ -585,7 +587,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     };
 #define Z(ptr, bytes) \
   if ((st = zalloc(&(ptr), (bytes))) != DEC_OK) return bail(st);
-    Z(p.lengths, sizeof(int32_t) * MB);
+    Z(p.lengths, sizeof(int32_t) * c.max_batch);
+    Z(e->d_accepted, sizeof(int32_t) * 4);
     Z(p.xbuf, 2ull * MB * d * 2);
     Z(p.xmid, (size_t)MB * d * 2);
     Z(p.qbuf, (size_t)MB * qd * 2);
@@ -662,7 +665,6 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, e->device);
   for (int i = 0; i < 4; ++i) {
     const int bm = kBmChoices[i];
-    if (bm > std::max(1, c.max_batch) && i > 0 && kBmChoices[i - 1] >= c.max_batch) continue;
     KernelFn k = kernel_for(bm, e->hd, e->group);
     if (!k) return bail(DEC_ERR_UNSUPPORTED);
     int ring = 16;
@@ -695,6 +697,85 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   return DEC_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// One launch of the decode kernel: B tokens, either one per slot seq0 .. seq0 + B - 1, or (mpos)
+// consecutive positions of slot seq0; `accepted` (device) makes it a verify step. Arguments are
+// checked by the callers.
+dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t* tokens, const void* hidden_in,
+                       float* logits, int32_t* next_tokens, void* hidden_out, int32_t* accepted, cudaStream_t s) {
+  const dec_model_cfg& c = e->cfg;
+  int bi = 0;
+  while (kBmChoices[bi] < B) ++bi;
+  KParams p = e->base;
+  p.B = B;
+  p.seq0 = seq0;
+  p.mpos = mpos ? 1 : 0;
+  p.accepted = accepted;
+  p.tokens = tokens;
+  p.hidden_in = static_cast<const uint16_t*>(hidden_in);
+  p.logits = logits;
+  p.next_tokens = next_tokens;
+  p.hidden_out = static_cast<uint16_t*>(hidden_out);
+  if (dec_status os = order_on(e, s)) return os;
+  if (e->epoch >= e->epoch_limit) {
+    for (const auto& b : e->epoch_bufs) {
+      cudaError_t me = cudaMemsetAsync(b.first, 0, b.second, s);
+      if (me != cudaSuccess) return cuda_fail(e, me, "epoch restart");
+    }
+    e->epoch = 0;
+  }
+  p.epoch = ++e->epoch;
+  p.ring = e->ring[bi];
+  p.inflight = std::min(p.ring, kSlotsInFlight);
+  p.nch = std::max(1, std::min(e->nch_max, e->grid / (B * c.n_kv_heads)));
+  void* args[] = {&p};
+  cudaError_t ce = cudaLaunchCooperativeKernel((const void*)e->kern[bi], dim3(e->grid), dim3(kThreads), args,
+                                               (size_t)e->smem[bi], s);
+  if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaLaunchCooperativeKernel");
+  if (mpos) e->lengths[seq0] += B;
+  else
+    for (int b = 0; b < B; ++b) e->lengths[seq0 + b] += 1;
+  e->launches += 1;
+  return DEC_OK;
+}
+
+// Token-mode prefill from step-major ids tt[t][s] (device): one slot -> chunks of up to
+// DEC_MAX_STEP_TOKENS consecutive positions per launch; several slots -> one launch per position
+// with the slots side by side. Queued on the engine's stream.
+dec_status prefill_steps(dec_engine* e, const int32_t* tt, int n_seq, int n_tokens, int seq) {
+  dec_status st = DEC_OK;
+  if (n_seq == 1) {
+    for (int t = 0; t < n_tokens && st == DEC_OK; t += DEC_MAX_STEP_TOKENS) {
+      const int n = std::min(DEC_MAX_STEP_TOKENS, n_tokens - t);
+      st = launch_step(e, n, seq, true, tt + t, nullptr, nullptr, nullptr, nullptr, nullptr, e->stream);
+    }
+    return st;
+  }
+  for (int t = 0; t < n_tokens && st == DEC_OK; ++t)
+    st = launch_step(e, n_seq, seq, false, tt + (size_t)t * n_seq, nullptr, nullptr, nullptr, nullptr, nullptr,
+                     e->stream);
+  return st;
+}
+
+// Checks shared by the multi-position entry points.
+dec_status check_positions(dec_engine* e, int32_t seq, const int32_t* tokens, int32_t n) {
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  if (dec_status ds = check_device(e)) return ds;
+  const dec_model_cfg& c = e->cfg;
+  if (!tokens || n < 1 || n > DEC_MAX_STEP_TOKENS || seq < 0 || seq >= c.max_batch)
+    return fail(e, DEC_ERR_ARG, "positions: tokens, 1 <= n <= DEC_MAX_STEP_TOKENS, seq in range");
+  if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "positions need an embedding and an LM head");
+  if (e->lengths[seq] + n > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "sequence full");
+  return DEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 dec_status dec_step_ex(dec_engine* e, const dec_step_args* a) {
   if (!e || !a) return DEC_ERR_ARG;
   if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
@@ -709,35 +790,34 @@ dec_status dec_step_ex(dec_engine* e, const dec_step_args* a) {
   if (a->hidden_in && !aligned16(a->hidden_in)) return fail(e, DEC_ERR_ARG, "hidden_in must be 16-byte aligned");
   for (int b = 0; b < a->batch; ++b)
     if (e->lengths[a->seq0 + b] + 1 > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "sequence full");
-  int bi = 0;
-  while (kBmChoices[bi] < a->batch) ++bi;
-  KParams p = e->base;
-  p.B = a->batch;
-  p.seq0 = a->seq0;
-  p.tokens = a->tokens;
-  p.hidden_in = static_cast<const uint16_t*>(a->hidden_in);
-  p.logits = a->logits;
-  p.next_tokens = a->next_tokens;
-  p.hidden_out = static_cast<uint16_t*>(a->hidden_out);
   cudaStream_t s = a->stream ? static_cast<cudaStream_t>(a->stream) : e->stream;
-  if (dec_status os = order_on(e, s)) return os;
-  if (e->epoch >= e->epoch_limit) {
-    for (const auto& b : e->epoch_bufs) {
-      cudaError_t me = cudaMemsetAsync(b.first, 0, b.second, s);
-      if (me != cudaSuccess) return cuda_fail(e, me, "epoch restart");
-    }
-    e->epoch = 0;
-  }
-  p.epoch = ++e->epoch;
-  p.ring = e->ring[bi];
-  p.inflight = std::min(p.ring, kSlotsInFlight);
-  p.nch = std::max(1, std::min(e->nch_max, e->grid / (a->batch * c.n_kv_heads)));
-  void* args[] = {&p};
-  cudaError_t ce = cudaLaunchCooperativeKernel((const void*)e->kern[bi], dim3(e->grid), dim3(kThreads), args,
-                                               (size_t)e->smem[bi], s);
-  if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaLaunchCooperativeKernel");
-  for (int b = 0; b < a->batch; ++b) e->lengths[a->seq0 + b] += 1;
-  e->launches += 1;
+  return launch_step(e, a->batch, a->seq0, false, a->tokens, a->hidden_in, a->logits, a->next_tokens, a->hidden_out,
+                     nullptr, s);
+}
+
+dec_status dec_step_positions(dec_engine* e, int32_t seq, const int32_t* tokens, int32_t n, float* logits,
+                              int32_t* next_tokens, void* stream) {
+  if (!e) return DEC_ERR_ARG;
+  if (dec_status cs = check_positions(e, seq, tokens, n)) return cs;
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
+  return launch_step(e, n, seq, true, tokens, nullptr, logits, next_tokens, nullptr, nullptr, s);
+}
+
+dec_status dec_verify(dec_engine* e, int32_t seq, const int32_t* tokens, int32_t n, float* logits,
+                      int32_t* next_tokens, int32_t* n_accepted, void* stream) {
+  if (!e || !n_accepted) return DEC_ERR_ARG;
+  if (dec_status cs = check_positions(e, seq, tokens, n)) return cs;
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
+  const int32_t len0 = e->lengths[seq];
+  dec_status st = launch_step(e, n, seq, true, tokens, nullptr, logits, next_tokens, nullptr, e->d_accepted, s);
+  if (st != DEC_OK) return st;
+  int32_t acc = 0;
+  DEC_CUDA(cudaMemcpyAsync(&acc, e->d_accepted, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  DEC_CUDA(cudaStreamSynchronize(s));
+  if (dec_status ds = check_device_status(e)) return ds;
+  if (acc < 0 || acc >= n) return fail(e, DEC_ERR_DEVICE, "verify: accepted count out of range");
+  e->lengths[seq] = len0 + acc + 1;  // the kernel set the device length the same way
+  *n_accepted = acc;
   return DEC_OK;
 }
 
@@ -799,14 +879,7 @@ dec_status dec_prefill_kv(dec_engine* e, const dec_ctx* x) {
   DEC_CUDA(cudaMalloc(&tt, sizeof(int32_t) * (size_t)x->n_seq * x->n_tokens));
   const int n = x->n_seq * x->n_tokens;
   transpose_tokens_kernel<<<(n + 255) / 256, 256, 0, e->stream>>>(x->token_ids, x->n_seq, x->n_tokens, tt);
-  dec_status st = DEC_OK;
-  for (int t = 0; t < x->n_tokens && st == DEC_OK; ++t) {
-    dec_step_args a{};
-    a.tokens = tt + (size_t)t * x->n_seq;
-    a.batch = x->n_seq;
-    a.seq0 = x->seq;
-    st = dec_step_ex(e, &a);
-  }
+  dec_status st = prefill_steps(e, tt, x->n_seq, x->n_tokens, x->seq);
   cudaError_t ce = cudaStreamSynchronize(e->stream);
   cudaFree(tt);
   if (st != DEC_OK) return st;
@@ -850,13 +923,7 @@ dec_status dec_prefill_kv_noalloc(dec_engine* e, const dec_ctx* x) {
   const int n = x->n_seq * x->n_tokens;
   transpose_tokens_kernel<<<(n + 255) / 256, 256, 0, e->stream>>>(x->token_ids, x->n_seq, x->n_tokens, tt);
   DEC_CUDA(cudaGetLastError());
-  for (int t = 0; t < x->n_tokens && st == DEC_OK; ++t) {
-    dec_step_args a{};
-    a.tokens = tt + (size_t)t * x->n_seq;
-    a.batch = x->n_seq;
-    a.seq0 = x->seq;
-    st = dec_step_ex(e, &a);
-  }
+  st = prefill_steps(e, tt, x->n_seq, x->n_tokens, x->seq);
   cudaError_t ce = cudaStreamSynchronize(e->stream);
   if (st != DEC_OK) return st;
   if (ce != cudaSuccess) return cuda_fail(e, ce, "prefill synchronize");
@@ -942,7 +1009,7 @@ dec_status dec_get_routing(dec_engine* e, int32_t layer, int32_t* idx, float* ga
   const dec_model_cfg& c = e->cfg;
   if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
   if (dec_status os = order_on(e, e->stream)) return os;
-  const size_t n = (size_t)c.max_batch * c.top_k, off = (size_t)layer * n;
+  const size_t n = (size_t)e->base.MB * c.top_k, off = (size_t)layer * n;
   DEC_CUDA(cudaMemcpyAsync(idx, e->base.rt_idx + off, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, e->stream));
   DEC_CUDA(cudaMemcpyAsync(gates, e->base.rt_topk_gate + off, sizeof(float) * n, cudaMemcpyDeviceToHost, e->stream));
   DEC_CUDA(cudaStreamSynchronize(e->stream));
@@ -954,7 +1021,7 @@ dec_status dec_get_router_logits(dec_engine* e, int32_t layer, float* logits) {
   const dec_model_cfg& c = e->cfg;
   if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
   if (dec_status os = order_on(e, e->stream)) return os;
-  const size_t n = (size_t)c.max_batch * c.n_experts;
+  const size_t n = (size_t)e->base.MB * c.n_experts;
   DEC_CUDA(cudaMemcpyAsync(logits, e->base.rt_logits + (size_t)layer * n, sizeof(float) * n, cudaMemcpyDeviceToHost,
                            e->stream));
   DEC_CUDA(cudaStreamSynchronize(e->stream));

@@ -127,7 +127,11 @@ __host__ __device__ inline SmemLayout smem_layout(int ring, int bm, int xmax, in
   }
   s.red_off = align_up(s.xs_off + xs_bytes, 128);
   int red_gemv = 2 * kTileRows * bm * 4;
+  // attention: the warps' states, or the unit's q/k/v (+ raw sums) and, in multi-position steps,
+  // every new token's key and value
   int red_attn = kConsumerWarps * group * (hd + 2) * 4;
+  const int red_qkv = (2 * (group + 2) * hd + 2 * bm * hd) * 4;
+  red_attn = red_attn > red_qkv ? red_attn : red_qkv;
   int red_fin = (bm * kTileRows + kListCap + 16) * 4;
   int red = red_gemv > red_attn ? red_gemv : red_attn;
   red = red > red_fin ? red : red_fin;
@@ -325,7 +329,8 @@ __device__ __forceinline__ AttnUnit attn_unit(const KParams& p, const Misc* m, i
 }
 
 __device__ __forceinline__ size_t kv_row(const KParams& p, int l, int b, int g, int pos) {
-  return ((((size_t)l * p.MB + (p.seq0 + b)) * p.hkv + g) * p.max_ctx + pos) * p.hd;
+  const int slot = p.mpos ? p.seq0 : p.seq0 + b;  // (consecutive positions share one slot)
+  return ((((size_t)l * p.slots + slot) * p.hkv + g) * p.max_ctx + pos) * p.hd;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1522,9 +1527,20 @@ struct Consumer {
           int old = atom_add_acqrel(p.cnt_lm_done, 1);
           if (old + 1 == p.n_rb_lm) {
             __threadfence();
+            // verify steps: draft token j + 1 is accepted while it equals the argmax after
+            // position j; the slot keeps the positions up to the last accepted draft
+            int acc = 0;
+            bool run = p.accepted != nullptr;
             for (int b = 0; b < p.B; ++b) {
               unsigned long long key = atomicExch(p.amax + b, 0ull);
-              if (p.next_tokens) p.next_tokens[b] = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
+              const int tok = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
+              if (p.next_tokens) p.next_tokens[b] = tok;
+              if (run && b + 1 < p.B && tok == p.tokens[b + 1]) ++acc;
+              else run = false;
+            }
+            if (p.accepted) {
+              *p.accepted = acc;
+              p.lengths[p.seq0] = m->len[0] + acc + 1;
             }
             atomicExch(p.cnt_lm_done, 0);
           }
@@ -1688,6 +1704,43 @@ struct Consumer {
     cons_sync();
   }
 
+  // Multi-position steps: the key and value of every new token of the step at KV head a.g, for
+  // patching the KV tiles this unit reads (their copies of the cache may predate this step's
+  // writes): ext[2j][HD] the key of token j rotated at its position length + j, ext[2j + 1][HD]
+  // its value, both rounded to bf16. The sums and the rotation are the prologue's, so the unit's
+  // own token comes out bit for bit the same. (The q/k/v counters are complete: waited for by
+  // the prologue.)
+  __device__ void new_kv_rows(const AttnUnit& a, float* ext) {
+    const StageGeo gq = stage_geo(p, K_QKV, 0);
+    const size_t pst = (size_t)p.MB * kTileRows;
+    const int len0 = m->len[0];
+    constexpr int per = HD / 2 + HD;  // the key's rotation pairs, then the value's elements
+    auto sum = [&](int row, int j) {
+      const int rb = row / kTileRows;
+      const int nc = n_contrib(rb * gq.kbs, gq.kbs, gq.T, gridDim.x);
+      const float* src = p.part_qkv + (size_t)rb * gq.kbs * pst + (size_t)j * kTileRows + row % kTileRows;
+      float acc = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < nc; ++c) acc += ldcg(src + (size_t)c * pst);
+      return acc;
+    };
+#pragma unroll 1
+    for (int idx = tid; idx < p.B * per; idx += kConsumerWarps * 32) {
+      const int j = idx / per, r = idx % per;
+      if (r < HD / 2) {
+        const int row = p.hq * HD + a.g * HD + r;
+        const float x0 = sum(row, j), x1 = sum(row + HD / 2, j);
+        const float2 cs = __ldg(p.rope + (size_t)(len0 + j) * (HD / 2) + r);
+        ext[(2 * j) * HD + r] = bf16f(f2bf(x0 * cs.x - x1 * cs.y));
+        ext[(2 * j) * HD + r + HD / 2] = bf16f(f2bf(x1 * cs.x + x0 * cs.y));
+      } else {
+        const int d = r - HD / 2;
+        ext[(2 * j + 1) * HD + d] = bf16f(f2bf(sum((p.hq + p.hkv) * HD + a.g * HD + d, j)));
+      }
+    }
+    cons_sync();
+  }
+
   // wait for the merged attention output of every (sequence, KV head) whose heads the
   // CTA's output-projection tiles read
   __device__ void wait_o_groups(int l) {
@@ -1744,6 +1797,11 @@ struct Consumer {
       // memory: qkvn[t][HD] with t < G the query heads, t = G the key, t = G + 1 the value.
       float* qkvn = red;
       if (a.tile1 > a.tile0) qkv_prologue(l, a, qkvn);
+      // multi-position steps: the unit's tiles hold some of the step's new positions
+      float* ext = qkvn + 2 * (G + 2) * HD;
+      const bool mnew = p.mpos && a.tile1 > a.tile0 && (m->len[0] + p.B - 1) / kKvTilePos >= a.tile0 &&
+                        m->len[0] / kKvTilePos < a.tile1;
+      if (mnew) new_kv_rows(a, ext);
       float q[G][DPL];
 #pragma unroll
       for (int h = 0; h < G; ++h)
@@ -1768,7 +1826,27 @@ struct Consumer {
           // This step's key and value (from the prologue; the slot's copy of the cache may predate
           // them) are written into the slot once, so the loops below read every position alike.
           const int jn = newpos - t * kKvTilePos;
-          if (jn >= 0 && jn < kKvTilePos) {  // the same for all warps (`dead` may not be)
+          if (p.mpos) {
+            // every new position up to the unit's own (causal) that falls in this tile
+            if (mnew) {
+              const int first = m->len[0] - t * kKvTilePos;
+              bool hit = false;
+#pragma unroll 1
+              for (int jj = 0; jj <= a.b; ++jj) {
+                const int r = first + jj;
+                if (r < 0 || r >= kKvTilePos) continue;
+                hit = true;
+                uint16_t* kr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + r * row_bytes);
+                uint16_t* vr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + (kKvTilePos + r) * row_bytes);
+                if (!dead)
+                  for (int d = tid; d < HD; d += kConsumerWarps * 32) {
+                    kr[d] = f2bf(ext[(2 * jj) * HD + d]);
+                    vr[d] = f2bf(ext[(2 * jj + 1) * HD + d]);
+                  }
+              }
+              if (hit) cons_sync();  // (the same for all warps)
+            }
+          } else if (jn >= 0 && jn < kKvTilePos) {  // the same for all warps (`dead` may not be)
             uint16_t* kr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + jn * row_bytes);
             uint16_t* vr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + (kKvTilePos + jn) * row_bytes);
             if (!dead)
@@ -2069,7 +2147,7 @@ struct Consumer {
               trace(8 << 4 | 1);
               cta_stamp(l, S_BARRIER);
               if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
-                for (int b = 0; b < p.B; ++b) p.lengths[p.seq0 + b] = m->len[b] + 1;
+                for (int b = 0; b < p.B; ++b) p.lengths[p.mpos ? p.seq0 : p.seq0 + b] = m->len[b] + 1;
               break;
           }
         }
@@ -2271,7 +2349,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
   if (tid < kMaxBatch) {
     int len = 0, tok = 0;
     if (tid < p.B) {
-      len = p.lengths[p.seq0 + tid];
+      len = p.mpos ? p.lengths[p.seq0] + tid : p.lengths[p.seq0 + tid];
       if (len < 0 || len >= p.max_ctx) {
         raise_err(p, kDevBadArg, 1);
         len = 0;

@@ -138,6 +138,25 @@ class Engine:
                         _stream_ptr(stream if stream is not None else torch.cuda.current_stream()))
         self._check(self.lib.dec_step_ex(self.h, C.byref(a)), "dec_step_ex")
 
+    def step_positions(self, tokens: torch.Tensor, seq: int = 0, logits: Optional[torch.Tensor] = None,
+                       next_tokens: Optional[torch.Tensor] = None, stream=None):
+        """Consecutive positions of one sequence in one launch (device int32 tokens [n])."""
+        t = tokens.to(torch.int32).contiguous()
+        self._check(self.lib.dec_step_positions(self.h, seq, t.data_ptr(), t.numel(), _ptr(logits), _ptr(next_tokens),
+                                                _stream_ptr(stream if stream is not None else torch.cuda.current_stream())),
+                    "dec_step_positions")
+
+    def verify(self, tokens: torch.Tensor, seq: int = 0, logits: Optional[torch.Tensor] = None,
+               next_tokens: Optional[torch.Tensor] = None, stream=None) -> int:
+        """Speculative verify step: tokens = [next input, drafts...]; returns the accepted count."""
+        t = tokens.to(torch.int32).contiguous()
+        acc = C.c_int32()
+        self._check(self.lib.dec_verify(self.h, seq, t.data_ptr(), t.numel(), _ptr(logits), _ptr(next_tokens),
+                                        C.byref(acc),
+                                        _stream_ptr(stream if stream is not None else torch.cuda.current_stream())),
+                    "dec_verify")
+        return acc.value
+
     def generate(self, first_tokens, n_steps: int, stream=None) -> np.ndarray:
         """Greedy decode from host tokens; returns host int32 [n_steps, batch]."""
         first = np.ascontiguousarray(np.asarray(first_tokens, np.int32).reshape(-1))
@@ -178,14 +197,14 @@ class Engine:
 
     def routing(self, layer: int):
         c = self.cfg
-        idx = np.zeros((c.max_batch, c.top_k), np.int32)
-        gates = np.zeros((c.max_batch, c.top_k), np.float32)
+        idx = np.zeros((capi.DEC_MAX_STEP_TOKENS, c.top_k), np.int32)
+        gates = np.zeros((capi.DEC_MAX_STEP_TOKENS, c.top_k), np.float32)
         self._check(self.lib.dec_get_routing(self.h, layer, idx.ctypes.data, gates.ctypes.data), "dec_get_routing")
         return idx, gates
 
     def router_logits(self, layer: int) -> np.ndarray:
         c = self.cfg
-        out = np.zeros((c.max_batch, c.n_experts), np.float32)
+        out = np.zeros((capi.DEC_MAX_STEP_TOKENS, c.n_experts), np.float32)
         self._check(self.lib.dec_get_router_logits(self.h, layer, out.ctypes.data), "dec_get_router_logits")
         return out
 
