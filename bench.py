@@ -49,6 +49,15 @@ WORKLOADS = {
     "moe8_1k_b8": ("MOE8", 1024, 256, 8),
     # small captures for ncu: two layers of the same stack + LM head
     "moe2_1k_prof": ("MOE2", 1024, 8, 1),
+    "moe2_1k_b8_prof": ("MOE2", 1024, 4, 8),
+}
+# Several positions of one sequence per launch (dec_step_positions / dec_verify):
+# name: (model, context, launches per step, positions per launch, mode)
+POSITION_WORKLOADS = {
+    # token-mode prefill of a 1024-token prompt in launches of 8 positions (128 launches)
+    "moe8_prefill_1k": ("MOE8", 1024, 128, 8, "prefill"),
+    # speculative verify steps of 8 positions (the next token + 7 drafts) at context 1024
+    "moe8_verify8_1k": ("MOE8", 1024, 64, 8, "verify"),
 }
 
 
@@ -177,6 +186,118 @@ def algorithmic_bytes(cfg, routed_distinct, ctx_lens, batch):
     kv_row = cfg.n_kv_heads * cfg.head_dim * 2 * 2  # K and V, bf16
     kv = cfg.n_layers * kv_row * sum(t + 1 for t in ctx_lens) + cfg.n_layers * kv_row * batch
     return weights + kv
+
+
+def run_positions(args):
+    """Several positions of one sequence per launch: chunked prefill or speculative verify steps.
+    value: positions per second of device time (CUDA events around the step's launches on the
+    launch stream); beside it the same positions at one per launch (the decode kernel's own rate);
+    e2e: the public call with host buffers (prefill: prompt ids host->device + dec_prefill_kv +
+    the first generated token back; verify: drafts host->device + dec_verify, whose accepted count
+    comes back to the host)."""
+    import numpy as np
+    import torch
+
+    from latency_moe_decode_gb300 import synth
+    from latency_moe_decode_gb300.engine import Engine
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    model_name, ctx, n_launch, npos, mode = POSITION_WORKLOADS[args.workload]
+    cfg = synth.MOE8.replace(max_ctx=ctx + n_launch * npos + 64, max_batch=1)
+    model = synth.gen_model(cfg, seed=0, device="cuda")
+    eng = Engine(model, max_ctx=cfg.max_ctx, max_batch=1)
+    del model
+    torch.cuda.empty_cache()
+    stream = torch.cuda.current_stream()
+    if mode == "prefill":
+        ids = synth.gen_tokens(n_launch * npos, cfg.vocab, seed=0, device="cuda")
+        start = 0
+    else:
+        k, v = synth.gen_kv(cfg, ctx, seed=1, device="cuda")
+        eng.prefill_import(k, v, seq=0)
+        del k, v
+        ids = synth.gen_tokens(n_launch * npos, cfg.vocab, seed=5, device="cuda")  # random drafts
+        start = ctx
+
+    def timed(per_launch):
+        """device seconds for the step's positions, per_launch positions per launch"""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        eng.set_length(0, start)
+        e0.record(stream)
+        for i in range(0, n_launch * npos, per_launch):
+            if mode == "verify" and per_launch > 1:
+                eng.set_length(0, start)  # every verify step starts from the same context
+            eng.step_positions(ids[i:i + per_launch], seq=0, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    for _ in range(args.warmup):
+        timed(npos)
+    eng.sync()
+    times = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            times.append(timed(npos))
+    eng.sync()
+    single = [timed(1) for _ in range(max(1, min(args.steps, 2)))]
+    eng.sync()
+    positions = n_launch * npos
+    value = positions * args.steps / sum(times)
+    # e2e through the public calls with host buffers
+    e2e_t = []
+    if mode == "prefill":
+        ids_h = ids.cpu().pin_memory()
+        nxt_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+        for _ in range(max(1, args.steps)):
+            eng.set_length(0, 0)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            d = ids_h.to("cuda", non_blocking=True)
+            eng.prefill_tokens(d, seq=0)
+            nx = torch.empty(1, dtype=torch.int32, device="cuda")
+            eng.step(tokens=d[-1:], batch=1, next_tokens=nx)
+            nxt_h.copy_(nx)
+            torch.cuda.synchronize()
+            e2e_t.append(time.perf_counter() - t0)
+        e2e = {"value": round(positions * len(e2e_t) / sum(e2e_t), 2), "unit": "prefill tokens/s",
+               "h2d_bytes_per_step": 4 * positions, "d2h_bytes_per_step": 4}
+    else:
+        drafts_h = ids.cpu().pin_memory()
+        accepted = 0
+        for _ in range(max(1, args.steps)):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(0, positions, npos):
+                eng.set_length(0, start)
+                d = drafts_h[i:i + npos].to("cuda", non_blocking=True)
+                accepted += eng.verify(d, seq=0)
+            e2e_t.append(time.perf_counter() - t0)
+        e2e = {"value": round(positions * len(e2e_t) / sum(e2e_t), 2), "unit": "verified positions/s",
+               "h2d_bytes_per_step": 4 * positions, "d2h_bytes_per_step": 4 * n_launch,
+               "mean_accepted_random_drafts": accepted / (n_launch * len(e2e_t))}
+    info = eng.info()
+    eng.close()
+    unit = "prefill tokens/s" if mode == "prefill" else "verified positions/s"
+    line = {
+        "metric": "token-mode prefill throughput" if mode == "prefill" else "speculative verify throughput",
+        "value": round(value, 2), "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(times) / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3-w/bf16-a/fp32-acc",
+        "data": "synthetic (seeded random-init FP8 weights, random ids)",
+        "config": {"workload": args.workload, "layers": cfg.n_layers, "context": ctx, "positions_per_launch": npos,
+                   "launches_per_step": n_launch, "vocab": cfg.vocab, "experts": cfg.n_experts, "top_k": cfg.top_k,
+                   "l2": "no flush: every launch streams ~1.9 GB or more of weights"},
+        "ms_per_launch": round(sum(times) / args.steps / n_launch * 1e3, 4),
+        "one_position_per_launch": {"value": round(positions * len(single) / sum(single), 2), "unit": unit,
+                                    "ms_per_launch": round(sum(single) / len(single) / positions * 1e3, 4)},
+        "e2e": e2e,
+        "gpu_launches": n_launch * args.steps,
+        "clocks": clk.summary(),
+        "engine": {"grid": info["grid"], "threads": info["threads"], "csrc_hash": csrc_hash()},
+    }
+    return line
 
 
 def cpu_model() -> str:
@@ -434,7 +555,7 @@ def main():
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="moe8_1k1k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="moe8_1k1k", choices=sorted(WORKLOADS) + sorted(POSITION_WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--kv", default="prefill", choices=["prefill", "import"],
@@ -447,7 +568,7 @@ def main():
     else:
         import __graft_entry__
         __graft_entry__.build()
-        line = run_ours(args)
+        line = run_positions(args) if args.workload in POSITION_WORKLOADS else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 
