@@ -232,11 +232,21 @@ dec_status dec_step(dec_engine* eng, const int32_t* token_ids, int32_t batch, fl
                     int32_t* next_tokens, void* stream);
 
 /* Greedy generation from HOST buffers: copies first_tokens (host int32 [batch]) to the device,
-   runs n_steps device-chained decode steps of slots [0, batch) (step i's argmax is step i+1's
-   input, with no host round trip), copies the generated tokens back to out_tokens (host int32
-   [n_steps][batch]) and synchronises. Requires vocab > 0. */
+   runs n_steps greedy decode steps of slots [0, batch) in ONE launch of a resident kernel ("Ultra-
+   High Interactivity on NVIDIA GPUs? TileRT on InferenceX", section "But What Exactly is
+   TileRT?": the host launches once and execution stays on the GPU for the decode lifecycle):
+   step i's argmax becomes step i+1's input through device memory and a flag, and the producer
+   warps stream the next step's first weights while the LM head finishes. Copies the generated
+   tokens back to out_tokens (host int32 [n_steps][batch]) and synchronises. Requires vocab > 0
+   and length + n_steps <= max_ctx for every slot (DEC_ERR_CAPACITY otherwise). (A generation of
+   more steps than the engine's epoch period takes one launch per period.) */
 dec_status dec_generate(dec_engine* eng, const int32_t* first_tokens, int32_t batch,
                         int32_t n_steps, int32_t* out_tokens, void* stream);
+
+/* The same resident generation with DEVICE buffers (first_tokens device int32 [batch],
+   out_tokens device int32 [n_steps][batch]); queued on `stream`, nothing synchronised. */
+dec_status dec_generate_device(dec_engine* eng, const int32_t* first_tokens, int32_t batch,
+                               int32_t n_steps, int32_t* out_tokens, void* stream);
 
 /* Sequence lengths (positions already in the cache). Setting a length rewinds or advances a
    slot without touching the cache contents. */

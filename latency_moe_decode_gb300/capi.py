@@ -72,6 +72,7 @@ PROTOTYPES = {
     "dec_verify": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p,
                              C.POINTER(C.c_int32), C.c_void_p]),
     "dec_generate": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
+    "dec_generate_device": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
     "dec_set_length": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "dec_get_length": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_int32)]),
     "dec_export_kv": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),

@@ -126,6 +126,11 @@ struct KParams {
   // verify steps: the number of draft tokens accepted (tokens[j + 1] == argmax after position j
   // for j < m) is written here and the slot's length set to length + m + 1
   int32_t* accepted;
+  // resident generation: nsteps > 1 decode steps in one launch, step s using epoch + s, reading
+  // its tokens at tokens + s * MB and writing the argmax at next_tokens + s * MB; each step's
+  // last LM finaliser publishes tok_flag = its epoch once the next tokens are written
+  int nsteps;
+  unsigned* tok_flag;
   float* logits;
   int32_t* next_tokens;
   uint16_t* hidden_out;

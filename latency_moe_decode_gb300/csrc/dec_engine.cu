@@ -636,6 +636,9 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     Z(p.logits_ws, sizeof(float) * MB * std::max(1, c.vocab));
     Z(p.trace, sizeof(unsigned long long) * (kTraceSlots + (size_t)kBarTrace * G));
     Z(p.layer_ts, sizeof(unsigned long long) * (c.n_layers + 2));
+    Z(p.tok_flag, sizeof(unsigned) * 32);
+    e->epoch_bufs.push_back({p.tok_flag, sizeof(unsigned) * 32});
+    p.nsteps = 1;
     Z(e->d_hist, sizeof(int32_t) * (size_t)(c.max_ctx + 1) * MB);
 #undef Z
   }
@@ -705,7 +708,8 @@ namespace {
 // consecutive positions of slot seq0; `accepted` (device) makes it a verify step. Arguments are
 // checked by the callers.
 dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t* tokens, const void* hidden_in,
-                       float* logits, int32_t* next_tokens, void* hidden_out, int32_t* accepted, cudaStream_t s) {
+                       float* logits, int32_t* next_tokens, void* hidden_out, int32_t* accepted, cudaStream_t s,
+                       int nsteps = 1) {
   const dec_model_cfg& c = e->cfg;
   int bi = 0;
   while (kBmChoices[bi] < B) ++bi;
@@ -719,15 +723,17 @@ dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t*
   p.logits = logits;
   p.next_tokens = next_tokens;
   p.hidden_out = static_cast<uint16_t*>(hidden_out);
+  p.nsteps = nsteps;
   if (dec_status os = order_on(e, s)) return os;
-  if (e->epoch >= e->epoch_limit) {
+  if (e->epoch + (unsigned)nsteps > e->epoch_limit) {
     for (const auto& b : e->epoch_bufs) {
       cudaError_t me = cudaMemsetAsync(b.first, 0, b.second, s);
       if (me != cudaSuccess) return cuda_fail(e, me, "epoch restart");
     }
     e->epoch = 0;
   }
-  p.epoch = ++e->epoch;
+  p.epoch = e->epoch + 1;
+  e->epoch += (unsigned)nsteps;
   p.ring = e->ring[bi];
   p.inflight = std::min(p.ring, kSlotsInFlight);
   p.nch = std::max(1, std::min(e->nch_max, e->grid / (B * c.n_kv_heads)));
@@ -737,7 +743,7 @@ dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t*
   if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaLaunchCooperativeKernel");
   if (mpos) e->lengths[seq0] += B;
   else
-    for (int b = 0; b < B; ++b) e->lengths[seq0 + b] += 1;
+    for (int b = 0; b < B; ++b) e->lengths[seq0 + b] += nsteps;
   e->launches += 1;
   return DEC_OK;
 }
@@ -930,21 +936,55 @@ dec_status dec_prefill_kv_noalloc(dec_engine* e, const dec_ctx* x) {
   return check_device_status(e);
 }
 
+dec_status dec_generate_device(dec_engine* e, const int32_t* first, int32_t batch, int32_t n_steps, int32_t* out,
+                               void* stream) {
+  if (!e || !first || !out || batch < 1 || n_steps < 0) return DEC_ERR_ARG;
+  if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  if (dec_status ds = check_device(e)) return ds;
+  const dec_model_cfg& c = e->cfg;
+  if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "generate needs an LM head");
+  if (batch > c.max_batch || n_steps > c.max_ctx) return fail(e, DEC_ERR_ARG, "batch or n_steps too large");
+  for (int b = 0; b < batch; ++b)
+    if (e->lengths[b] + n_steps > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "sequence would pass max_ctx");
+  if (n_steps == 0) return DEC_OK;
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
+  if (dec_status os = order_on(e, s)) return os;  // d_hist may still be read by earlier work
+  const int MB = e->base.MB;
+  DEC_CUDA(cudaMemcpy2DAsync(e->d_hist, sizeof(int32_t) * MB, first, sizeof(int32_t) * batch, sizeof(int32_t) * batch,
+                             1, cudaMemcpyDeviceToDevice, s));
+  // resident steps: one launch runs up to epoch_limit steps (normally all of them)
+  for (int i = 0; i < n_steps;) {
+    const int n = std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
+    dec_status st = launch_step(e, batch, 0, false, e->d_hist + (size_t)i * MB, nullptr, nullptr,
+                                e->d_hist + (size_t)(i + 1) * MB, nullptr, nullptr, s, n);
+    if (st != DEC_OK) return st;
+    i += n;
+  }
+  DEC_CUDA(cudaMemcpy2DAsync(out, sizeof(int32_t) * batch, e->d_hist + MB, sizeof(int32_t) * MB,
+                             sizeof(int32_t) * batch, n_steps, cudaMemcpyDeviceToDevice, s));
+  return DEC_OK;
+}
+
 dec_status dec_generate(dec_engine* e, const int32_t* first, int32_t batch, int32_t n_steps, int32_t* out,
                         void* stream) {
   if (!e || !first || !out || batch < 1 || n_steps < 0) return DEC_ERR_ARG;
   if (e->poisoned) return fail(e, DEC_ERR_POISONED, "engine poisoned");
+  if (dec_status ds = check_device(e)) return ds;
   const dec_model_cfg& c = e->cfg;
   if (c.vocab == 0) return fail(e, DEC_ERR_ARG, "generate needs an LM head");
   if (batch > c.max_batch || n_steps > c.max_ctx) return fail(e, DEC_ERR_ARG, "batch or n_steps too large");
-  if (dec_status ds = check_device(e)) return ds;
+  for (int b = 0; b < batch; ++b)
+    if (e->lengths[b] + n_steps > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "sequence would pass max_ctx");
   cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
   if (dec_status os = order_on(e, s)) return os;  // d_hist may still be read by earlier steps
-  const int MB = c.max_batch;
+  const int MB = e->base.MB;
   DEC_CUDA(cudaMemcpyAsync(e->d_hist, first, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s));
-  for (int i = 0; i < n_steps; ++i) {
-    dec_status st = dec_step(e, e->d_hist + (size_t)i * MB, batch, nullptr, e->d_hist + (size_t)(i + 1) * MB, s);
+  for (int i = 0; i < n_steps;) {
+    const int n = std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
+    dec_status st = launch_step(e, batch, 0, false, e->d_hist + (size_t)i * MB, nullptr, nullptr,
+                                e->d_hist + (size_t)(i + 1) * MB, nullptr, nullptr, s, n);
     if (st != DEC_OK) return st;
+    i += n;
   }
   if (n_steps > 0)
     DEC_CUDA(cudaMemcpy2DAsync(out, sizeof(int32_t) * batch, e->d_hist + MB, sizeof(int32_t) * MB,

@@ -314,13 +314,13 @@ struct TilePos {
 struct AttnUnit {
   int b, g, c, tile0, tile1, T;
 };
-__device__ __forceinline__ AttnUnit attn_unit(const KParams& p, const Misc* m, int u) {
+__device__ __forceinline__ AttnUnit attn_unit(const KParams& p, const Misc* m, int u, int soff) {
   AttnUnit a;
   int per_b = p.hkv * p.nch;
   a.b = u / per_b;
   a.g = (u / p.nch) % p.hkv;
   a.c = u % p.nch;
-  a.T = m->len[a.b] + 1;
+  a.T = m->len[a.b] + soff + 1;  // (m->len: lengths at the launch; soff: resident steps done)
   int ntile = (a.T + kKvTilePos - 1) / kKvTilePos;
   int tpc = (ntile + p.nch - 1) / p.nch;
   a.tile0 = min(ntile, a.c * tpc);
@@ -356,6 +356,8 @@ struct Producer {
   unsigned llap = 0;    // its lap (landed / ring)
   bool dead = false;
   int stamp = 0;
+  int soff = 0;       // resident steps done in this launch
+  unsigned lay = 0;   // layers done in this launch (the routing barrier's phase)
 
   // CTA 0's producer records (code, %globaltimer) pairs in the last kProducerTrace words:
   // code = what << 4 | event, event 0 = first copy of a stage issued, 1 = last copy issued
@@ -479,10 +481,33 @@ struct Producer {
 
   __device__ void issue_attn(int l) {
     if (dead) return;
+    if (soff > 0) {
+      // Resident steps: the KV cache is not static data. The previous step's keys and values
+      // (written by whichever CTA held their position) must be in place before this step's KV
+      // tiles are copied, and the producer may otherwise run steps ahead of them: wait (bounded)
+      // for the previous step's token flag, published after all of that step's work, then order
+      // the copies (async proxy) after the writes it made visible.
+      const unsigned want = p.epoch + (unsigned)soff - 1u;
+      const unsigned long long t0 = gtimer();
+      for (unsigned it = 1; ld_acquire(p.tok_flag) < want; ++it) {
+        if ((it & 15u) == 0) {
+          if (aborted(p)) {
+            dead = true;
+            return;
+          }
+          if (gtimer() - t0 > p.timeout_ns) {
+            raise_err(p, kDevTimeout, 32);
+            dead = true;
+            return;
+          }
+        }
+      }
+      fence_proxy_async_global();
+    }
     const int NU = p.B * p.hkv * p.nch;
     const unsigned row_bytes = HD * 2;
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
-      AttnUnit a = attn_unit(p, m, u);
+      AttnUnit a = attn_unit(p, m, u, soff);
       for (int t = a.tile0; t < a.tile1; ++t) {
         int slot;
         if (!claim(slot, false)) return;
@@ -510,7 +535,7 @@ struct Producer {
   __device__ bool routing(int l, int& U, int* elist) {
     if (dead) return false;
     trace(9 << 4);
-    if (!mbar_wait(&m->rt_bar, (unsigned)l & 1u, p, 11)) {
+    if (!mbar_wait(&m->rt_bar, lay & 1u, p, 11)) {
       dead = true;
       return false;
     }
@@ -542,6 +567,8 @@ struct Producer {
     pol_stream = l2_policy(true);
     pol_kv = l2_policy(false);
 #pragma unroll 1
+    for (soff = 0; soff < p.nsteps && !dead; ++soff)
+#pragma unroll 1
     for (int l = 0; l <= p.L && !dead; ++l) {
       const bool lm = l == p.L;
 #pragma unroll 1
@@ -566,6 +593,7 @@ struct Producer {
         }
         if (kind >= 0) issue_gemv(kind, lm ? 0 : l, U, elist);
       }
+      if (!lm) ++lay;
     }
     // every copy this thread issued lands before it exits: consumers that gave up (an abort
     // elsewhere) no longer wait for their slots, and the CTA's shared memory must outlive them
@@ -598,6 +626,8 @@ struct Consumer {
   bool range_bad = false;  // (CUDA-core path) an activation staged as f16 was outside its range
   // tensor-core tiles: tiles whose products were added so far in this step (the sequence picks
   // the TMEM accumulator and its barriers' phases), the TMEM base, the B operand layout
+  unsigned ep = 0;    // this step's epoch (resident steps: the launch's epoch + steps done)
+  int soff = 0;       // resident steps done in this launch
   unsigned gseq = 0;  // groups of tiles handed over so far (slot of TMEM slices, barrier phases)
   uint32_t tmem = 0;
   BGeo bg;
@@ -667,13 +697,13 @@ struct Consumer {
     if (!direct && !from_o && l_src > 0) {
       // the previous layer's output rows (published by the down projection's finalisers)
       const unsigned* f = p.x_flag + (size_t)(l_src - 1) * p.n_rb_d;
-      cta_wait_all(p.n_rb_d, [&](int rb) { return WaitCond{f + rb, p.epoch}; }, 22);
+      cta_wait_all(p.n_rb_d, [&](int rb) { return WaitCond{f + rb, ep}; }, 22);
       if (blockIdx.x == 0 && tid == 0) p.layer_ts[l_src] = gtimer();
     }
     if (from_o) {
       const int* cnt = p.cnt_o + (size_t)l_src * p.n_rb_d;
       cta_wait_all(p.n_rb_d, [&](int rb) {
-        return count_reached(cnt + rb, (int)p.epoch * go.kbs);
+        return count_reached(cnt + rb, (int)ep * go.kbs);
       }, 18);
       // Every output-projection tile has arrived, and each waited for the attention merges it
       // reads (together: all of layer l_src's), each merge having waited for all of its chunks.
@@ -1250,7 +1280,7 @@ struct Consumer {
     const StageGeo g = stage_geo(p, K_ROUTER, 0);
     const int nc = n_contrib(0, g.kbs, g.T, gridDim.x);
     const int* cnt = p.cnt_router + l;
-    cta_wait_all(1, [&](int) { return count_reached(cnt, (int)p.epoch * g.kbs); }, 19);
+    cta_wait_all(1, [&](int) { return count_reached(cnt, (int)ep * g.kbs); }, 19);
     float* tmp = red;                                        // [BM][128] logits
     int* mark = reinterpret_cast<int*>(tmp + BM * kTileRows);  // [128] rank + 1 of expert e
     int* sel = mark + kMaxExperts;                              // [BM][16]
@@ -1484,7 +1514,7 @@ struct Consumer {
         }
         // the next layer's input row block is final
         cons_sync();
-        if (tid == kPubThread) st_release(p.x_flag + (size_t)l * p.n_rb_d + grp, p.epoch);
+        if (tid == kPubThread) st_release(p.x_flag + (size_t)l * p.n_rb_d + grp, ep);
         break;
       }
       default: {  // LM head
@@ -1534,7 +1564,7 @@ struct Consumer {
             for (int b = 0; b < p.B; ++b) {
               unsigned long long key = atomicExch(p.amax + b, 0ull);
               const int tok = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
-              if (p.next_tokens) p.next_tokens[b] = tok;
+              if (p.next_tokens) p.next_tokens[(size_t)soff * p.MB + b] = tok;
               if (run && b + 1 < p.B && tok == p.tokens[b + 1]) ++acc;
               else run = false;
             }
@@ -1543,6 +1573,8 @@ struct Consumer {
               p.lengths[p.seq0] = m->len[0] + acc + 1;
             }
             atomicExch(p.cnt_lm_done, 0);
+            // resident steps: the next step's tokens are written (the release orders them)
+            if (p.nsteps > 1) st_release(p.tok_flag, ep);
           }
         }
         break;
@@ -1640,7 +1672,7 @@ struct Consumer {
       const int* cnt = p.cnt_qkv + (size_t)l * p.n_rb_qkv;
       cta_wait_all(qn + kn + vn, [&](int i) {
         const int rb = i < qn ? qa + i : (i < qn + kn ? ka + i - qn : va + i - qn - kn);
-        return count_reached(cnt + rb, (int)p.epoch * gq.kbs);
+        return count_reached(cnt + rb, (int)ep * gq.kbs);
       }, 13);
     }
     // Each thread sums the contributor partials of its NPT values. All loads of a batch of five
@@ -1650,7 +1682,7 @@ struct Consumer {
     constexpr int NV_ = (G + 2) * HD;
     constexpr int NPT = (NV_ + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
     float* raw = qkvn + NV_;
-    const int pos = m->len[a.b];
+    const int pos = m->len[a.b] + soff;
     const size_t pst = (size_t)p.MB * kTileRows;
     const float* pbase[NPT];
     int pnc[NPT], ncmax = 0;
@@ -1713,7 +1745,7 @@ struct Consumer {
   __device__ void new_kv_rows(const AttnUnit& a, float* ext) {
     const StageGeo gq = stage_geo(p, K_QKV, 0);
     const size_t pst = (size_t)p.MB * kTileRows;
-    const int len0 = m->len[0];
+    const int len0 = m->len[0] + soff;
     constexpr int per = HD / 2 + HD;  // the key's rotation pairs, then the value's elements
     auto sum = [&](int row, int j) {
       const int rb = row / kTileRows;
@@ -1775,7 +1807,7 @@ struct Consumer {
     cta_wait_all(n, [&](int j) {
       const int v = (v0 + j) % nv;
       const int slot = v < U ? v : p.umax;
-      return count_reached(p.h_cnt + (size_t)l * (p.umax + 1) + slot, (int)p.epoch * p.n_rb_gu);
+      return count_reached(p.h_cnt + (size_t)l * (p.umax + 1) + slot, (int)ep * p.n_rb_gu);
     }, 17);
   }
 
@@ -1792,15 +1824,15 @@ struct Consumer {
     const int NU = p.B * p.hkv * p.nch;
     trace(7 << 4);
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
-      AttnUnit a = attn_unit(p, m, u);
+      AttnUnit a = attn_unit(p, m, u, soff);
       // The group's q heads, k and v for this token, rotated and rounded to bf16, in shared
       // memory: qkvn[t][HD] with t < G the query heads, t = G the key, t = G + 1 the value.
       float* qkvn = red;
       if (a.tile1 > a.tile0) qkv_prologue(l, a, qkvn);
       // multi-position steps: the unit's tiles hold some of the step's new positions
       float* ext = qkvn + 2 * (G + 2) * HD;
-      const bool mnew = p.mpos && a.tile1 > a.tile0 && (m->len[0] + p.B - 1) / kKvTilePos >= a.tile0 &&
-                        m->len[0] / kKvTilePos < a.tile1;
+      const bool mnew = p.mpos && a.tile1 > a.tile0 && (m->len[0] + soff + p.B - 1) / kKvTilePos >= a.tile0 &&
+                        (m->len[0] + soff) / kKvTilePos < a.tile1;
       if (mnew) new_kv_rows(a, ext);
       float q[G][DPL];
 #pragma unroll
@@ -1829,7 +1861,7 @@ struct Consumer {
           if (p.mpos) {
             // every new position up to the unit's own (causal) that falls in this tile
             if (mnew) {
-              const int first = m->len[0] - t * kKvTilePos;
+              const int first = m->len[0] + soff - t * kKvTilePos;
               bool hit = false;
 #pragma unroll 1
               for (int jj = 0; jj <= a.b; ++jj) {
@@ -2055,6 +2087,23 @@ struct Consumer {
     }
     int U = 0;
 #pragma unroll 1
+    for (soff = 0; soff < p.nsteps; ++soff) {
+    ep = p.epoch + (unsigned)soff;
+    if (soff > 0) {
+      // resident steps: this step's tokens are the previous step's argmax (its last LM finaliser
+      // publishes the flag after writing them)
+      cta_wait_all(1, [&](int) { return WaitCond{p.tok_flag, ep - 1u}; }, 26);
+      if (tid < p.B) {
+        int tok = __ldcg(p.tokens + (size_t)soff * p.MB + tid);
+        if (tok < 0 || tok >= p.V) {
+          raise_err(p, kDevBadArg, 2);
+          tok = 0;
+        }
+        m->tok[tid] = tok;
+      }
+      cons_sync();
+    }
+#pragma unroll 1
     for (int l = 0; l <= p.L; ++l) {
       const bool lm = l == p.L;
       if (lm && p.V == 0) break;
@@ -2147,7 +2196,7 @@ struct Consumer {
               trace(8 << 4 | 1);
               cta_stamp(l, S_BARRIER);
               if (l == 0 && blockIdx.x == 0 && tid == 0 && !dead)
-                for (int b = 0; b < p.B; ++b) p.lengths[p.mpos ? p.seq0 : p.seq0 + b] = m->len[b] + 1;
+                for (int b = 0; b < p.B; ++b) p.lengths[p.mpos ? p.seq0 : p.seq0 + b] = m->len[b] + soff + 1;
               break;
           }
         }
@@ -2168,6 +2217,7 @@ struct Consumer {
         }
         if (kind >= 0) gemv_stage(kind, lm ? 0 : l, lm ? 0 : U);
       }
+    }
     }
     trace(10 << 4 | 1);
     if (blockIdx.x == 0 && tid == 0) p.layer_ts[p.L + 1] = gtimer();
@@ -2205,6 +2255,8 @@ struct MmaIssuer {
   bool dead = false;
   uint32_t tmem = 0;
   BGeo bg;
+  int soff = 0;      // resident steps done in this launch
+  unsigned lay = 0;  // layers done in this launch (the routing barrier's phase)
 
   __device__ MmaIssuer(const KParams& p_, uint8_t* r, uint64_t* f, uint64_t* me, Misc* m_, const uint8_t* x)
       : p(p_), ring(r), full(f), mempty(me), m(m_), xsb(x) {
@@ -2277,6 +2329,8 @@ struct MmaIssuer {
   // expert, routed gate/up, down projections; then the LM head
   __device__ void run() {
 #pragma unroll 1
+    for (soff = 0; soff < p.nsteps; ++soff)
+#pragma unroll 1
     for (int l = 0; l <= p.L; ++l) {
       if (l == p.L) {
         if (p.V > 0) gemv(K_LM, 0);
@@ -2285,7 +2339,7 @@ struct MmaIssuer {
       gemv(K_QKV, 0);
       int items = 0;
       for (int u = blockIdx.x; u < p.B * p.hkv * p.nch; u += gridDim.x) {
-        const AttnUnit a = attn_unit(p, m, u);
+        const AttnUnit a = attn_unit(p, m, u, soff);
         items += a.tile1 - a.tile0;
       }
       skip(items);
@@ -2295,12 +2349,13 @@ struct MmaIssuer {
         gemv(K_SHGU, 0);
       } else {
         gemv(K_ROUTER, 0);
-        if (!dead && !mbar_wait(&m->rt_bar, (unsigned)l & 1u, p, 29)) dead = true;
+        if (!dead && !mbar_wait(&m->rt_bar, lay & 1u, p, 29)) dead = true;
         U = min(max(m->U, 0), p.umax);
         if (p.nsh) gemv(K_SHGU, 0);
         gemv(K_RTGU, U);
       }
       gemv(K_D, U);
+      ++lay;
     }
     // the last MMAs complete before the consumers may free TMEM (bounded wait)
     if (gseq > 0) {

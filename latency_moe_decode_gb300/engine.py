@@ -171,6 +171,13 @@ class Engine:
         self._check(self.lib.dec_generate(self.h, first.data_ptr(), first.numel(), out.shape[0], out.data_ptr(),
                                           _stream_ptr(stream)), "dec_generate")
 
+    def generate_device(self, first: torch.Tensor, out: torch.Tensor, stream=None):
+        """Resident greedy generation with device tensors: first int32 [batch], out int32
+        [n_steps, batch]; one launch, queued on the stream, not synchronised."""
+        self._check(self.lib.dec_generate_device(self.h, first.data_ptr(), first.numel(), out.shape[0], out.data_ptr(),
+                                                 _stream_ptr(stream if stream is not None else torch.cuda.current_stream())),
+                    "dec_generate_device")
+
     def set_length(self, seq: int, length: int):
         self._check(self.lib.dec_set_length(self.h, seq, length), "dec_set_length")
 
