@@ -78,7 +78,7 @@ typedef struct {
   int32_t dense_ffn;  /* dense SwiGLU width (multiple of 128) when n_experts == 0, else 0 */
   int32_t vocab;      /* 0: headless stack */
   int32_t max_ctx;    /* KV positions per sequence */
-  int32_t max_batch;  /* sequences decoded together, 1..8 */
+  int32_t max_batch;  /* sequences decoded together, 1..64 (above 8: the wide kernels) */
   float rms_eps;
   float rope_theta;
 } dec_model_cfg;
@@ -191,7 +191,12 @@ dec_status dec_prefill_kv_noalloc(dec_engine* eng, const dec_ctx* ctx);
      hidden_out  device bf16 [batch][hidden]  final residual stream (before the final norm),
                                               may be NULL
    batch == 0 is a no-op. Errors: DEC_ERR_ARG, DEC_ERR_CAPACITY (a length would pass max_ctx),
-   DEC_ERR_POISONED, DEC_ERR_CUDA (launch failure). */
+   DEC_ERR_POISONED, DEC_ERR_CUDA (launch failure).
+   Batches of 9 .. 64 (engines built with max_batch > 8) run the wide kernel: every GEMV on the
+   tensor cores with all of the step's tokens as the N dimension, tokens grouped per routed expert
+   (an expert's products kept for the tokens routed to it), phases separated by grid barriers
+   ("vLLM's Kimi K3 Backend Hits 842 Tokens per Second", section "A narrow deployment lane":
+   decode batches up to 64). Same arguments, results and errors. */
 typedef struct {
   const int32_t* tokens;
   const void* hidden_in;
@@ -239,7 +244,8 @@ dec_status dec_step(dec_engine* eng, const int32_t* token_ids, int32_t batch, fl
    warps stream the next step's first weights while the LM head finishes. Copies the generated
    tokens back to out_tokens (host int32 [n_steps][batch]) and synchronises. Requires vocab > 0
    and length + n_steps <= max_ctx for every slot (DEC_ERR_CAPACITY otherwise). (A generation of
-   more steps than the engine's epoch period takes one launch per period.) */
+   more steps than the engine's epoch period takes one launch per period; batches above 8 take
+   one wide-kernel launch per step, the tokens still chained on the device.) */
 dec_status dec_generate(dec_engine* eng, const int32_t* first_tokens, int32_t batch,
                         int32_t n_steps, int32_t* out_tokens, void* stream);
 
@@ -276,14 +282,14 @@ typedef struct {
 dec_status dec_get_info(dec_engine* eng, dec_info* out);
 
 /* Routing of the most recent step at one layer (MoE models): copies the selected experts
-   (score-descending) into host idx [DEC_MAX_STEP_TOKENS][top_k] and their normalised gates into
-   host gates [DEC_MAX_STEP_TOKENS][top_k], one row per token of the step; rows >= the step's
-   token count are stale. Synchronises. */
+   (score-descending) into host idx [R][top_k] and their normalised gates into host gates
+   [R][top_k], R = max(DEC_MAX_STEP_TOKENS, max_batch), one row per token of the step; rows >=
+   the step's token count are stale. Synchronises. */
 dec_status dec_get_routing(dec_engine* eng, int32_t layer, int32_t* idx, float* gates);
 
 /* The router logits (fp32, before the sigmoid) the most recent step selected from at one layer
-   (MoE models): host logits [DEC_MAX_STEP_TOKENS][n_experts]; rows >= the step's token count
-   are stale. With
+   (MoE models): host logits [R][n_experts], R = max(DEC_MAX_STEP_TOKENS, max_batch); rows >=
+   the step's token count are stale. With
    dec_get_routing this lets a caller check that a selection is the top_k of its own logits
    (ties to the lower expert index). Synchronises. */
 dec_status dec_get_router_logits(dec_engine* eng, int32_t layer, float* logits);

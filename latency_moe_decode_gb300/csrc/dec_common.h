@@ -22,7 +22,8 @@ constexpr int kSlotsInFlight = 2;                     // copies a CTA keeps in f
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + the producer warp and the MMA warp
 constexpr int kKvTilePos = 64;                       // KV positions per ring slot
-constexpr int kMaxBatch = 8;
+constexpr int kMaxBatch = 8;                         // tokens of one step of decode_step_kernel
+constexpr int kWideMax = 64;                         // tokens of one step of the wide kernel (9 .. 64)
 constexpr int kMaxHidden = 4096;                     // hidden sizes the kernel handles
 constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
 #ifndef DEC_STAMPS
@@ -82,6 +83,8 @@ struct KParams {
   uint16_t* vc;
   int32_t* lengths;    // [slots]
   int slots;           // KV cache slots (sequences); MB is the token capacity of one step
+  int rows;            // max(kMaxBatch, slots): token rows of the routing records and of the
+                       // per-step token arrays of a resident generation
   // activations
   uint16_t* xbuf;   // [2][MB][d]
   uint16_t* xmid;   // [MB][d]
@@ -105,10 +108,10 @@ struct KParams {
   float* attn_part;
   int* attn_cnt;  // [L][MB][hkv] chunk partials published (zero between launches)
   // routing of each layer, written by CTA 0 for inspection (every CTA computes it itself)
-  int* rt_idx;        // [L][MB][topk] selections (score-descending)
-  float* rt_topk_gate;// [L][MB][topk]
-  float* rt_logits;   // [L][MB][E] router logits the selection was made from
-  unsigned long long* amax;  // [MB] packed (ordered logit, ~id) maxima
+  int* rt_idx;        // [L][rows][topk] selections (score-descending)
+  float* rt_topk_gate;// [L][rows][topk]
+  float* rt_logits;   // [L][rows][E] router logits the selection was made from
+  unsigned long long* amax;  // [rows] packed (ordered logit, ~id) maxima
   int* err;           // device status word
   float* logits_ws;   // [MB][V] when the caller gives no logits buffer
   unsigned long long* trace;  // [kTraceSlots + kBarTrace * grid]
@@ -127,7 +130,7 @@ struct KParams {
   // for j < m) is written here and the slot's length set to length + m + 1
   int32_t* accepted;
   // resident generation: nsteps > 1 decode steps in one launch, step s using epoch + s, reading
-  // its tokens at tokens + s * MB and writing the argmax at next_tokens + s * MB; each step's
+  // its tokens at tokens + s * rows and writing the argmax at next_tokens + s * rows; each step's
   // last LM finaliser publishes tok_flag = its epoch once the next tokens are written
   int nsteps;
   unsigned* tok_flag;
@@ -136,6 +139,31 @@ struct KParams {
   uint16_t* hidden_out;
   unsigned epoch;
   unsigned long long timeout_ns;
+};
+
+// The wide kernel's own buffers (steps of 9 .. 64 tokens). Every GEMV stage input is kept in
+// global memory as the tensor cores' B operand: per k block of 128 activations one block of
+// nr rows x 128 bytes (token t's two E4M3 pieces in rows 2t and 2t + 1, canonical K-major layout
+// of 8-row x 16-byte core matrices; nr = the kernel's row count, 32, 64 or 128) and one exponent
+// byte per token (the pieces encode x * 2^a). The producer copies a tile's block into the ring
+// slot beside the weight tile.
+struct WideParams {
+  const uint8_t* pb;  // the B operand arena (pbx, pbo, pbh), for the copies' bounds checks
+  unsigned long long pb_bytes;
+  uint8_t* pbx;       // [kb_d][nr * 128]: the normalised input of a q/k/v, router, gate/up or LM stage
+  uint8_t* pbo;       // [kb_o][nr * 128]: the attention output
+  uint8_t* pbh;       // [U + n_shared][kb_i][nr * 128]: the SwiGLU rows of each expert slot
+  int8_t* exx;        // [kb_d][kWideMax] exponents of pbx
+  int8_t* exo;        // [kb_o][kWideMax]
+  int8_t* exh;        // [U + n_shared][kb_i][kWideMax]
+  int32_t* sel;       // [kWideMax][topk] this layer's selected experts
+  float* selg;        // [kWideMax][topk] and their normalised gates
+  unsigned* bar;      // grid barrier counter: zero at launch, + 1 per CTA and barrier
+  float* attn_part;   // [MB][hkv][nch][group][hd + 2] chunk states (split context)
+  uint16_t* xbuf;     // [MB][d] the layer input (residual stream)
+  uint16_t* xmid;     // [MB][d] x + attention output projection
+  int nch;            // attention chunks per (sequence, KV head)
+  int hmax;           // expert slots pbh / exh hold (at least U + n_shared)
 };
 
 }  // namespace dec

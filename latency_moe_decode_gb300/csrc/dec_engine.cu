@@ -13,6 +13,7 @@
 
 #include "dec.h"
 #include "dec_kernel.cuh"
+#include "dec_wide_host.h"
 
 using namespace dec;
 
@@ -136,6 +137,14 @@ struct dec_engine {
   int smem[4] = {0, 0, 0, 0};
   int ring[4] = {0, 0, 0, 0};
   int nch_max = 1;
+  int rows = kMaxBatch;  // max(kMaxBatch, max_batch): routing records and per-step token rows
+  // steps of more than kMaxBatch tokens: the wide kernels (B operand blocks of 32, 64, 128 rows
+  // for up to 16, 32, 64 tokens), their parameters and buffers
+  KParams wbase{};
+  WideParams wp{};
+  wide::WideKernelFn wkern[3] = {nullptr, nullptr, nullptr};
+  int wsmem[3] = {0, 0, 0}, wring[3] = {0, 0, 0};
+  int wnch_max = 1;
   std::vector<int32_t> lengths;
   unsigned epoch = 0;
   // Counters that grow across steps (each arrival adds its tile count, at most kbs per row block
@@ -366,7 +375,7 @@ dec_status dec_validate_cfg(const dec_model_cfg* c) {
   } else if (c->dense_ffn % 128 != 0) {
     return DEC_ERR_UNSUPPORTED;
   }
-  if (c->max_batch > kMaxBatch || c->n_kv_heads > 64 || c->hidden > kMaxHidden) return DEC_ERR_UNSUPPORTED;
+  if (c->max_batch > kWideMax || c->n_kv_heads > 64 || c->hidden > kMaxHidden) return DEC_ERR_UNSUPPORTED;
   return DEC_OK;
 }
 
@@ -427,6 +436,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
   p.max_ctx = c.max_ctx;
   p.MB = kMaxBatch;  // tokens one step can take: sequences side by side, or positions of one
   p.slots = c.max_batch;
+  e->rows = std::max(kMaxBatch, c.max_batch);
+  p.rows = e->rows;
   p.eps = c.rms_eps;
   p.kb_d = c.hidden / kTileK;
   p.kb_o = c.n_heads * c.head_dim / kTileK;
@@ -628,18 +639,19 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
       const long v = atol(el);
       if (v >= 1 && (unsigned long)v < e->epoch_limit) e->epoch_limit = (unsigned)v;
     }
-    Z(p.rt_idx, sizeof(int) * c.n_layers * MB * std::max(1, c.top_k));
-    Z(p.rt_topk_gate, sizeof(float) * c.n_layers * MB * std::max(1, c.top_k));
-    Z(p.rt_logits, sizeof(float) * c.n_layers * MB * std::max(1, c.n_experts));
-    Z(p.amax, sizeof(unsigned long long) * MB);
+    const size_t RW = (size_t)e->rows;
+    Z(p.rt_idx, sizeof(int) * c.n_layers * RW * std::max(1, c.top_k));
+    Z(p.rt_topk_gate, sizeof(float) * c.n_layers * RW * std::max(1, c.top_k));
+    Z(p.rt_logits, sizeof(float) * c.n_layers * RW * std::max(1, c.n_experts));
+    Z(p.amax, sizeof(unsigned long long) * RW);
     Z(p.err, sizeof(int) * 32);
-    Z(p.logits_ws, sizeof(float) * MB * std::max(1, c.vocab));
+    Z(p.logits_ws, sizeof(float) * RW * std::max(1, c.vocab));
     Z(p.trace, sizeof(unsigned long long) * (kTraceSlots + (size_t)kBarTrace * G));
     Z(p.layer_ts, sizeof(unsigned long long) * (c.n_layers + 2));
     Z(p.tok_flag, sizeof(unsigned) * 32);
     e->epoch_bufs.push_back({p.tok_flag, sizeof(unsigned) * 32});
     p.nsteps = 1;
-    Z(e->d_hist, sizeof(int32_t) * (size_t)(c.max_ctx + 1) * MB);
+    Z(e->d_hist, sizeof(int32_t) * (size_t)(c.max_ctx + 1) * RW);
 #undef Z
   }
 
@@ -693,6 +705,97 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     const char* sk = getenv("DEC_TEST_SKIP_ARRIVAL");
     p.test_skip = (sk && atoi(sk) == 1) ? 1 : 0;
   }
+  // ---- the wide kernels: steps of more than kMaxBatch tokens (own partial sums with a token
+  // stride of max_batch, B operand blocks, exchange buffers)
+  if (c.max_batch > kMaxBatch) {
+    KParams& w = e->wbase;
+    w = p;
+    w.MB = c.max_batch;
+    const int umax_w = dense ? 0 : std::min(c.n_experts, c.max_batch * c.top_k);
+    w.umax = umax_w;
+    WideParams& wp = e->wp;
+    wp.hmax = umax_w + p.nsh;
+    const int nr_max = c.max_batch <= 16 ? 32 : c.max_batch <= 32 ? 64 : 128;
+    auto wz = [&](auto** ptr, size_t bytes) -> dec_status {
+      dec_status s2 = dalloc(e, ptr, bytes, &e->ws_bytes);
+      if (s2 == DEC_OK && cudaMemsetAsync(*ptr, 0, bytes ? bytes : 16, e->stream) != cudaSuccess) s2 = DEC_ERR_CUDA;
+      return s2;
+    };
+#define WZ(ptr, bytes) \
+  if ((st = wz(&(ptr), (bytes))) != DEC_OK) return bail(st);
+    {
+      const long long t_max = std::max((long long)(umax_w + p.nsh) * p.n_rb_d * p.kb_i,
+                                       (long long)std::max(1, umax_w) * p.n_rb_gu * p.kb_d);
+      if ((t_max + 1) * G >= (1LL << 31)) return bail(fail(e, DEC_ERR_UNSUPPORTED, "too many tiles in one stage"));
+      // the exponents a CTA's down tiles read (the expert slots its range spans) fit its table
+      for (int U = 0; U <= umax_w; ++U) {
+        const int tpe = p.n_rb_d * p.kb_i, T = (U + p.nsh) * tpe;
+        for (int cta = 0; cta < G; ++cta) {
+          const int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
+          if (t1 > t0 && ((t1 - 1) / tpe - t0 / tpe + 1) * p.kb_i > kMaxKb)
+            return bail(fail(e, DEC_ERR_UNSUPPORTED, "down projection too narrow for the exponent table"));
+        }
+      }
+    }
+    const size_t PBS = (size_t)nr_max * 128;
+    const size_t nbx = p.kb_d, nbo = p.kb_o, nbh = (size_t)wp.hmax * p.kb_i;
+    uint8_t* pb = nullptr;
+    WZ(pb, (nbx + nbo + nbh) * PBS);
+    wp.pb = pb;
+    wp.pb_bytes = (nbx + nbo + nbh) * PBS;
+    wp.pbx = pb;
+    wp.pbo = pb + nbx * PBS;
+    wp.pbh = pb + (nbx + nbo) * PBS;
+    int8_t* ex = nullptr;
+    WZ(ex, (nbx + nbo + nbh) * kWideMax);
+    wp.exx = ex;
+    wp.exo = ex + nbx * kWideMax;
+    wp.exh = ex + (nbx + nbo) * kWideMax;
+    WZ(wp.sel, sizeof(int32_t) * kWideMax * std::max(1, c.top_k));
+    WZ(wp.selg, sizeof(float) * kWideMax * std::max(1, c.top_k));
+    WZ(wp.bar, sizeof(unsigned) * 32);
+    e->wnch_max = std::max(1, G / ((kMaxBatch + 1) * c.n_kv_heads));
+    WZ(wp.attn_part, sizeof(float) * (size_t)w.MB * c.n_kv_heads * e->wnch_max * e->group * (c.head_dim + 2));
+    WZ(wp.xbuf, (size_t)w.MB * c.hidden * 2);
+    WZ(wp.xmid, (size_t)w.MB * c.hidden * 2);
+    // partial sums: [segment][slot][MB][128] fp32 (routed stages: the largest over the expert count)
+    const size_t fb = sizeof(float) * (size_t)w.MB * kTileRows;
+    auto plain = [&](int kind, int n_rb) {
+      return (size_t)std::max(1, n_rb) * wide::stage_slots(w, kind, 0, G);
+    };
+    size_t n_rtgu = 1, n_d = 1;
+    for (int U = 1; U <= std::max(1, umax_w); ++U)
+      n_rtgu = std::max(n_rtgu, (size_t)U * p.n_rb_gu * wide::stage_slots(w, K_RTGU, U, G));
+    for (int U = 0; U <= umax_w; ++U)
+      n_d = std::max(n_d, (size_t)(U + p.nsh) * p.n_rb_d * wide::stage_slots(w, K_D, U, G));
+    WZ(w.part_qkv, fb * plain(K_QKV, p.n_rb_qkv));
+    WZ(w.part_o, fb * plain(K_O, p.n_rb_d));
+    WZ(w.part_router, fb * plain(K_ROUTER, p.n_rb_router));
+    WZ(w.part_shgu, fb * plain(K_SHGU, p.n_rb_gu));
+    WZ(w.part_rtgu, fb * n_rtgu);
+    WZ(w.part_d, fb * n_d);
+    WZ(w.part_lm, fb * plain(K_LM, p.n_rb_lm));
+#undef WZ
+    for (int i = 0; i < 3; ++i) {
+      const int nr = 32 << i;
+      if (nr > nr_max) break;
+      wide::WideKernelFn k = wide::kernel_for(nr, e->hd, e->group);
+      if (!k) return bail(DEC_ERR_UNSUPPORTED);
+      int ring = kMaxRing;
+      while (ring >= 2 && wide::smem_bytes(ring, nr, e->hd, e->group) > max_optin) --ring;
+      if (ring < 2) return bail(fail(e, DEC_ERR_UNSUPPORTED, "shared memory too small for the wide ring"));
+      const int smem = wide::smem_bytes(ring, nr, e->hd, e->group);
+      ce = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "cudaFuncSetAttribute"));
+      int nb = 0;
+      ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, (const void*)k, kThreads, smem);
+      if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "occupancy"));
+      if (nb < 1) return bail(fail(e, DEC_ERR_UNSUPPORTED, "wide CTA does not fit on an SM"));
+      e->wkern[i] = k;
+      e->wsmem[i] = smem;
+      e->wring[i] = ring;
+    }
+  }
   e->lengths.assign(c.max_batch, 0);
   ce = cudaStreamSynchronize(e->stream);
   if (ce != cudaSuccess) return bail(cuda_fail(e, ce, "init synchronize"));
@@ -704,6 +807,39 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
 
 namespace {
 
+// One launch of the wide kernel: B = 9 .. 64 tokens, one per slot seq0 .. seq0 + B - 1.
+dec_status launch_wide(dec_engine* e, int B, int seq0, const int32_t* tokens, const void* hidden_in, float* logits,
+                       int32_t* next_tokens, void* hidden_out, cudaStream_t s) {
+  const dec_model_cfg& c = e->cfg;
+  const int wi = B <= 16 ? 0 : B <= 32 ? 1 : 2;
+  if (B > kWideMax || !e->wkern[wi]) return fail(e, DEC_ERR_UNSUPPORTED, "no wide kernel for this batch");
+  KParams p = e->wbase;
+  p.B = B;
+  p.seq0 = seq0;
+  p.mpos = 0;
+  p.accepted = nullptr;
+  p.tokens = tokens;
+  p.hidden_in = static_cast<const uint16_t*>(hidden_in);
+  p.logits = logits;
+  p.next_tokens = next_tokens;
+  p.hidden_out = static_cast<uint16_t*>(hidden_out);
+  p.nsteps = 1;
+  p.ring = e->wring[wi];
+  p.inflight = std::min(p.ring, kSlotsInFlight);
+  WideParams wp = e->wp;
+  wp.nch = std::max(1, std::min(e->wnch_max, e->grid / (B * c.n_kv_heads)));
+  if (dec_status os = order_on(e, s)) return os;
+  cudaError_t ce = cudaMemsetAsync(wp.bar, 0, sizeof(unsigned), s);
+  if (ce != cudaSuccess) return cuda_fail(e, ce, "grid barrier reset");
+  void* args[] = {&p, &wp};
+  ce = cudaLaunchCooperativeKernel((const void*)e->wkern[wi], dim3(e->grid), dim3(kThreads), args,
+                                   (size_t)e->wsmem[wi], s);
+  if (ce != cudaSuccess) return cuda_fail(e, ce, "cudaLaunchCooperativeKernel (wide)");
+  for (int b = 0; b < B; ++b) e->lengths[seq0 + b] += 1;
+  e->launches += 1;
+  return DEC_OK;
+}
+
 // One launch of the decode kernel: B tokens, either one per slot seq0 .. seq0 + B - 1, or (mpos)
 // consecutive positions of slot seq0; `accepted` (device) makes it a verify step. Arguments are
 // checked by the callers.
@@ -711,6 +847,12 @@ dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t*
                        float* logits, int32_t* next_tokens, void* hidden_out, int32_t* accepted, cudaStream_t s,
                        int nsteps = 1) {
   const dec_model_cfg& c = e->cfg;
+  if (B > kMaxBatch) {
+    // (multi-position steps hold at most DEC_MAX_STEP_TOKENS <= kMaxBatch tokens; generation
+    // loops one step per launch at these batches)
+    if (mpos || accepted || nsteps != 1) return fail(e, DEC_ERR_ARG, "wide steps take one decode position per slot");
+    return launch_wide(e, B, seq0, tokens, hidden_in, logits, next_tokens, hidden_out, s);
+  }
   int bi = 0;
   while (kBmChoices[bi] < B) ++bi;
   KParams p = e->base;
@@ -949,12 +1091,13 @@ dec_status dec_generate_device(dec_engine* e, const int32_t* first, int32_t batc
   if (n_steps == 0) return DEC_OK;
   cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
   if (dec_status os = order_on(e, s)) return os;  // d_hist may still be read by earlier work
-  const int MB = e->base.MB;
+  const int MB = e->rows;
   DEC_CUDA(cudaMemcpy2DAsync(e->d_hist, sizeof(int32_t) * MB, first, sizeof(int32_t) * batch, sizeof(int32_t) * batch,
                              1, cudaMemcpyDeviceToDevice, s));
-  // resident steps: one launch runs up to epoch_limit steps (normally all of them)
+  // resident steps: one launch runs up to epoch_limit steps (normally all of them); wide batches
+  // one step per launch, the tokens chained through d_hist on the device
   for (int i = 0; i < n_steps;) {
-    const int n = std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
+    const int n = batch > kMaxBatch ? 1 : std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
     dec_status st = launch_step(e, batch, 0, false, e->d_hist + (size_t)i * MB, nullptr, nullptr,
                                 e->d_hist + (size_t)(i + 1) * MB, nullptr, nullptr, s, n);
     if (st != DEC_OK) return st;
@@ -977,10 +1120,10 @@ dec_status dec_generate(dec_engine* e, const int32_t* first, int32_t batch, int3
     if (e->lengths[b] + n_steps > c.max_ctx) return fail(e, DEC_ERR_CAPACITY, "sequence would pass max_ctx");
   cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : e->stream;
   if (dec_status os = order_on(e, s)) return os;  // d_hist may still be read by earlier steps
-  const int MB = e->base.MB;
+  const int MB = e->rows;
   DEC_CUDA(cudaMemcpyAsync(e->d_hist, first, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s));
   for (int i = 0; i < n_steps;) {
-    const int n = std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
+    const int n = batch > kMaxBatch ? 1 : std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
     dec_status st = launch_step(e, batch, 0, false, e->d_hist + (size_t)i * MB, nullptr, nullptr,
                                 e->d_hist + (size_t)(i + 1) * MB, nullptr, nullptr, s, n);
     if (st != DEC_OK) return st;
@@ -1049,7 +1192,7 @@ dec_status dec_get_routing(dec_engine* e, int32_t layer, int32_t* idx, float* ga
   const dec_model_cfg& c = e->cfg;
   if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
   if (dec_status os = order_on(e, e->stream)) return os;
-  const size_t n = (size_t)e->base.MB * c.top_k, off = (size_t)layer * n;
+  const size_t n = (size_t)e->rows * c.top_k, off = (size_t)layer * n;
   DEC_CUDA(cudaMemcpyAsync(idx, e->base.rt_idx + off, sizeof(int32_t) * n, cudaMemcpyDeviceToHost, e->stream));
   DEC_CUDA(cudaMemcpyAsync(gates, e->base.rt_topk_gate + off, sizeof(float) * n, cudaMemcpyDeviceToHost, e->stream));
   DEC_CUDA(cudaStreamSynchronize(e->stream));
@@ -1061,7 +1204,7 @@ dec_status dec_get_router_logits(dec_engine* e, int32_t layer, float* logits) {
   const dec_model_cfg& c = e->cfg;
   if (c.n_experts == 0 || layer < 0 || layer >= c.n_layers) return fail(e, DEC_ERR_ARG, "no routing for this layer");
   if (dec_status os = order_on(e, e->stream)) return os;
-  const size_t n = (size_t)e->base.MB * c.n_experts;
+  const size_t n = (size_t)e->rows * c.n_experts;
   DEC_CUDA(cudaMemcpyAsync(logits, e->base.rt_logits + (size_t)layer * n, sizeof(float) * n, cudaMemcpyDeviceToHost,
                            e->stream));
   DEC_CUDA(cudaStreamSynchronize(e->stream));

@@ -1324,7 +1324,7 @@ struct Consumer {
       const int b = idx / p.E, e = idx - b * p.E;
       const float* row = tmp + b * kTileRows;
       float v = row[e];
-      if (blockIdx.x == 0) p.rt_logits[((size_t)l * p.MB + b) * p.E + e] = v;  // for inspection
+      if (blockIdx.x == 0) p.rt_logits[((size_t)l * p.rows + b) * p.E + e] = v;  // for inspection
       if (v != v) v = -INFINITY;
       int rank = 0;
 #pragma unroll 4
@@ -1351,8 +1351,8 @@ struct Consumer {
         const float gt = sg[b * 16 + lane] / ssum;
         sg[b * 16 + lane] = gt;
         if (blockIdx.x == 0) {
-          p.rt_idx[((size_t)l * p.MB + b) * p.topk + lane] = sel[b * 16 + lane];
-          p.rt_topk_gate[((size_t)l * p.MB + b) * p.topk + lane] = gt;
+          p.rt_idx[((size_t)l * p.rows + b) * p.topk + lane] = sel[b * 16 + lane];
+          p.rt_topk_gate[((size_t)l * p.rows + b) * p.topk + lane] = gt;
         }
       }
     }
@@ -1564,7 +1564,7 @@ struct Consumer {
             for (int b = 0; b < p.B; ++b) {
               unsigned long long key = atomicExch(p.amax + b, 0ull);
               const int tok = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
-              if (p.next_tokens) p.next_tokens[(size_t)soff * p.MB + b] = tok;
+              if (p.next_tokens) p.next_tokens[(size_t)soff * p.rows + b] = tok;
               if (run && b + 1 < p.B && tok == p.tokens[b + 1]) ++acc;
               else run = false;
             }
@@ -2094,7 +2094,7 @@ struct Consumer {
       // publishes the flag after writing them)
       cta_wait_all(1, [&](int) { return WaitCond{p.tok_flag, ep - 1u}; }, 26);
       if (tid < p.B) {
-        int tok = __ldcg(p.tokens + (size_t)soff * p.MB + tid);
+        int tok = __ldcg(p.tokens + (size_t)soff * p.rows + tid);
         if (tok < 0 || tok >= p.V) {
           raise_err(p, kDevBadArg, 2);
           tok = 0;

@@ -30,7 +30,7 @@ __device__ __forceinline__ bool aborted(const KParams& p) {
   return *reinterpret_cast<volatile int*>(p.err) != 0;
 }
 
-__device__ __noinline__ void raise_err(const KParams& p, int code, int where) {
+static __device__ __noinline__ void raise_err(const KParams& p, int code, int where) {
   atomicCAS(p.err, 0, code | (where << 8));
 }
 
@@ -70,7 +70,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
 // Wait for phase `parity` of an mbarrier; false on timeout or abort. The first test is inline;
 // the polling loop is one out-of-line copy. The clock and the status word (an L2 round trip) are
 // consulted only every 64 polls, so a wait that ends quickly costs no global traffic.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, unsigned parity, int* err, unsigned long long timeout_ns,
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* b, unsigned parity, int* err, unsigned long long timeout_ns,
                                             int where) {
   const unsigned long long t0 = gtimer();
   for (unsigned it = 1;; ++it) {
@@ -130,7 +130,7 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
 // every i < n with a non-null address; lane j polls conditions j, j + 32, ... Returns 1 when they
 // all hold, 0 on abort or after timeout_ns (then the status word records a timeout at `where`).
 // One out-of-line copy serves every wait of the kernel.
-__device__ __noinline__ int poll_all_geq(const unsigned* const* addr, const unsigned* want, int n,
+static __device__ __noinline__ int poll_all_geq(const unsigned* const* addr, const unsigned* want, int n,
                                          int* err, unsigned long long timeout_ns, int where) {
   const int lane = threadIdx.x & 31;
   const unsigned long long t0 = gtimer();
@@ -274,6 +274,27 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&d)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) d[i] = i < NC ? __uint_as_float(r[i]) : 0.f;
+}
+
+// Wider loads for the wide kernel's epilogue: 16 or 32 consecutive columns of the thread's lane
+// (fp32 bit patterns), completed before returning.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&d)[16]) {
+  uint32_t r[16];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) d[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&d)[32]) {
+  uint32_t r[32];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) d[i] = __uint_as_float(r[i]);
 }
 
 // ---------------------------------------------------------------------------------------------

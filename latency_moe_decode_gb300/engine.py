@@ -202,16 +202,21 @@ class Engine:
         self._check(self.lib.dec_get_info(self.h, C.byref(i)), "dec_get_info")
         return {f: getattr(i, f) for f, _ in DecInfo._fields_}
 
+    @property
+    def rows(self) -> int:
+        """Token rows of the routing records: max(DEC_MAX_STEP_TOKENS, max_batch)."""
+        return max(capi.DEC_MAX_STEP_TOKENS, self.cfg.max_batch)
+
     def routing(self, layer: int):
         c = self.cfg
-        idx = np.zeros((capi.DEC_MAX_STEP_TOKENS, c.top_k), np.int32)
-        gates = np.zeros((capi.DEC_MAX_STEP_TOKENS, c.top_k), np.float32)
+        idx = np.zeros((self.rows, c.top_k), np.int32)
+        gates = np.zeros((self.rows, c.top_k), np.float32)
         self._check(self.lib.dec_get_routing(self.h, layer, idx.ctypes.data, gates.ctypes.data), "dec_get_routing")
         return idx, gates
 
     def router_logits(self, layer: int) -> np.ndarray:
         c = self.cfg
-        out = np.zeros((capi.DEC_MAX_STEP_TOKENS, c.n_experts), np.float32)
+        out = np.zeros((self.rows, c.n_experts), np.float32)
         self._check(self.lib.dec_get_router_logits(self.h, layer, out.ctypes.data), "dec_get_router_logits")
         return out
 

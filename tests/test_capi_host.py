@@ -57,7 +57,9 @@ def test_validate_cfg(lib):
     assert v(n_layers=0) == -1
     assert v(head_dim=96) == -5                # not implemented
     assert v(hidden=4000) == -5
-    assert v(max_batch=9) == -5
+    assert v(max_batch=9) == 0                 # 9 .. 64: the wide kernels
+    assert v(max_batch=64) == 0
+    assert v(max_batch=65) == -5
     assert v(hidden=8192) == -5             # above the hidden sizes the kernel handles
     assert v(n_shared=2) == -5
     assert v(n_experts=200, top_k=8) == -5
