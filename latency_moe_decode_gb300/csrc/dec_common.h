@@ -152,10 +152,13 @@ struct WideParams {
   unsigned long long pb_bytes;
   uint8_t* pbx;       // [kb_d][nr * 128]: the normalised input of a q/k/v, router, gate/up or LM stage
   uint8_t* pbo;       // [kb_o][nr * 128]: the attention output
-  uint8_t* pbh;       // [U + n_shared][kb_i][nr * 128]: the SwiGLU rows of each expert slot
+  uint8_t* pbh;       // [U + n_shared][kb_i][nr * 128]: the SwiGLU rows of each expert slot (its
+                      // tokens in ascending order, compact: the slot's j-th token in rows 2j, 2j + 1)
+  uint8_t* pbg;       // [U][kb_d][nr * 128]: pbx's rows of each routed slot's tokens, compact
   int8_t* exx;        // [kb_d][kWideMax] exponents of pbx
   int8_t* exo;        // [kb_o][kWideMax]
-  int8_t* exh;        // [U + n_shared][kb_i][kWideMax]
+  int8_t* exh;        // [U + n_shared][kb_i][kWideMax] (by the slot's token index)
+  int8_t* exg;        // [U][kb_d][kWideMax] (by the slot's token index)
   int32_t* sel;       // [kWideMax][topk] this layer's selected experts
   float* selg;        // [kWideMax][topk] and their normalised gates
   unsigned* bar;      // grid barrier counter: zero at launch, + 1 per CTA and barrier

@@ -145,6 +145,7 @@ struct dec_engine {
   wide::WideKernelFn wkern[3] = {nullptr, nullptr, nullptr};
   int wsmem[3] = {0, 0, 0}, wring[3] = {0, 0, 0};
   int wnch_max = 1;
+  int winflight = 4;  // copies one CTA of the wide kernel keeps in flight (DEC_WIDE_INFLIGHT)
   std::vector<int32_t> lengths;
   unsigned epoch = 0;
   // Counters that grow across steps (each arrival adds its tile count, at most kbs per row block
@@ -727,30 +728,40 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
       const long long t_max = std::max((long long)(umax_w + p.nsh) * p.n_rb_d * p.kb_i,
                                        (long long)std::max(1, umax_w) * p.n_rb_gu * p.kb_d);
       if ((t_max + 1) * G >= (1LL << 31)) return bail(fail(e, DEC_ERR_UNSUPPORTED, "too many tiles in one stage"));
-      // the exponents a CTA's down tiles read (the expert slots its range spans) fit its table
-      for (int U = 0; U <= umax_w; ++U) {
-        const int tpe = p.n_rb_d * p.kb_i, T = (U + p.nsh) * tpe;
-        for (int cta = 0; cta < G; ++cta) {
-          const int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
-          if (t1 > t0 && ((t1 - 1) / tpe - t0 / tpe + 1) * p.kb_i > kMaxKb)
-            return bail(fail(e, DEC_ERR_UNSUPPORTED, "down projection too narrow for the exponent table"));
+      // the work-weighted split's positions (tiles x weight <= 8) times the grid stay 32-bit
+      if ((t_max * 8 + 1) * G >= (1LL << 32)) return bail(fail(e, DEC_ERR_UNSUPPORTED, "expert stage too large"));
+      if (!dense && c.top_k > wide::kWideTopkHost)
+        return bail(fail(e, DEC_ERR_UNSUPPORTED, "batches above 8 take at most 8 experts per token"));
+      // the exponents a CTA's expert tiles read (the expert slots its range spans) fit its table
+      for (int U = 0; U <= umax_w; ++U)
+        for (int st = 0; st < 2; ++st) {
+          const int kbs = st ? p.kb_d : p.kb_i, tpe = (st ? p.n_rb_gu : p.n_rb_d) * kbs;
+          const int T = (st ? U : U + p.nsh) * tpe;
+          for (int cta = 0; cta < G; ++cta) {
+            const int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
+            if (t1 > t0 && ((t1 - 1) / tpe - t0 / tpe + 1) * kbs > kMaxKb)
+              return bail(fail(e, DEC_ERR_UNSUPPORTED, "expert stage too narrow for the exponent table"));
+          }
         }
-      }
     }
     const size_t PBS = (size_t)nr_max * 128;
     const size_t nbx = p.kb_d, nbo = p.kb_o, nbh = (size_t)wp.hmax * p.kb_i;
+    const size_t nbg = (size_t)std::max(1, umax_w) * p.kb_d;
+    const size_t nb = nbx + nbo + nbh + nbg;
     uint8_t* pb = nullptr;
-    WZ(pb, (nbx + nbo + nbh) * PBS);
+    WZ(pb, nb * PBS);
     wp.pb = pb;
-    wp.pb_bytes = (nbx + nbo + nbh) * PBS;
+    wp.pb_bytes = nb * PBS;
     wp.pbx = pb;
     wp.pbo = pb + nbx * PBS;
     wp.pbh = pb + (nbx + nbo) * PBS;
+    wp.pbg = pb + (nbx + nbo + nbh) * PBS;
     int8_t* ex = nullptr;
-    WZ(ex, (nbx + nbo + nbh) * kWideMax);
+    WZ(ex, nb * kWideMax);
     wp.exx = ex;
     wp.exo = ex + nbx * kWideMax;
     wp.exh = ex + (nbx + nbo) * kWideMax;
+    wp.exg = ex + (nbx + nbo + nbh) * kWideMax;
     WZ(wp.sel, sizeof(int32_t) * kWideMax * std::max(1, c.top_k));
     WZ(wp.selg, sizeof(float) * kWideMax * std::max(1, c.top_k));
     WZ(wp.bar, sizeof(unsigned) * 32);
@@ -795,6 +806,10 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
       e->wsmem[i] = smem;
       e->wring[i] = ring;
     }
+    if (const char* wf = getenv("DEC_WIDE_INFLIGHT")) {
+      const int v = atoi(wf);
+      if (v >= 1 && v <= kMaxRing) e->winflight = v;
+    }
   }
   e->lengths.assign(c.max_batch, 0);
   ce = cudaStreamSynchronize(e->stream);
@@ -825,7 +840,7 @@ dec_status launch_wide(dec_engine* e, int B, int seq0, const int32_t* tokens, co
   p.hidden_out = static_cast<uint16_t*>(hidden_out);
   p.nsteps = 1;
   p.ring = e->wring[wi];
-  p.inflight = std::min(p.ring, kSlotsInFlight);
+  p.inflight = std::min(p.ring, e->winflight);
   WideParams wp = e->wp;
   wp.nch = std::max(1, std::min(e->wnch_max, e->grid / (B * c.n_kv_heads)));
   if (dec_status os = order_on(e, s)) return os;

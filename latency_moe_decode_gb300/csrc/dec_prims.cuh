@@ -297,6 +297,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&d)[32]) {
   for (int i = 0; i < 32; ++i) d[i] = __uint_as_float(r[i]);
 }
 
+// TMEM reads of 8 columns for one or two tiles, completed in the same statement (both loads in
+// flight before the one wait; the outputs are defined only once they are valid).
+__device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld8x2_wait(uint32_t ta0, uint32_t ta1, uint32_t (&r)[2][8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0][0]), "=r"(r[0][1]), "=r"(r[0][2]), "=r"(r[0][3]), "=r"(r[0][4]), "=r"(r[0][5]), "=r"(r[0][6]),
+        "=r"(r[0][7]), "=r"(r[1][0]), "=r"(r[1][1]), "=r"(r[1][2]), "=r"(r[1][3]), "=r"(r[1][4]), "=r"(r[1][5]),
+        "=r"(r[1][6]), "=r"(r[1][7])
+      : "r"(ta0), "r"(ta1)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // conversions (CUDA's own FP8 conversion instruction; bf16 -> fp32 is a shift)
 

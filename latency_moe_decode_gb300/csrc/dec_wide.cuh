@@ -11,16 +11,18 @@
 // tile and the B block of its k block into one ring slot; the MMA warp multiplies them with
 // tcgen05.mma kind::f8f6f4 (M = 128 weight rows, N = nr, K = 128) into a TMEM slice; the consumer
 // warps scale each tile's product (block scale, the pieces' exponent) into fp32 registers and
-// write one split-K partial per output row block. Routed experts multiply every token of the step
-// (the MMA costs the same for any N <= 128) and keep only their routed tokens' rows.
+// write one split-K partial per output row block. A routed expert's tiles multiply only its own
+// tokens: after the routing every CTA knows each expert slot's tokens, their B rows are gathered
+// into compact blocks (the slot's j-th token in rows 2j, 2j + 1), and the MMA's N is twice the
+// slot's token count rounded up to 16.
 //
 // Phases of a layer (barrier after each):
 //   q/k/v GEMV | attention (each unit sums its q/k/v partials, applies RoPE, appends its key and
 //   value, streams its KV tiles) | chunk merge -> B blocks of the attention output | output
 //   projection GEMV | x_mid = x + projection, RMSNorm -> B blocks | router and shared expert
-//   gate/up GEMVs | routing (one CTA per token) | routed gate/up GEMV | SwiGLU -> B blocks per
-//   expert slot | down GEMV (expert-major, gate applied per partial) | layer output, next RMSNorm
-//   -> B blocks.
+//   gate/up GEMVs | routing (one CTA per token) | each slot's tokens' B rows gathered | routed
+//   gate/up GEMV | SwiGLU -> B blocks per expert slot | down GEMV (expert-major, gate applied per
+//   partial) | layer output, next RMSNorm -> B blocks.
 // Then the LM head GEMV, its finalisation (logits, argmax) and the next tokens.
 #pragma once
 #include "dec_kernel.cuh"
@@ -30,11 +32,23 @@ namespace wide {
 
 constexpr int kGC = 256;           // TMEM columns per group of tile products
 constexpr int kNGW = 2;            // groups in flight (all 512 columns)
-constexpr int kBarsPerLayer = 11;  // grid barriers of one layer
+constexpr int kBarsPerLayer = 12;  // grid barriers of one layer
+constexpr int kWideTopk = 8;       // experts per token the wide kernel's routing tables hold
+// diagnostics build: CTA 0's wait totals (ns) over the step's routed gate/up stages, in trace
+// words kWaitTrace + {0: producer waiting for copies in flight, 1: producer waiting for slot
+// releases, 2: MMA waiting for slot data, 3: MMA waiting for free TMEM, 4: consumers waiting for
+// products, 5: consumers' stage time}
+constexpr int kWaitTrace = 400;
 
-// ring slot: slot_tiles weight tiles, then their B blocks (a 32 KB hand-off per slot at most)
-__host__ __device__ constexpr int slot_tiles(int nr) { return nr >= 128 ? 1 : 2; }
-__host__ __device__ constexpr int slot_bytes(int nr) { return slot_tiles(nr) * (kTileBytes + nr * 128); }
+// Ring slot: two weight tiles and a B area. Two tiles whose B blocks fit half the area each share
+// a slot, their blocks side by side (a 32 KB weight hand-off; one SM's streaming rate grows with
+// the bytes per hand-off up to ~32 KB). A wider tile (a dense stage of many tokens, an expert
+// with many) has a slot to itself, its block in the second tile's place. The area is 8 KB (pairs
+// of up to 32 rows, 16 tokens: five slots) except for steps of 17 .. 32 tokens, where 16 KB lets
+// every tile pair up (four slots).
+__host__ __device__ constexpr int b_area(int nr) { return nr == 64 ? 16384 : 8192; }
+__host__ __device__ constexpr int pair_rows(int nr) { return b_area(nr) / 2 / 128; }
+__host__ __device__ constexpr int slot_bytes(int nr) { return 2 * kTileBytes + b_area(nr); }
 
 // Partial-sum slots reserved per segment (output row block) of kbs tiles when a stage of T tiles
 // is split into contiguous ranges over G CTAs: with T < G every tile has its own CTA; otherwise a
@@ -51,12 +65,19 @@ struct WGeo {
   int kbs;  // tiles per segment (one output row block's k blocks)
   int tpe;  // expert stages: tiles of one expert slot
   int S;    // partial slots per segment
+  // expert stages split by work (see wsplit below): prefix sums of the slots' tile weights, or
+  // null for the even split by tiles; WT = the stage's total weight (WT x grid < 2^32, checked
+  // by the host)
+  const int* pw;
+  unsigned WT;
 };
 // Routed gate/up: U expert slots x n_rb_gu row blocks x kb_d k blocks. Down: U + n_shared slots
 // (the shared expert last), expert major, segment (u, rb) = its kb_i k blocks.
 __host__ __device__ inline WGeo wgeo(const KParams& p, int kind, int U, int G) {
   WGeo g;
   g.tpe = 0;
+  g.pw = nullptr;
+  g.WT = 0;
   switch (kind) {
     case K_QKV: g.kbs = p.kb_d; g.T = p.n_rb_qkv * p.kb_d; break;
     case K_O: g.kbs = p.kb_o; g.T = p.n_rb_d * p.kb_o; break;
@@ -66,7 +87,8 @@ __host__ __device__ inline WGeo wgeo(const KParams& p, int kind, int U, int G) {
     case K_D: g.kbs = p.kb_i; g.tpe = p.n_rb_d * p.kb_i; g.T = (U + p.nsh) * g.tpe; break;
     default: g.kbs = p.kb_d; g.T = p.n_rb_lm * p.kb_d; break;
   }
-  g.S = seg_slots(g.T, g.kbs, G);
+  // expert stages: one slot per k block (any split, even or by work, fits)
+  g.S = (kind == K_RTGU || kind == K_D) ? g.kbs : seg_slots(g.T, g.kbs, G);
   return g;
 }
 
@@ -97,11 +119,57 @@ struct WMisc {
   int len[kWideMax];
   int tok[kWideMax];
   unsigned long long umask[kMaxExperts + 1];  // tokens routed to expert slot u (slot U: shared)
-  uint8_t wsel[kWideMax][16];                 // expert slot of each token's selections
-  float wgate[kWideMax][16];                  // and their gates
+  int pw[kMaxExperts + 2];                    // prefix sums of the slots' tile weights (wsplit)
+  int wmax;                                   // the heaviest slot's weight
+  uint8_t wsel[kWideMax][kWideTopk];          // expert slot of each token's selections
+  float wgate[kWideMax][kWideTopk];           // and their gates
   float rsum[kConsumerWarps];
   alignas(16) int8_t ex[kMaxKb * kWideMax];  // exponents of the running GEMV stage's B blocks [row][token]
 };
+
+// Work-weighted split of an expert stage. A tile of expert slot u costs w(u) = its B rows / 16
+// (at least 2): the epilogue work and the slot pairing grow with the slot's tokens, and at large
+// batches one slot (the shared expert's, or a routed one that drew many tokens) can cost several
+// times the rest. Tile t of slot u starts at weight position tpe pw[u] + (t - u tpe) w(u); CTA c
+// owns the tiles whose start lies in [c WT / G, (c + 1) WT / G), a contiguous range. Used when
+// a CTA's share WT / G is at least the heaviest tile (so every CTA owns a tile of each segment it
+// straddles); otherwise, and whenever the stage has fewer tiles than CTAs, the even split.
+__device__ __forceinline__ unsigned wpos(const WGeo& g, int t) {
+  const int u = t / g.tpe;
+  return (unsigned)(g.tpe * g.pw[u] + (t - u * g.tpe) * (g.pw[u + 1] - g.pw[u]));
+}
+__device__ __forceinline__ int wowner(const WGeo& g, int t, int G) { return (int)(wpos(g, t) * (unsigned)G / g.WT); }
+// first tile of CTA c (c = G: the stage's end)
+__device__ inline int wstart(const WGeo& g, int c, int G) {
+  if (!g.pw) return range_lo(g.T, c, G);
+  if (c >= G) return g.T;
+  const unsigned P = ((unsigned)c * g.WT + (unsigned)G - 1u) / (unsigned)G;
+  int u = 0;
+  while ((unsigned)(g.tpe * g.pw[u + 1]) <= P) ++u;
+  const unsigned r = P - (unsigned)(g.tpe * g.pw[u]);
+  const unsigned w = (unsigned)(g.pw[u + 1] - g.pw[u]);
+  return u * g.tpe + (int)min((unsigned)g.tpe, (r + w - 1u) / w);
+}
+// contributors of segment seg, and CTA c's slot among them (its first tile of the segment: f)
+__device__ __forceinline__ int wn_contrib(const WGeo& g, int seg, int G) {
+  if (!g.pw) return n_contrib(seg * g.kbs, g.kbs, g.T, G);
+  return wowner(g, seg * g.kbs + g.kbs - 1, G) - wowner(g, seg * g.kbs, G) + 1;
+}
+__device__ __forceinline__ int wcontrib_slot(const WGeo& g, int c, int f, int seg, int G) {
+  if (!g.pw) return contrib_slot(c, f, seg * g.kbs, g.T, G);
+  return c - wowner(g, seg * g.kbs, G);
+}
+
+// attach the work-weighted split to an expert stage's geometry where it applies (the slots'
+// weights come from the CTA's routing tables)
+template <class M>
+__device__ __forceinline__ void wsplit(WGeo& g, const M* m, const KParams& p, int kind, int U, int G) {
+  if ((kind != K_RTGU && kind != K_D) || g.T < G) return;
+  const unsigned WT = (unsigned)(g.tpe * m->pw[kind == K_RTGU ? U : U + p.nsh]);
+  if (WT / (unsigned)G < (unsigned)m->wmax) return;
+  g.pw = m->pw;
+  g.WT = WT;
+}
 
 struct WLayout {
   int ring_off, full_off, empty_off, mempty_off, red_off, misc_off, total;
@@ -115,7 +183,8 @@ __host__ __device__ inline WLayout wlayout(int ring, int nr, int hd, int group) 
   s.red_off = align_up(s.mempty_off + ring * 8, 128);
   int red = kConsumerWarps * group * (hd + 2) * 4;       // attention: the warps' states
   red = red > 2 * (group + 2) * hd * 4 ? red : 2 * (group + 2) * hd * 4;  // the unit's q/k/v
-  const int pairs = (kMaxExperts + kWideMax * 17) * 4;   // routing marks, SwiGLU pairs
+  // routing marks, SwiGLU pairs, each expert slot's tokens
+  const int pairs = (kMaxExperts + kWideMax * 17) * 4 + (kMaxExperts + 1) * kWideMax;
   red = red > pairs ? red : pairs;
   s.misc_off = align_up(s.red_off + red, 128);
   s.total = align_up(s.misc_off + (int)sizeof(WMisc), 128);
@@ -140,6 +209,67 @@ __device__ __forceinline__ WUnit wunit(const KParams& p, const WideParams& w, co
 // 128 bytes apart, rows of a core matrix 16 bytes apart
 __device__ __forceinline__ int boff(int row, int c) { return (row >> 3) * 1024 + (c >> 4) * 128 + (row & 7) * 16 + (c & 15); }
 
+// B rows (tokens x 2 pieces, padded to the MMA's N granularity of 16) of n tokens
+__device__ __forceinline__ int brows(int n) { return (2 * n + 15) & ~15; }
+
+// tokens a GEMV tile multiplies: its expert slot's (routed stages), or the whole step's
+__device__ __forceinline__ int tile_tokens(const KParams& p, const WMisc* m, int kind, const WGeo& g, int t) {
+  if (kind == K_RTGU || kind == K_D) return __popcll(m->umask[t / g.tpe]);
+  return p.B;
+}
+
+// TMEM columns of one tile's product (its B rows) and tiles per group (one hand-off between the
+// MMA warp and the consumers): as many as a group's kGC columns hold, at most 8. A group's tiles
+// belong to one segment, hence to one expert slot, so they share the width.
+struct GroupShape {
+  int w, gt;
+};
+// B rows of tile t (its tokens' pieces, padded)
+template <int NR>
+__device__ __forceinline__ int tile_rows(const KParams& p, const WMisc* m, int kind, const WGeo& g, int t) {
+  return min(NR, brows(tile_tokens(p, m, kind, g, t)));
+}
+// tiles of the slot that starts at tile t (< t1): two when both have at most pair_rows B rows
+template <int NR>
+__device__ __forceinline__ int slot_take(const KParams& p, const WMisc* m, int kind, const WGeo& g, int t, int t1) {
+  return (t + 1 < t1 && tile_rows<NR>(p, m, kind, g, t) <= pair_rows(NR) &&
+          tile_rows<NR>(p, m, kind, g, t + 1) <= pair_rows(NR)) ? 2 : 1;
+}
+// Slots of the tile range [t0, t1) under slot_take's rule: consecutive tiles of at most
+// pair_rows rows pair up from the start of each run of them; a wider tile takes a slot alone.
+// O(expert slots the range spans): an expert's tiles share their row count.
+template <int NR>
+__device__ int range_slots(const KParams& p, const WMisc* m, int kind, const WGeo& g, int t0, int t1) {
+  if (t1 <= t0) return 0;
+  if (kind != K_RTGU && kind != K_D) {
+    const int n = t1 - t0;
+    return tile_rows<NR>(p, m, kind, g, t0) <= pair_rows(NR) ? (n + 1) / 2 : n;
+  }
+  int slots = 0, run = 0;  // run: tiles of the current run of narrow tiles
+  for (int u = t0 / g.tpe; u * g.tpe < t1; ++u) {
+    const int a = max(t0, u * g.tpe), b = min(t1, (u + 1) * g.tpe);
+    if (tile_rows<NR>(p, m, kind, g, a) <= pair_rows(NR)) {
+      run += b - a;
+    } else {
+      slots += (run + 1) / 2 + (b - a);
+      run = 0;
+    }
+  }
+  return slots + (run + 1) / 2;
+}
+
+// byte offset of tile j's B block in a slot of n tiles
+template <int NR>
+__device__ __forceinline__ int b_off(int n, int j) { return n == 2 ? 2 * kTileBytes + j * (b_area(NR) / 2) : kTileBytes; }
+
+template <int NR>
+__device__ __forceinline__ GroupShape group_shape(const KParams& p, const WMisc* m, int kind, const WGeo& g, int t) {
+  GroupShape s;
+  s.w = min(NR, brows(tile_tokens(p, m, kind, g, t)));
+  s.gt = min(8, kGC / s.w);
+  return s;
+}
+
 __device__ __forceinline__ float* part_of(const KParams& p, int kind) {
   switch (kind) {
     case K_QKV: return p.part_qkv;
@@ -157,7 +287,7 @@ __device__ __forceinline__ float* part_of(const KParams& p, int kind) {
 
 template <int NR, int HD, int G>
 struct WProducer {
-  static constexpr int ST = slot_tiles(NR), PBS = NR * 128, SB = slot_bytes(NR);
+  static constexpr int PBS = NR * 128, SB = slot_bytes(NR);
   const KParams& p;
   const WideParams& w;
   uint8_t* ring;
@@ -188,7 +318,10 @@ struct WProducer {
   }
 
   // the next slot, once at most p.inflight - 1 copies are in flight and its last use is over
+  unsigned long long tw_fl = 0, tw_rel = 0;  // diagnostics: wait totals
+  bool tw_on = false;
   __device__ bool claim(int& slot, bool mma_use) {
+    const unsigned long long c0 = (DEC_TRACE && tw_on) ? gtimer() : 0;
     while (item - landed >= (unsigned)p.inflight) {
       if (!mbar_wait(&full[lslot], llap & 1, p, 42)) {
         dead = true;
@@ -202,6 +335,7 @@ struct WProducer {
     }
     slot = pslot;
     const uint32_t bit = 1u << slot;
+    const unsigned long long c1 = (DEC_TRACE && tw_on) ? gtimer() : 0;
     if (plap > 0) {
       const bool pm = (last_mma & bit) != 0;
       const unsigned par = (((pm ? nm_par : ne_par) >> slot) & 1u) ^ 1u;
@@ -209,6 +343,10 @@ struct WProducer {
         dead = true;
         return false;
       }
+    }
+    if (DEC_TRACE && tw_on) {
+      tw_fl += c1 - c0;
+      tw_rel += gtimer() - c1;
     }
     if (mma_use) {
       last_mma |= bit;
@@ -272,29 +410,36 @@ struct WProducer {
     const int kb = t % g.kbs;
     if (kind == K_O) return w.pbo + (size_t)kb * PBS;
     if (kind == K_D) return w.pbh + ((size_t)(t / g.tpe) * p.kb_i + kb) * PBS;
+    if (kind == K_RTGU) return w.pbg + ((size_t)(t / g.tpe) * p.kb_d + kb) * PBS;
     return w.pbx + (size_t)kb * PBS;
   }
 
   __device__ void issue_gemv(int kind, int l, int U, const int* elist) {
     if (dead) return;
-    const WGeo g = wgeo(p, kind, U, gridDim.x);
-    const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
+    WGeo g = wgeo(p, kind, U, gridDim.x);
+    wsplit(g, m, p, kind, U, gridDim.x);
+    const int t0 = wstart(g, blockIdx.x, gridDim.x), t1 = wstart(g, blockIdx.x + 1, gridDim.x);
     const LayerDev& Ld = p.layers[l < p.L ? l : 0];
-    for (int t = t0; t < t1; t += ST) {
+    for (int t = t0; t < t1;) {
       int slot;
       if (!claim(slot, true)) return;
-      const int n = min(ST, t1 - t);
-      const uint8_t* a[ST];
-      const uint8_t* b[ST];
+      const int n = slot_take<NR>(p, m, kind, g, t, t1);
+      const uint8_t* a[2];
+      const uint8_t* b[2];
+      unsigned bb[2];  // B bytes of each tile: its tokens' rows
+      unsigned tx = 0;
       bool ok = true;
 #pragma unroll
-      for (int j = 0; j < ST; ++j) {
+      for (int j = 0; j < 2; ++j) {
         if (j < n) {
           a[j] = tile_src(kind, Ld, g, t + j, U, elist);
           b[j] = b_src(kind, g, t + j);
-          ok = ok && within(a[j], kTileBytes, p.warena, p.warena_bytes) && within(b[j], PBS, w.pb, w.pb_bytes);
+          bb[j] = (unsigned)tile_rows<NR>(p, m, kind, g, t + j) * 128u;
+          tx += kTileBytes + bb[j];
+          ok = ok && within(a[j], kTileBytes, p.warena, p.warena_bytes) && within(b[j], bb[j], w.pb, w.pb_bytes);
         }
       }
+      t += n;
       uint8_t* dst = ring + (size_t)slot * SB;
       if (!ok) {
         raise_err(p, kDevBadArg, 45);
@@ -302,18 +447,13 @@ struct WProducer {
         advance();
         continue;
       }
-      mbar_arrive_expect_tx(&full[slot], (unsigned)n * (kTileBytes + PBS));
-      if (n == 2 && a[ST - 1] == a[0] + kTileBytes) {
+      mbar_arrive_expect_tx(&full[slot], tx);
+      if (n == 2 && a[1] == a[0] + kTileBytes) {
         bulk_g2s_hint(dst, a[0], 2 * kTileBytes, &full[slot], pol_stream);
       } else {
         for (int j = 0; j < n; ++j) bulk_g2s_hint(dst + (size_t)j * kTileBytes, a[j], kTileBytes, &full[slot], pol_stream);
       }
-      uint8_t* bdst = dst + (size_t)ST * kTileBytes;
-      if (n == 2 && b[ST - 1] == b[0] + PBS) {
-        bulk_g2s_hint(bdst, b[0], 2 * PBS, &full[slot], pol_near);
-      } else {
-        for (int j = 0; j < n; ++j) bulk_g2s_hint(bdst + (size_t)j * PBS, b[j], PBS, &full[slot], pol_near);
-      }
+      for (int j = 0; j < n; ++j) bulk_g2s_hint(dst + b_off<NR>(n, j), b[j], bb[j], &full[slot], pol_near);
       advance();
     }
   }
@@ -391,24 +531,31 @@ struct WProducer {
       int U = 0;
       if (!p.dense) {
         if (!routing(U, elist)) break;
+        if (!wait_bar(base + 8)) break;  // (the slots' tokens gathered)
+        tw_on = true;
         issue_gemv(K_RTGU, l, U, elist);
+        tw_on = false;
       }
-      if (!wait_bar(base + 9)) break;
+      if (!wait_bar(base + 10)) break;
       issue_gemv(K_D, l, U, elist);
       ++lay;
     }
     if (p.V > 0 && !dead && wait_bar(1u + (unsigned)(kBarsPerLayer * p.L))) issue_gemv(K_LM, 0, 0, elist);
     drain();
+    if (DEC_TRACE && blockIdx.x == 0) {
+      p.trace[kWaitTrace + 0] = tw_fl;
+      p.trace[kWaitTrace + 1] = tw_rel;
+    }
   }
 };
 
 // ---------------------------------------------------------------------------------------------
-// MMA warp (one thread): the CTA's tiles in the consumers' order, in groups of up to GT tiles of
-// one segment per TMEM group (kGC columns), kNGW groups in flight.
+// MMA warp (one thread): the CTA's tiles in the consumers' order, in groups of tiles of one
+// segment (group_shape: as many as kGC TMEM columns hold), kNGW groups in flight.
 
 template <int NR, int HD, int G>
 struct WMma {
-  static constexpr int ST = slot_tiles(NR), PBS = NR * 128, SB = slot_bytes(NR), GT = kGC / NR;
+  static constexpr int SB = slot_bytes(NR);
   const KParams& p;
   const WideParams& w;
   uint8_t* ring;
@@ -419,6 +566,7 @@ struct WMma {
   unsigned lap = 0;
   unsigned gseq = 0;
   unsigned stage = 0;  // GEMV stages reached
+  unsigned long long tw_full = 0, tw_tmem = 0;  // diagnostics: wait totals in routed gate/up stages
   bool dead = false;
   uint32_t tmem = 0;
   unsigned lay = 0;
@@ -457,31 +605,41 @@ struct WMma {
   __device__ void gemv(int kind, int U) {
     ++stage;
     wait_stage();
-    const WGeo g = wgeo(p, kind, U, gridDim.x);
-    const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
-    constexpr uint32_t idesc = idesc_e4m3_f32(kTileRows, NR);
-    int j = 0;
+    WGeo g = wgeo(p, kind, U, gridDim.x);
+    wsplit(g, m, p, kind, U, gridDim.x);
+    const int t0 = wstart(g, blockIdx.x, gridDim.x), t1 = wstart(g, blockIdx.x + 1, gridDim.x);
+    int j = 0, ns = 0;  // tile j of the current slot of ns tiles
 #pragma unroll 1
     for (int t = t0; t < t1;) {
       const int seg = t / g.kbs;
-      const int n = min(GT, min(t1, (seg + 1) * g.kbs) - t);
+      const GroupShape gs = group_shape<NR>(p, m, kind, g, t);
+      const int n = min(gs.gt, min(t1, (seg + 1) * g.kbs) - t);
       const int gsl = gseq % kNGW;
+      const bool tw = DEC_TRACE && kind == K_RTGU;
+      unsigned long long c0 = tw ? gtimer() : 0;
       if (!dead && gseq >= (unsigned)kNGW && !mbar_wait(&m->tempty[gsl], (gseq / kNGW - 1) & 1, p, 48)) dead = true;
+      if (tw) tw_tmem += gtimer() - c0;
 #pragma unroll 1
       for (int i = 0; i < n; ++i, ++t) {
-        if (!dead && j == 0 && !mbar_wait(&full[slot], lap & 1, p, 49)) dead = true;
+        if (j == 0) {
+          ns = slot_take<NR>(p, m, kind, g, t, t1);
+          if (tw) c0 = gtimer();
+          if (!dead && !mbar_wait(&full[slot], lap & 1, p, 49)) dead = true;
+          if (tw) tw_full += gtimer() - c0;
+        }
         const uint8_t* a = ring + (size_t)slot * SB + (size_t)j * kTileBytes;
-        const uint8_t* b = ring + (size_t)slot * SB + (size_t)ST * kTileBytes + (size_t)j * PBS;
+        const uint8_t* b = ring + (size_t)slot * SB + b_off<NR>(ns, j);
         if (!dead) {
           tc_fence_after();
           m->hdr[gsl][i] = *reinterpret_cast<const float2*>(a + kTileData);
           const uint64_t ad = smem_desc(a, 128, 1024), bd = smem_desc(b, 128, 1024);
-          const uint32_t d = tmem + (uint32_t)(gsl * kGC + i * NR);
+          const uint32_t d = tmem + (uint32_t)(gsl * kGC + i * gs.w);
+          const uint32_t idesc = idesc_e4m3_f32(kTileRows, gs.w);
 #pragma unroll
           for (int k = 0; k < kTileK / 32; ++k)
             mma_e4m3(d, ad + (uint64_t)(k * 16), bd + (uint64_t)(k * 16), idesc, k > 0 ? 1u : 0u);
         }
-        if (++j == ST || t == t1 - 1) {
+        if (++j == ns) {
           if (!dead) mma_commit(&mempty[slot]);
           j = 0;
           skip(1);
@@ -527,6 +685,10 @@ struct WMma {
       while (!mbar_try_wait(&m->tfull[last % kNGW], (last / kNGW) & 1) && gtimer() - t0 < p.timeout_ns) {
       }
     }
+    if (DEC_TRACE && blockIdx.x == 0) {
+      p.trace[kWaitTrace + 2] = tw_full;
+      p.trace[kWaitTrace + 3] = tw_tmem;
+    }
     mbar_arrive(&m->mma_done);
   }
 };
@@ -536,7 +698,7 @@ struct WMma {
 
 template <int NR, int HD, int G>
 struct WConsumer {
-  static constexpr int ST = slot_tiles(NR), PBS = NR * 128, SB = slot_bytes(NR), GT = kGC / NR;
+  static constexpr int PBS = NR * 128, SB = slot_bytes(NR);
   static constexpr int TPT = NR / 4;  // tokens per thread in a tile's epilogue
   static constexpr int MAXV = kMaxHidden / (kConsumerWarps * 32 * 8);  // 8-element chunks per thread
   const KParams& p;
@@ -554,6 +716,8 @@ struct WConsumer {
   unsigned gseq = 0;  // tile groups handed over so far
   unsigned nbar = 0;  // grid barriers passed
   unsigned nstage = 0;  // GEMV stages begun (thread 0)
+  unsigned long long tw_prod = 0, tw_stage = 0, tw_ld = 0, tw_flush = 0;  // diagnostics (thread 0): routed gate/up
+  int rtgu_seen = 0;
   uint32_t tmem = 0;
 
   __device__ WConsumer(const KParams& p_, const WideParams& w_, uint8_t* r, uint64_t* f, uint64_t* e, float* rd,
@@ -606,6 +770,8 @@ struct WConsumer {
       if (lane == 0) m->flag = ok;
     }
     dead = cons_any(dead) || !m->flag;
+    // diagnostics build: CTA 0's time at each grid barrier (phase boundaries)
+    if (DEC_TRACE && blockIdx.x == 0 && tid == 0 && nbar < (unsigned)kTraceSlots) p.trace[nbar] = gtimer();
   }
 
   // ---- B blocks
@@ -706,34 +872,55 @@ struct WConsumer {
 
   // ---- GEMV stages
 
-  // Add the products of group gs (n consecutive tiles of one segment, from tile t) into the
-  // thread's accumulators: thread (warp w, lane) holds weight row 32 (w & 3) + lane of tokens
-  // TPT (w >> 2) + j; token b's pieces are columns 2b, 2b + 1 of the tile's TMEM slice. Each
-  // product is scaled by the tile's block scale and the pieces' 2^-a.
-  __device__ __forceinline__ void epilogue(unsigned gs, int n, int kind, const WGeo& g, int t, int u_lo, float (&acc)[TPT]) {
+  // Add the products of group gs (n consecutive tiles of one segment, from tile t: one expert
+  // slot, k blocks kb0 .. kb0 + n - 1) into the thread's accumulators. The tile's tokens (the
+  // step's, or the expert slot's in ascending order) come in chunks of 8 (16 TMEM columns, token
+  // j's pieces in columns 2j, 2j + 1); the two warps of a TMEM lane quadrant (w, w + 4) take 4
+  // tokens of each chunk: thread (warp w, lane) holds weight row 32 (w & 3) + lane of tokens
+  // 8c + 4 (w >> 2) + j, accumulator 4c + j. The loads of two tiles are issued before one wait.
+  // Each product is scaled by the tile's block scale and the pieces' 2^-a.
+  static constexpr int LB = 2;
+  __device__ __forceinline__ void epilogue(unsigned gs, int n, int sw, int kind, const WGeo& g, int t, int u_lo,
+                                          float (&acc)[TPT]) {
     const int gsl = gs % kNGW;
+    const unsigned long long c0 = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
     if (!dead && !mbar_wait(&m->tfull[gsl], (gs / kNGW) & 1, p, 54)) dead = true;
+    if (DEC_TRACE && kind == K_RTGU && tid == 0) tw_prod += gtimer() - c0;
     dead = __any_sync(0xffffffffu, dead);  // (the TMEM loads below are warp-collective)
     const int q = warp & 3, h = warp >> 2, row = 32 * q + lane;
-    if (!dead && h * TPT < p.B) {  // (warp-uniform)
+    const int seg = t / g.kbs, kb0 = t - seg * g.kbs;
+    const int ntok = tile_tokens(p, m, kind, g, t);  // (the group's tiles share it)
+    const int xr0 = (kind == K_RTGU || kind == K_D) ? (t / g.tpe - u_lo) * g.kbs + kb0 : kb0;
+    if (!dead) {
       tc_fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gsl * kGC + 8 * h);
+#pragma unroll
+      for (int c = 0; c < NR / 16; ++c) {
+        if (8 * c + 4 * h >= ntok) break;  // (warp-uniform)
 #pragma unroll 1
-      for (int i = 0; i < n; ++i, ++t) {
-        const int kb = t % g.kbs;
-        const int xr = kind == K_D ? (t / g.tpe - u_lo) * p.kb_i + kb : kb;
-        const int8_t* ex = m->ex + xr * kWideMax + h * TPT;
-        const float2 sc = m->hdr[gsl][i];
-        const float s_r = row < 64 ? sc.x : sc.y;
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(gsl * kGC + i * NR + h * (NR / 2));
-        // 16 columns (8 tokens) per load
+        for (int i0 = 0; i0 < n; i0 += LB) {
+          const int nb = min(LB, n - i0);
+          uint32_t d[LB][8];
+          const uint32_t ta = tb + (uint32_t)(i0 * sw + 16 * c);
+          const unsigned long long cl = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
+          if (nb == 2) tmem_ld8x2_wait(ta, ta + (uint32_t)sw, d);
+          else tmem_ld8_wait(ta, d[0]);
+          if (DEC_TRACE && kind == K_RTGU && tid == 0) tw_ld += gtimer() - cl;
 #pragma unroll
-        for (int c = 0; c < NR / 32; ++c) {
-          float d[16];
-          tmem_ld16(ta + 16 * c, d);
+          for (int k = 0; k < LB; ++k) {
+            if (k < nb) {
+              const int i = i0 + k;
+              const float2 sc = m->hdr[gsl][i];
+              const float s_r = row < 64 ? sc.x : sc.y;
+              const uint32_t e4 = *reinterpret_cast<const uint32_t*>(m->ex + (xr0 + i) * kWideMax + 8 * c + 4 * h);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float inv = __int_as_float((127 - (int)ex[8 * c + j]) << 23);
-            acc[8 * c + j] = fmaf(s_r * inv, fmaf(d[2 * j + 1], 0.0625f, d[2 * j]), acc[8 * c + j]);
+              for (int j = 0; j < 4; ++j) {
+                const int a = (int)(int8_t)(e4 >> (8 * j));
+                const float inv = __int_as_float((127 - a) << 23);
+                acc[4 * c + j] = fmaf(s_r * inv, fmaf(__uint_as_float(d[k][2 * j + 1]), 0.0625f, __uint_as_float(d[k][2 * j])),
+                                      acc[4 * c + j]);
+              }
+            }
           }
         }
       }
@@ -749,46 +936,64 @@ struct WConsumer {
     return 0.f;
   }
 
-  // One segment's partial sums of the CTA: plain stores (read after the next grid barrier). The
-  // routed stages keep only the tokens routed to the segment's expert slot; the down projection's
-  // partials carry that token's gate.
+  // One segment's partial sums of the CTA: plain stores (read after the next grid barrier), per
+  // token of the step. Routed stages: the expert slot's j-th token is tl[u][j]; the down
+  // projection's partials carry that token's gate.
   __device__ __forceinline__ void flush(int kind, const WGeo& g, int seg, int first, int U, const float (&acc)[TPT]) {
     if (dead) return;
-    const int slot = contrib_slot(blockIdx.x, first, seg * g.kbs, g.T, gridDim.x);
+    const int slot = wcontrib_slot(g, blockIdx.x, first, seg, gridDim.x);
     float* dst = part_of(p, kind) + (size_t)(seg * g.S + slot) * p.MB * kTileRows;
     const int row = 32 * (warp & 3) + lane, h = warp >> 2;
-    int u = -1;
-    unsigned long long mask = ~0ull;
-    if (kind == K_RTGU) u = seg / p.n_rb_gu;
-    if (kind == K_D) u = seg / p.n_rb_d;
-    if (u >= 0) mask = m->umask[u];
-    // (the thread's tokens h TPT + j: one base address, constant offsets)
-    float* base = dst + (size_t)h * TPT * kTileRows + row;
-    const unsigned long long mh = mask >> (h * TPT);
-    const int nb = p.B - h * TPT;
+    // accumulator 4c + j holds the tile's token 8c + 4h + j
+    if (kind == K_RTGU || kind == K_D) {
+      const int u = seg / (kind == K_RTGU ? p.n_rb_gu : p.n_rb_d);
+      const int n = __popcll(m->umask[u]);
+      const uint8_t* tl = slot_tokens() + u * kWideMax + 4 * h;
 #pragma unroll
-    for (int j = 0; j < TPT; ++j) {
-      if (j < nb && ((mh >> j) & 1ull)) {
-        float v = acc[j];
-        if (kind == K_D && u < U) v *= gate_of(h * TPT + j, u);
-        base[j * kTileRows] = v;
+      for (int k = 0; k < TPT; ++k) {
+        const int jl = 8 * (k >> 2) + (k & 3);  // (local token 8c + 4h + j, minus 4h)
+        if (jl + 4 * h < n) {
+          const int t = tl[jl];
+          float v = acc[k];
+          if (kind == K_D && u < U) v *= gate_of(t, u);
+          dst[(size_t)t * kTileRows + row] = v;
+        }
       }
+      return;
+    }
+    // (the thread's tokens: one base address, constant offsets)
+    float* base = dst + (size_t)4 * h * kTileRows + row;
+    const int nb = p.B - 4 * h;
+#pragma unroll
+    for (int k = 0; k < TPT; ++k) {
+      const int jl = 8 * (k >> 2) + (k & 3);
+      if (jl < nb) base[jl * kTileRows] = acc[k];
     }
   }
 
+  // shared-memory tables of the routing phases (in red): expert marks, the SwiGLU (slot, token)
+  // pairs, each slot's tokens in ascending order
+  __device__ __forceinline__ int* route_marks() const { return reinterpret_cast<int*>(red); }
+  __device__ __forceinline__ int* swiglu_pairs() const { return reinterpret_cast<int*>(red) + kMaxExperts; }
+  __device__ __forceinline__ uint8_t* slot_tokens() const {
+    return reinterpret_cast<uint8_t*>(reinterpret_cast<int*>(red) + kMaxExperts + kWideMax * 17);
+  }
+
   __device__ void gemv(int kind, int U) {
-    const WGeo g = wgeo(p, kind, U, gridDim.x);
-    const int t0 = range_lo(g.T, blockIdx.x, gridDim.x), t1 = range_lo(g.T, blockIdx.x + 1, gridDim.x);
+    const unsigned long long cs = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
+    WGeo g = wgeo(p, kind, U, gridDim.x);
+    wsplit(g, m, p, kind, U, gridDim.x);
+    const int t0 = wstart(g, blockIdx.x, gridDim.x), t1 = wstart(g, blockIdx.x + 1, gridDim.x);
     // the exponents of the B blocks the CTA's tiles read (written before the last barrier)
     int u_lo = 0;
     if (t1 > t0 && !dead) {
       const int8_t* src;
       int rows;
-      if (kind == K_D) {
+      if (kind == K_D || kind == K_RTGU) {
         u_lo = t0 / g.tpe;
         const int u_hi = (t1 - 1) / g.tpe;
-        rows = (u_hi - u_lo + 1) * p.kb_i;
-        src = w.exh + (size_t)u_lo * p.kb_i * kWideMax;
+        rows = (u_hi - u_lo + 1) * g.kbs;
+        src = (kind == K_D ? w.exh : w.exg) + (size_t)u_lo * g.kbs * kWideMax;
       } else {
         rows = g.kbs;
         src = kind == K_O ? w.exo : w.exx;
@@ -812,19 +1017,31 @@ struct WConsumer {
     for (int t = t0;;) {
       const int seg = t < t1 ? t / g.kbs : -1;
       if (t == t1 || seg != seg_cur) {
+        const unsigned long long cf = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
         if (seg_cur >= 0) flush(kind, g, seg_cur, seg_first, U, acc);
+        if (DEC_TRACE && kind == K_RTGU && tid == 0) tw_flush += gtimer() - cf;
         if (t == t1) break;
         seg_cur = seg;
         seg_first = t;
 #pragma unroll
         for (int j = 0; j < TPT; ++j) acc[j] = 0.f;
       }
-      const int n = min(GT, min(t1, (seg + 1) * g.kbs) - t);
-      epilogue(gseq++, n, kind, g, t, u_lo, acc);
+      const GroupShape gsh = group_shape<NR>(p, m, kind, g, t);
+      const int n = min(gsh.gt, min(t1, (seg + 1) * g.kbs) - t);
+      epilogue(gseq++, n, gsh.w, kind, g, t, u_lo, acc);
       t += n;
     }
-    ring_skip((t1 - t0 + ST - 1) / ST);
+    // the stage's slots (freed by the MMA warp): keep the ring position in step
+    ring_skip(range_slots<NR>(p, m, kind, g, t0, t1));
     dead = cons_any(dead);
+    if (DEC_TRACE && kind == K_RTGU && tid == 0) {
+      const unsigned long long dt = gtimer() - cs;
+      tw_stage += dt;
+      if (DEC_STAMPS && ++rtgu_seen == 4) {  // (layer 3: start and end of every CTA's stage)
+        p.trace[kTraceSlots + blockIdx.x] = cs;
+        p.trace[kTraceSlots + gridDim.x + blockIdx.x] = cs + dt;
+      }
+    }
   }
 
   // ---- attention
@@ -1274,8 +1491,9 @@ struct WConsumer {
   // selections as slots and gates, the tokens of each slot, and the (slot, token) pairs of the
   // SwiGLU phase (the shared expert: slot U, every token). Dense FFN: slot 0, every token.
   __device__ void local_routing() {
-    int* mark = reinterpret_cast<int*>(red);  // [kMaxExperts]
-    int* pairs = mark + kMaxExperts;          // [kWideMax * 17]
+    int* mark = route_marks();
+    int* pairs = swiglu_pairs();
+    uint8_t* tl = slot_tokens();
     const unsigned long long all = p.B >= 64 ? ~0ull : ((1ull << p.B) - 1ull);
     if (p.dense) {
       if (tid == 0) {
@@ -1283,8 +1501,12 @@ struct WConsumer {
         m->umask[0] = all;
         m->npairs = p.B;
       }
-      for (int t = tid; t < p.B; t += kConsumerWarps * 32) pairs[t] = t;
+      for (int t = tid; t < p.B; t += kConsumerWarps * 32) {
+        pairs[t] = t;
+        tl[t] = (uint8_t)t;
+      }
       cons_sync();
+      slot_weights(0);
       return;
     }
     for (int i = tid; i < kMaxExperts; i += kConsumerWarps * 32) mark[i] = 0;
@@ -1324,7 +1546,51 @@ struct WConsumer {
       m->npairs = p.B * p.topk + (p.nsh ? p.B : 0);
     }
     cons_sync();
+    // each slot's tokens in ascending order (thread u scans its mask)
+    for (int u = tid; u <= U; u += kConsumerWarps * 32) {
+      unsigned long long mk = (u < U || p.nsh) ? m->umask[u] : 0ull;
+      for (int j = 0; mk; ++j, mk &= mk - 1) tl[u * kWideMax + j] = (uint8_t)(__ffsll((long long)mk) - 1);
+    }
+    cons_sync();
+    slot_weights(U);
     if (tid == 0) mbar_arrive(&m->rt_bar);  // the producer and the MMA warp may take the routed experts
+  }
+
+  // the expert slots' tile weights for the work-weighted split (wsplit): B rows / 16, at least 2
+  __device__ void slot_weights(int U) {
+    if (tid == 0) {
+      int acc = 0, wm = 0;
+      m->pw[0] = 0;
+      for (int u = 0; u < U + p.nsh; ++u) {
+        const int wu = max(2, min(NR, brows(__popcll(m->umask[u]))) / 16);
+        acc += wu;
+        m->pw[u + 1] = acc;
+        wm = max(wm, wu);
+      }
+      m->wmax = wm;
+    }
+    cons_sync();
+  }
+
+  // The B rows of each routed slot's tokens, gathered from pbx into compact blocks (pbg, exg):
+  // warp unit (slot u, k block kb) copies 2 x 8 16-byte chunks per token.
+  __device__ void gather(int U) {
+    const uint8_t* tl = slot_tokens();
+    const int nw = gridDim.x * kConsumerWarps;
+#pragma unroll 1
+    for (int wu = blockIdx.x * kConsumerWarps + warp; wu < U * p.kb_d && !dead; wu += nw) {
+      const int u = wu / p.kb_d, kb = wu % p.kb_d;
+      const int n = __popcll(m->umask[u]);
+      const uint8_t* src = w.pbx + (size_t)kb * PBS;
+      uint8_t* dst = w.pbg + ((size_t)u * p.kb_d + kb) * PBS;
+      for (int i = lane; i < 16 * n; i += 32) {
+        const int r = i >> 3, c = (i & 7) * 16;  // local row r (token r / 2, piece r % 2), chunk c
+        const int t = tl[u * kWideMax + (r >> 1)];
+        *reinterpret_cast<uint4*>(dst + boff(r, c)) = ldcg4(src + boff(2 * t + (r & 1), c));
+      }
+      for (int j = lane; j < n; j += 32)
+        w.exg[((size_t)u * p.kb_d + kb) * kWideMax + j] = __ldcg(w.exx + (size_t)kb * kWideMax + tl[u * kWideMax + j]);
+    }
   }
   __device__ __forceinline__ static int ldcg_i(const int32_t* a) { return __ldcg(a); }
 
@@ -1332,8 +1598,10 @@ struct WConsumer {
   // bf16(silu(gate) * up) from the gate/up partials (each row block: 64 gate rows, then the
   // matching 64 up rows), as B blocks of the slot's down projection.
   __device__ void swiglu_pack(int U) {
-    const int* pairs = reinterpret_cast<const int*>(red) + kMaxExperts;
-    const WGeo gr = wgeo(p, K_RTGU, U, gridDim.x), gs = wgeo(p, K_SHGU, 0, gridDim.x);
+    const int* pairs = swiglu_pairs();
+    WGeo gr = wgeo(p, K_RTGU, U, gridDim.x);
+    wsplit(gr, m, p, K_RTGU, U, gridDim.x);
+    const WGeo gs = wgeo(p, K_SHGU, 0, gridDim.x);
     const size_t pst = (size_t)p.MB * kTileRows;
     const int nw = gridDim.x * kConsumerWarps;
     const int nu = m->npairs * p.kb_i;
@@ -1347,7 +1615,7 @@ struct WConsumer {
       const int rbg = j0 / 64, r = j0 % 64;
       const WGeo& g = sh ? gs : gr;
       const int seg = sh ? rbg : u * p.n_rb_gu + rbg;
-      const int nc = n_contrib(seg * g.kbs, g.kbs, g.T, gridDim.x);
+      const int nc = wn_contrib(g, seg, gridDim.x);
       const float* src = (sh ? p.part_shgu : p.part_rtgu) + ((size_t)seg * g.S * p.MB + t) * kTileRows;
       float gv[4] = {0.f, 0.f, 0.f, 0.f}, uv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
@@ -1360,8 +1628,10 @@ struct WConsumer {
       float f[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) f[i] = bf16f(f2bf((gv[i] / (1.0f + expf(-gv[i]))) * uv[i]));
+      // the slot's j-th token (ascending): rows 2j, 2j + 1
+      const int j = __popcll(m->umask[u] & ((1ull << t) - 1ull));
       const size_t blk = (size_t)u * p.kb_i + kb;
-      pack4(w.pbh + blk * PBS, w.exh + blk * kWideMax + t, t, lane * 4, f);
+      pack4(w.pbh + blk * PBS, w.exh + blk * kWideMax + j, j, lane * 4, f);
     }
   }
 
@@ -1369,7 +1639,8 @@ struct WConsumer {
   // already) and of the shared expert, rounded to bf16; then the next layer's (or the final)
   // RMSNorm as B blocks.
   __device__ void layer_out(int l, int U) {
-    const WGeo gd = wgeo(p, K_D, U, gridDim.x);
+    WGeo gd = wgeo(p, K_D, U, gridDim.x);
+    wsplit(gd, m, p, K_D, U, gridDim.x);
     const size_t pst = (size_t)p.MB * kTileRows;
     const int nsel = p.dense ? 0 : p.topk;
     for (int t = blockIdx.x; t < p.B && !dead; t += gridDim.x) {
@@ -1385,7 +1656,7 @@ struct WConsumer {
         for (int s = 0; s < nsel + p.nsh; ++s) {
           const int u = s < nsel ? (int)m->wsel[t][s] : U;
           const int seg = u * p.n_rb_d + rb;
-          const int nc = n_contrib(seg * gd.kbs, gd.kbs, gd.T, gridDim.x);
+          const int nc = wn_contrib(gd, seg, gridDim.x);
           const float* src = p.part_d + ((size_t)seg * gd.S * p.MB + t) * kTileRows + k % kTileRows;
 #pragma unroll 1
           for (int c = 0; c < nc; ++c) {
@@ -1459,6 +1730,7 @@ struct WConsumer {
   }
 
   __device__ void run() {
+    if (DEC_TRACE && blockIdx.x == 0 && tid == 0) p.trace[0] = gtimer();
     if (warp == 0) tmem_alloc(&m->tmem_base, kTmemCols);
     tc_fence_before();
     cons_sync();
@@ -1487,6 +1759,8 @@ struct WConsumer {
       gbar();
       local_routing();
       const int U = m->U;
+      gather(U);
+      gbar();
       if (!p.dense) gemv(K_RTGU, U);
       gbar();
       swiglu_pack(U);
@@ -1509,6 +1783,12 @@ struct WConsumer {
     }
     if (blockIdx.x == 0 && tid < p.B && !dead) p.lengths[p.seq0 + tid] = m->len[tid] + 1;
     if (blockIdx.x == 0 && tid == 0) p.layer_ts[p.L + 1] = gtimer();
+    if (DEC_TRACE && blockIdx.x == 0 && tid == 0) {
+      p.trace[kWaitTrace + 4] = tw_prod;
+      p.trace[kWaitTrace + 5] = tw_stage;
+      p.trace[kWaitTrace + 6] = tw_ld;
+      p.trace[kWaitTrace + 7] = tw_flush;
+    }
     // TMEM is freed once the MMA warp has finished (bounded wait)
     if (warp == 0) {
       if (lane == 0) {

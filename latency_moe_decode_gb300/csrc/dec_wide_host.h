@@ -16,7 +16,7 @@ int smem_bytes(int ring, int nr, int hd, int group);
 int stage_slots(const KParams& p, int kind, int U, int G);
 int stage_tiles(const KParams& p, int kind, int U, int G);
 
-constexpr int kBarsPerLayerHost = 11;
+constexpr int kWideTopkHost = 8;  // the wide kernel's experts per token (its routing tables)
 
 }  // namespace wide
 }  // namespace dec
