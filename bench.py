@@ -86,7 +86,7 @@ def measured_peaks():
 def profile_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, only if it was taken on the
     current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "decode_step_kernel_traffic.json")
+    path = os.path.join(ROOT, "profiles", "dram_traffic_per_launch.json")
     try:
         d = json.load(open(path))
     except Exception:
