@@ -126,6 +126,8 @@ dec_status dec_validate_cfg(const dec_model_cfg* cfg);
    queued on `stream` and synchronised before return. *out receives the engine (NULL on
    failure).
    Environment, read here: DEC_TIMEOUT_MS bounds every device-side wait (default 1000);
+   DEC_INFLIGHT / DEC_WIDE_INFLIGHT set how many ring slots one CTA keeps in flight (defaults 2
+   and 4; tuning only);
    DEC_TEST_SKIP_ARRIVAL=1 (tests of the failure path only) makes the CTA holding the first
    q/k/v tile withhold that partial sum's arrival in layer 0, so the waits for it run out after
    DEC_TIMEOUT_MS and the step ends with DEC_ERR_TIMEOUT instead of hanging;

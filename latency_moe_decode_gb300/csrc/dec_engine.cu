@@ -146,6 +146,7 @@ struct dec_engine {
   int wsmem[3] = {0, 0, 0}, wring[3] = {0, 0, 0};
   int wnch_max = 1;
   int winflight = 4;  // copies one CTA of the wide kernel keeps in flight (DEC_WIDE_INFLIGHT)
+  int inflight = kSlotsInFlight;  // the same for decode_step_kernel (DEC_INFLIGHT)
   std::vector<int32_t> lengths;
   unsigned epoch = 0;
   // Counters that grow across steps (each arrival adds its tile count, at most kbs per row block
@@ -705,6 +706,10 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     // tests only: the first q/k/v tile's layer-0 arrival is withheld, so the waits for it run out
     const char* sk = getenv("DEC_TEST_SKIP_ARRIVAL");
     p.test_skip = (sk && atoi(sk) == 1) ? 1 : 0;
+    if (const char* fl = getenv("DEC_INFLIGHT")) {
+      const int v = atoi(fl);
+      if (v >= 1 && v <= kMaxRing) e->inflight = v;
+    }
   }
   // ---- the wide kernels: steps of more than kMaxBatch tokens (own partial sums with a token
   // stride of max_batch, B operand blocks, exchange buffers)
@@ -892,7 +897,7 @@ dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t*
   p.epoch = e->epoch + 1;
   e->epoch += (unsigned)nsteps;
   p.ring = e->ring[bi];
-  p.inflight = std::min(p.ring, kSlotsInFlight);
+  p.inflight = std::min(p.ring, e->inflight);
   p.nch = std::max(1, std::min(e->nch_max, e->grid / (B * c.n_kv_heads)));
   void* args[] = {&p};
   cudaError_t ce = cudaLaunchCooperativeKernel((const void*)e->kern[bi], dim3(e->grid), dim3(kThreads), args,

@@ -718,6 +718,7 @@ struct WConsumer {
   unsigned nstage = 0;  // GEMV stages begun (thread 0)
   unsigned long long tw_prod = 0, tw_stage = 0, tw_ld = 0, tw_flush = 0;  // diagnostics (thread 0): routed gate/up
   int rtgu_seen = 0;
+  unsigned long long tw_kv = 0, tw_attn = 0, tw_pro = 0, tw_post = 0;  // diagnostics: attention
   uint32_t tmem = 0;
 
   __device__ WConsumer(const KParams& p_, const WideParams& w_, uint8_t* r, uint64_t* f, uint64_t* e, float* rd,
@@ -729,7 +730,9 @@ struct WConsumer {
   }
 
   __device__ const uint8_t* wait_item() {
+    const unsigned long long c0 = DEC_TRACE ? gtimer() : 0;
     if (!dead && !mbar_wait(&full[rslot], rpar, p, 52)) dead = true;
+    if (DEC_TRACE && tid == 0) tw_kv += gtimer() - c0;
     return ring + (size_t)rslot * SB;
   }
   __device__ void release_item() {
@@ -1132,11 +1135,14 @@ struct WConsumer {
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);
     const unsigned row_bytes = HD * 2;
     const int NU = p.B * p.hkv * w.nch;
+    const unsigned long long ca = DEC_TRACE ? gtimer() : 0;
 #pragma unroll 1
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
       const WUnit a = wunit(p, w, m, u);
       float* qkvn = red;
+      const unsigned long long cp = DEC_TRACE ? gtimer() : 0;
       if (a.tile1 > a.tile0) prologue(l, a, qkvn);  // (CTA barriers inside: no branch on `dead`)
+      if (DEC_TRACE && tid == 0) tw_pro += gtimer() - cp;
       float q[G][DPL];
 #pragma unroll
       for (int h = 0; h < G; ++h)
@@ -1260,6 +1266,7 @@ struct WConsumer {
         release_item();
       }
       dead = cons_any(dead);  // (one verdict: the packing below is warp-collective)
+      const unsigned long long cq = DEC_TRACE ? gtimer() : 0;
       // the warps' states -> the unit's (max, sum, unnormalised output) per head
       float* wst = red;
 #pragma unroll
@@ -1333,7 +1340,9 @@ struct WConsumer {
         }
       }
       cons_sync();
+      if (DEC_TRACE && tid == 0) tw_post += gtimer() - cq;
     }
+    if (DEC_TRACE && tid == 0) tw_attn += gtimer() - ca;
   }
 
   // Chunk merge (more than one chunk per sequence and KV head): warp unit (token b, k block kb
@@ -1788,6 +1797,10 @@ struct WConsumer {
       p.trace[kWaitTrace + 5] = tw_stage;
       p.trace[kWaitTrace + 6] = tw_ld;
       p.trace[kWaitTrace + 7] = tw_flush;
+      p.trace[kWaitTrace + 8] = tw_kv;
+      p.trace[kWaitTrace + 9] = tw_attn;
+      p.trace[kWaitTrace + 10] = tw_pro;
+      p.trace[kWaitTrace + 11] = tw_post;
     }
     // TMEM is freed once the MMA warp has finished (bounded wait)
     if (warp == 0) {
