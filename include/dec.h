@@ -129,7 +129,8 @@ dec_status dec_validate_cfg(const dec_model_cfg* cfg);
    DEC_INFLIGHT / DEC_WIDE_INFLIGHT set how many ring slots one CTA keeps in flight (defaults 2
    and 4; tuning only);
    DEC_TEST_SKIP_ARRIVAL=1 (tests of the failure path only) makes the CTA holding the first
-   q/k/v tile withhold that partial sum's arrival in layer 0, so the waits for it run out after
+   q/k/v tile withhold that partial sum's arrival in layer 0 (in a step of more than 8 tokens:
+   CTA 0 its arrival at the first grid barrier), so the waits for it run out after
    DEC_TIMEOUT_MS and the step ends with DEC_ERR_TIMEOUT instead of hanging;
    DEC_EPOCH_LIMIT lowers the number of steps after which a step first zeroes the engine's
    cross-step counters and flags (a cudaMemsetAsync on the step's stream) and restarts its epoch

@@ -94,11 +94,13 @@ struct Misc {
   float rsum[kConsumerWarps][kMaxBatch];
   int tok[kMaxBatch];
   // tensor-core tiles: the scale exponent a of each token's staged k block (its pieces encode
-  // x * 2^a), the consumers -> MMA warp "stage operand ready" barrier (one phase per GEMV stage),
-  // the MMA warp's "done" barrier, per group of TMEM slices a "products ready" (MMA commit) and
-  // a "products read" (one arrival per consumer warp) barrier, and the TMEM base address
+  // x * 2^a), the count of GEMV stages whose operand the consumers have staged (consumers -> MMA
+  // warp; a count, so that two stages staged before the MMA warp looks cannot be mistaken for
+  // one), the MMA warp's "done" barrier, per group of TMEM slices a "products ready" (MMA commit)
+  // and a "products read" (one arrival per consumer warp) barrier, and the TMEM base address
   int8_t xexp[kMaxBatch][kMaxKb];
-  uint64_t b_ready, mma_done;
+  unsigned stages_staged;
+  uint64_t mma_done;
   uint64_t tfull[kNG], tempty[kNG];
   float2 hdr[kNG][kGT];  // the block scales of each group's tiles (their slots may be refilled first)
   uint32_t tmem_base;
@@ -629,6 +631,7 @@ struct Consumer {
   unsigned ep = 0;    // this step's epoch (resident steps: the launch's epoch + steps done)
   int soff = 0;       // resident steps done in this launch
   unsigned gseq = 0;  // groups of tiles handed over so far (slot of TMEM slices, barrier phases)
+  unsigned nstaged = 0;  // GEMV stages staged so far (thread 0)
   uint32_t tmem = 0;
   BGeo bg;
 
@@ -1174,7 +1177,11 @@ struct Consumer {
     const int G_ = gridDim.x;
     const int t0 = range_lo(g.T, blockIdx.x, G_), t1 = range_lo(g.T, blockIdx.x + 1, G_);
     cons_sync();  // the stage's activations are staged (and fenced for the tensor cores)
-    if (kTC && tid == 0) mbar_arrive(&m->b_ready);
+    if (kTC && tid == 0) {
+      ++nstaged;
+      __threadfence_block();
+      *reinterpret_cast<volatile unsigned*>(&m->stages_staged) = nstaged;
+    }
     trace(kind << 4);
     float gmul[BM];
     float acc[4];
@@ -2274,9 +2281,29 @@ struct MmaIssuer {
   // The stage's tiles in groups of up to kGT per segment (as the consumers take them): each tile
   // gets TMEM slice (group slot) * kGT + i; a slot is freed (commit on its mempty barrier) after
   // its last tile's MMAs, a group announced (commit on tfull) after its last tile's.
+  // wait (bounded) until the consumers have staged the operand of GEMV stage number `stage`
+  __device__ void wait_staged() {
+    if (dead) return;
+    const unsigned long long t0 = gtimer();
+    for (unsigned it = 1; *reinterpret_cast<volatile unsigned*>(&m->stages_staged) < stage; ++it) {
+      if ((it & 63u) == 0) {
+        if (aborted(p)) {
+          dead = true;
+          return;
+        }
+        if (gtimer() - t0 > p.timeout_ns) {
+          raise_err(p, kDevTimeout, 26);
+          dead = true;
+          return;
+        }
+      }
+    }
+    __threadfence_block();
+  }
+
   __device__ void gemv(int kind, int U) {
-    if (!dead && !mbar_wait(&m->b_ready, stage & 1, p, 26)) dead = true;
     ++stage;
+    wait_staged();
     tc_fence_after();
     tmem = m->tmem_base;
     const StageGeo g = stage_geo(p, kind, U);
@@ -2390,7 +2417,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
       mbar_init(&mempty[s], 1);
     }
     mbar_init(&m->rt_bar, 1);
-    mbar_init(&m->b_ready, 1);
+    m->stages_staged = 0;
     mbar_init(&m->mma_done, 1);
     for (int i = 0; i < kNG; ++i) {
       mbar_init(&m->tfull[i], 2);  // MMA commit + the MMA thread's release of the headers
