@@ -416,7 +416,7 @@ def run_ours(args):
                     "samples": len(layer_ts),
                     "source": "first CTA's %globaltimer when each layer's input became final, median over "
                               "decode tokens of an untimed replay of the step"}
-    wide = batch > 8  # the wide kernel: one launch per decode step
+    wide = batch >= 8  # the wide kernel (batches of 8 and more): one launch per decode step
     launches = (n_dec if headless or wide else 1) * args.steps
     per_launch_s = total / (args.steps * world) / n_dec
     achieved = bytes_per_step / n_dec / per_launch_s / 1e9

@@ -147,6 +147,10 @@ struct dec_engine {
   int wnch_max = 1;
   int winflight = 4;  // copies one CTA of the wide kernel keeps in flight (DEC_WIDE_INFLIGHT)
   int inflight = kSlotsInFlight;  // the same for decode_step_kernel (DEC_INFLIGHT)
+  // decode steps of at least this many tokens take the wide kernel (measured at 1k context on
+  // the 8-layer stack: 8 tokens 3921 vs 3313 tokens/s on decode_step_kernel, 4 tokens 2494 vs
+  // 2663, 2 tokens 1525 vs 2001)
+  int wide_min = wide::kWideMinBatch;
   std::vector<int32_t> lengths;
   unsigned epoch = 0;
   // Counters that grow across steps (each arrival adds its tile count, at most kbs per row block
@@ -378,6 +382,8 @@ dec_status dec_validate_cfg(const dec_model_cfg* c) {
     return DEC_ERR_UNSUPPORTED;
   }
   if (c->max_batch > kWideMax || c->n_kv_heads > 64 || c->hidden > kMaxHidden) return DEC_ERR_UNSUPPORTED;
+  // decode batches above 8 (the wide kernel) hold at most 8 experts per token
+  if (c->max_batch > kMaxBatch && c->n_experts > 0 && c->top_k > wide::kWideTopkHost) return DEC_ERR_UNSUPPORTED;
   return DEC_OK;
 }
 
@@ -710,10 +716,41 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
       const int v = atoi(fl);
       if (v >= 1 && v <= kMaxRing) e->inflight = v;
     }
+    if (const char* wm = getenv("DEC_WIDE_MIN_BATCH")) {
+      const int v = atoi(wm);
+      if (v >= 2 && v <= kMaxBatch + 1) e->wide_min = v;
+    }
   }
   // ---- the wide kernels: steps of more than kMaxBatch tokens (own partial sums with a token
   // stride of max_batch, B operand blocks, exchange buffers)
-  if (c.max_batch > kMaxBatch) {
+  if (c.max_batch >= e->wide_min) {
+    // the wide kernel's shape limits; an engine of at most 8 sequences that exceeds them keeps
+    // every decode step on decode_step_kernel
+    const int umax_w = dense ? 0 : std::min(c.n_experts, c.max_batch * c.top_k);
+    const char* why = nullptr;
+    {
+      const long long t_max = std::max((long long)(umax_w + p.nsh) * p.n_rb_d * p.kb_i,
+                                       (long long)std::max(1, umax_w) * p.n_rb_gu * p.kb_d);
+      if ((t_max + 1) * G >= (1LL << 31)) why = "too many tiles in one stage";
+      // the work-weighted split's positions (tiles x weight <= 8) times the grid stay 32-bit
+      if ((t_max * 8 + 1) * G >= (1LL << 32)) why = "expert stage too large";
+      if (!dense && c.top_k > wide::kWideTopkHost) why = "more than 8 experts per token";
+      // the exponents a CTA's expert tiles read (the expert slots its range spans) fit its table
+      for (int U = 0; U <= umax_w && !why; ++U)
+        for (int st = 0; st < 2; ++st) {
+          const int kbs = st ? p.kb_d : p.kb_i, tpe = (st ? p.n_rb_gu : p.n_rb_d) * kbs;
+          const int T = (st ? U : U + p.nsh) * tpe;
+          for (int cta = 0; cta < G; ++cta) {
+            const int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
+            if (t1 > t0 && ((t1 - 1) / tpe - t0 / tpe + 1) * kbs > kMaxKb) why = "expert stage too narrow";
+          }
+        }
+    }
+    if (why && c.max_batch > kMaxBatch)
+      return bail(fail(e, DEC_ERR_UNSUPPORTED, std::string("decode batches above 8: ") + why));
+    if (why) e->wide_min = kMaxBatch + 1;
+  }
+  if (c.max_batch >= e->wide_min) {
     KParams& w = e->wbase;
     w = p;
     w.MB = c.max_batch;
@@ -729,26 +766,6 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     };
 #define WZ(ptr, bytes) \
   if ((st = wz(&(ptr), (bytes))) != DEC_OK) return bail(st);
-    {
-      const long long t_max = std::max((long long)(umax_w + p.nsh) * p.n_rb_d * p.kb_i,
-                                       (long long)std::max(1, umax_w) * p.n_rb_gu * p.kb_d);
-      if ((t_max + 1) * G >= (1LL << 31)) return bail(fail(e, DEC_ERR_UNSUPPORTED, "too many tiles in one stage"));
-      // the work-weighted split's positions (tiles x weight <= 8) times the grid stay 32-bit
-      if ((t_max * 8 + 1) * G >= (1LL << 32)) return bail(fail(e, DEC_ERR_UNSUPPORTED, "expert stage too large"));
-      if (!dense && c.top_k > wide::kWideTopkHost)
-        return bail(fail(e, DEC_ERR_UNSUPPORTED, "batches above 8 take at most 8 experts per token"));
-      // the exponents a CTA's expert tiles read (the expert slots its range spans) fit its table
-      for (int U = 0; U <= umax_w; ++U)
-        for (int st = 0; st < 2; ++st) {
-          const int kbs = st ? p.kb_d : p.kb_i, tpe = (st ? p.n_rb_gu : p.n_rb_d) * kbs;
-          const int T = (st ? U : U + p.nsh) * tpe;
-          for (int cta = 0; cta < G; ++cta) {
-            const int t0 = range_lo_h(T, cta, G), t1 = range_lo_h(T, cta + 1, G);
-            if (t1 > t0 && ((t1 - 1) / tpe - t0 / tpe + 1) * kbs > kMaxKb)
-              return bail(fail(e, DEC_ERR_UNSUPPORTED, "expert stage too narrow for the exponent table"));
-          }
-        }
-    }
     const size_t PBS = (size_t)nr_max * 128;
     const size_t nbx = p.kb_d, nbo = p.kb_o, nbh = (size_t)wp.hmax * p.kb_i;
     const size_t nbg = (size_t)std::max(1, umax_w) * p.kb_d;
@@ -827,7 +844,7 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
 
 namespace {
 
-// One launch of the wide kernel: B = 9 .. 64 tokens, one per slot seq0 .. seq0 + B - 1.
+// One launch of the wide kernel: B (up to 64) tokens, one per slot seq0 .. seq0 + B - 1.
 dec_status launch_wide(dec_engine* e, int B, int seq0, const int32_t* tokens, const void* hidden_in, float* logits,
                        int32_t* next_tokens, void* hidden_out, cudaStream_t s) {
   const dec_model_cfg& c = e->cfg;
@@ -867,12 +884,13 @@ dec_status launch_step(dec_engine* e, int B, int seq0, bool mpos, const int32_t*
                        float* logits, int32_t* next_tokens, void* hidden_out, int32_t* accepted, cudaStream_t s,
                        int nsteps = 1) {
   const dec_model_cfg& c = e->cfg;
-  if (B > kMaxBatch) {
-    // (multi-position steps hold at most DEC_MAX_STEP_TOKENS <= kMaxBatch tokens; generation
-    // loops one step per launch at these batches)
-    if (mpos || accepted || nsteps != 1) return fail(e, DEC_ERR_ARG, "wide steps take one decode position per slot");
+  if (B >= e->wide_min && !mpos) {
+    // (multi-position steps hold at most DEC_MAX_STEP_TOKENS <= kMaxBatch tokens and stay on
+    // decode_step_kernel; generation loops one step per launch at these batches)
+    if (accepted || nsteps != 1) return fail(e, DEC_ERR_ARG, "wide steps take one decode position per slot");
     return launch_wide(e, B, seq0, tokens, hidden_in, logits, next_tokens, hidden_out, s);
   }
+  if (B > kMaxBatch) return fail(e, DEC_ERR_ARG, "more tokens than one step of decode_step_kernel takes");
   int bi = 0;
   while (kBmChoices[bi] < B) ++bi;
   KParams p = e->base;
@@ -1117,7 +1135,7 @@ dec_status dec_generate_device(dec_engine* e, const int32_t* first, int32_t batc
   // resident steps: one launch runs up to epoch_limit steps (normally all of them); wide batches
   // one step per launch, the tokens chained through d_hist on the device
   for (int i = 0; i < n_steps;) {
-    const int n = batch > kMaxBatch ? 1 : std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
+    const int n = batch >= e->wide_min ? 1 : std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
     dec_status st = launch_step(e, batch, 0, false, e->d_hist + (size_t)i * MB, nullptr, nullptr,
                                 e->d_hist + (size_t)(i + 1) * MB, nullptr, nullptr, s, n);
     if (st != DEC_OK) return st;
@@ -1143,7 +1161,7 @@ dec_status dec_generate(dec_engine* e, const int32_t* first, int32_t batch, int3
   const int MB = e->rows;
   DEC_CUDA(cudaMemcpyAsync(e->d_hist, first, sizeof(int32_t) * batch, cudaMemcpyHostToDevice, s));
   for (int i = 0; i < n_steps;) {
-    const int n = batch > kMaxBatch ? 1 : std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
+    const int n = batch >= e->wide_min ? 1 : std::min<int>(n_steps - i, (int)std::max(1u, e->epoch_limit));
     dec_status st = launch_step(e, batch, 0, false, e->d_hist + (size_t)i * MB, nullptr, nullptr,
                                 e->d_hist + (size_t)(i + 1) * MB, nullptr, nullptr, s, n);
     if (st != DEC_OK) return st;

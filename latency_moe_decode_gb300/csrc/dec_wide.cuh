@@ -1,4 +1,4 @@
-// The decode step for 9 .. 64 tokens (sequences side by side): the tensor-core expert GEMMs of a
+// The decode step for 8 .. 64 tokens (sequences side by side): the tensor-core expert GEMMs of a
 // batched decode ("vLLM's Kimi K3 Backend Hits 842 Tokens per Second", section "A narrow
 // deployment lane": decode batches up to 64; section "Throughput holds across the tested range").
 //

@@ -60,6 +60,8 @@ def test_validate_cfg(lib):
     assert v(max_batch=9) == 0                 # 9 .. 64: the wide kernels
     assert v(max_batch=64) == 0
     assert v(max_batch=65) == -5
+    assert v(max_batch=16, n_experts=64, top_k=9) == -5  # the wide kernel: at most 8 experts per token
+    assert v(max_batch=8, n_experts=64, top_k=9) == 0     # (8 sequences: decode_step_kernel instead)
     assert v(hidden=8192) == -5             # above the hidden sizes the kernel handles
     assert v(n_shared=2) == -5
     assert v(n_experts=200, top_k=8) == -5
