@@ -1,4 +1,4 @@
-"""GPU parity of the wide kernel (decode steps of 9 .. 64 sequences: every GEMV on the tensor cores
+"""GPU parity of the wide kernel (decode steps of 8 .. 64 sequences: every GEMV on the tensor cores
 with the step's tokens as N, tokens grouped per routed expert) against the CPU oracle, through
 the C ABI. Each sequence has its own seeded KV history and is compared with the oracle's decode
 of that sequence alone.
@@ -159,3 +159,80 @@ def test_wide_moe_layer_full_size(batch):
             compared += 1
         assert eng.get_length(b) == lens[b] + 1
     assert compared >= batch - 2
+
+
+def test_wide_moe8_every_layer_teacher_forced():
+    """Every layer of the full-size 8-layer stack through the wide kernel, 16 sequences side by side
+    (each with its own seeded KV history at context 512), for 2 consecutive tokens: each layer's
+    engine is fed every sequence's oracle input to that layer and keeps its own KV cache; per
+    sequence, the layer output and sublayer delta (rel L2 <= 1e-2), the new K/V rows, the gates and
+    the routing (RouteCheck) against the oracle. Then the LM head, fed each sequence's oracle final
+    hidden state: logits, argmax and hidden state."""
+    from tests.parity import HIDDEN_REL_L2, RouteCheck
+    from tests.test_gpu_parity import _bf16
+    B, ctx, n_tok = 16, 512, 2
+    m_gpu = synth.gen_model(synth.MOE8, seed=0, device="cuda")
+    m_cpu = synth.model_to(m_gpu, "cpu")
+    cfg8 = synth.MOE8.replace(max_ctx=ctx + n_tok + 16, max_batch=B)
+    kvs = [synth.gen_kv(cfg8, ctx, seed=600 + b, device="cuda") for b in range(B)]
+    orc = oracle.Oracle(m_cpu)
+    outs, toks, okvs = [], [], []
+    for b in range(B):
+        kv = orc.new_kv(cfg8.max_ctx)
+        orc.import_kv(kv, kvs[b][0].cpu(), kvs[b][1].cpu(), ctx)
+        tok, ob, tb = 100 + 37 * b, [], []
+        for i in range(n_tok):
+            tb.append(tok)
+            o = orc.decode_step(kv, ctx + i, token=tok, want_trace=True)
+            ob.append(o)
+            tok = o["token"]
+        outs.append(ob)
+        toks.append(tb)
+        okvs.append(kv)
+    cfg1 = synth.MOE_LAYER.replace(max_ctx=cfg8.max_ctx, max_batch=B)
+    rc = RouteCheck()
+    compared = 0
+    for l in range(8):
+        eng = _engine({"cfg": cfg1, "layers": [m_gpu["layers"][l]]}, max_ctx=cfg1.max_ctx, max_batch=B)
+        for b in range(B):
+            eng.prefill_import(kvs[b][0][l:l + 1].contiguous(), kvs[b][1][l:l + 1].contiguous(), seq=b)
+        for i in range(n_tok):
+            lay_in = [bf16_to_f64(t_bits(m_cpu["embed"][toks[b][i]])) if l == 0 else outs[b][i]["trace"]["layer_out"][l - 1]
+                      for b in range(B)]
+            _, _, g = _gpu_step(eng, hidden=_bf16(np.stack(lay_in)).cuda(), batch=B)
+            gi, gg = eng.routing(0)
+            lg = eng.router_logits(0)
+            for b in range(B):
+                o = outs[b][i]
+                where = f"sequence {b} token {i} layer {l}"
+                same = rc.check(gi[b], lg[b], o["trace"]["topk_idx"][l], o["trace"]["router_score"][l], 8, where)
+                assert abs(gg[b].sum() - 1) < 1e-5
+                kg, vg = eng.export_kv(b, 0, ctx + i, 1)
+                assert rel_l2(bf16_to_f64(t_bits(kg)), bf16_to_f64(okvs[b]["k"][l, :, ctx + i])) < 1e-2, where
+                assert rel_l2(bf16_to_f64(t_bits(vg)), bf16_to_f64(okvs[b]["v"][l, :, ctx + i])) < 1e-2, where
+                if same:
+                    compared += 1
+                    gx, ox = bf16_to_f64(g[b]), o["trace"]["layer_out"][l]
+                    assert rel_l2(gx, ox) <= HIDDEN_REL_L2, where
+                    assert rel_l2(gx - lay_in[b], ox - lay_in[b]) <= HIDDEN_REL_L2, f"{where} delta"
+                    order = np.argsort(o["trace"]["topk_idx"][l])
+                    assert np.allclose(gg[b][np.argsort(gi[b])], o["trace"]["topk_gate"][l][order], atol=GATE_ABS), where
+        eng.close()
+    print(f"\nwide teacher-forced layers: {compared} of {8 * n_tok * B} layer outputs compared; {rc.summary()}")
+    assert compared >= 8 * n_tok * B - 8, "too few layer outputs compared"
+    m_head = {"cfg": synth.MOE8.replace(n_layers=1, max_ctx=cfg8.max_ctx, max_batch=B), "layers": [m_gpu["layers"][7]],
+              "embed": m_gpu["embed"], "final_norm": m_gpu["final_norm"], "lm_head": m_gpu["lm_head"]}
+    eng = _engine(m_head, max_ctx=cfg8.max_ctx, max_batch=B)
+    for b in range(B):
+        eng.prefill_import(kvs[b][0][7:8].contiguous(), kvs[b][1][7:8].contiguous(), seq=b)
+    chk = StepCheck()
+    for i in range(n_tok):
+        hin = _bf16(np.stack([outs[b][i]["trace"]["layer_out"][6] for b in range(B)])).cuda()
+        g_logits, g_next, g_hidden = _gpu_step(eng, hidden=hin, batch=B)
+        gi, _ = eng.routing(0)
+        for b in range(B):
+            o = outs[b][i]
+            if set(gi[b].tolist()) == set(o["trace"]["topk_idx"][7].tolist()):
+                chk.add(g_logits[b], o["logits"], g_next[b], o["token"], g_hidden[b], o["hidden"])
+    assert chk.steps >= n_tok * B - 2
+    chk.assert_ok()
