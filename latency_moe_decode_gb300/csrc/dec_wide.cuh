@@ -40,13 +40,12 @@ constexpr int kWideTopk = 8;       // experts per token the wide kernel's routin
 // products, 5: consumers' stage time}
 constexpr int kWaitTrace = 400;
 
-// Ring slot: two weight tiles and a B area. Two tiles whose B blocks fit half the area each share
-// a slot, their blocks side by side (a 32 KB weight hand-off; one SM's streaming rate grows with
-// the bytes per hand-off up to ~32 KB). A wider tile (a dense stage of many tokens, an expert
-// with many) has a slot to itself, its block in the second tile's place. The area is 8 KB (pairs
-// of up to 32 rows, 16 tokens: five slots) except for steps of 17 .. 32 tokens, where 16 KB lets
-// every tile pair up (four slots).
-__host__ __device__ constexpr int b_area(int nr) { return nr == 64 ? 16384 : 8192; }
+// Ring slot: two weight tiles and an 8 KB B area. Two tiles whose B blocks fit half the area each
+// (up to 32 rows, 16 tokens) share a slot, their blocks side by side (a 32 KB weight hand-off;
+// one SM's streaming rate grows with the bytes per hand-off up to ~32 KB). A wider tile (a dense
+// stage of more than 16 tokens, an expert with more) has a slot to itself, its block in the
+// second tile's place. Four slots fit beside the GEMV accumulators (below).
+__host__ __device__ constexpr int b_area(int) { return 8192; }
 __host__ __device__ constexpr int pair_rows(int nr) { return b_area(nr) / 2 / 128; }
 __host__ __device__ constexpr int slot_bytes(int nr) { return 2 * kTileBytes + b_area(nr); }
 
@@ -172,8 +171,12 @@ __device__ __forceinline__ void wsplit(WGeo& g, const M* m, const KParams& p, in
 }
 
 struct WLayout {
-  int ring_off, full_off, empty_off, mempty_off, red_off, misc_off, total;
+  int ring_off, full_off, empty_off, mempty_off, red_off, acc_off, misc_off, total;
 };
+// The GEMV accumulators live in shared memory, not registers: nr / 4 per consumer thread (up to
+// 32) did not fit beside the rest of the kernel's live state at the 168-register cap, and the
+// spills cost more than the shared-memory round trips (measured: 64 tokens 13761 vs 11452
+// tokens/s, 16 tokens 6144 vs 5894).
 __host__ __device__ inline WLayout wlayout(int ring, int nr, int hd, int group) {
   WLayout s;
   s.ring_off = 0;
@@ -186,7 +189,10 @@ __host__ __device__ inline WLayout wlayout(int ring, int nr, int hd, int group) 
   // routing marks, SwiGLU pairs, each expert slot's tokens
   const int pairs = (kMaxExperts + kWideMax * 17) * 4 + (kMaxExperts + 1) * kWideMax;
   red = red > pairs ? red : pairs;
-  s.misc_off = align_up(s.red_off + red, 128);
+  s.acc_off = align_up(s.red_off + red, 128);
+  // one float4 per (token chunk, warp half, weight row): thread (row, half) owns its entries
+  const int acc = kTileRows * (nr / 2) * 4;
+  s.misc_off = align_up(s.acc_off + acc, 128);
   s.total = align_up(s.misc_off + (int)sizeof(WMisc), 128);
   return s;
 }
@@ -700,6 +706,7 @@ template <int NR, int HD, int G>
 struct WConsumer {
   static constexpr int PBS = NR * 128, SB = slot_bytes(NR);
   static constexpr int TPT = NR / 4;  // tokens per thread in a tile's epilogue
+  float4* acc4 = nullptr;  // the GEMV accumulators [token chunk][warp half][row] (shared memory)
   static constexpr int MAXV = kMaxHidden / (kConsumerWarps * 32 * 8);  // 8-element chunks per thread
   const KParams& p;
   const WideParams& w;
@@ -722,8 +729,8 @@ struct WConsumer {
   uint32_t tmem = 0;
 
   __device__ WConsumer(const KParams& p_, const WideParams& w_, uint8_t* r, uint64_t* f, uint64_t* e, float* rd,
-                       WMisc* m_)
-      : p(p_), w(w_), ring(r), full(f), empty(e), red(rd), m(m_) {
+                       WMisc* m_, float4* a4)
+      : p(p_), w(w_), ring(r), full(f), empty(e), red(rd), m(m_), acc4(a4) {
     tid = threadIdx.x;
     warp = tid >> 5;
     lane = tid & 31;
@@ -886,7 +893,7 @@ struct WConsumer {
   // Each product is scaled by the tile's block scale and the pieces' 2^-a.
   static constexpr int LB = 2;
   __device__ __forceinline__ void epilogue(unsigned gs, int n, int sw, int kind, const WGeo& g, int t, int u_lo,
-                                          float (&acc)[TPT]) {
+                                          int) {
     const int gsl = gs % kNGW;
     const unsigned long long c0 = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
     if (!dead && !mbar_wait(&m->tfull[gsl], (gs / kNGW) & 1, p, 54)) dead = true;
@@ -902,6 +909,7 @@ struct WConsumer {
 #pragma unroll
       for (int c = 0; c < NR / 16; ++c) {
         if (8 * c + 4 * h >= ntok) break;  // (warp-uniform)
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};  // the group's sum for this chunk
 #pragma unroll 1
         for (int i0 = 0; i0 < n; i0 += LB) {
           const int nb = min(LB, n - i0);
@@ -922,12 +930,14 @@ struct WConsumer {
               for (int j = 0; j < 4; ++j) {
                 const int a = (int)(int8_t)(e4 >> (8 * j));
                 const float inv = __int_as_float((127 - a) << 23);
-                acc[4 * c + j] = fmaf(s_r * inv, fmaf(__uint_as_float(d[k][2 * j + 1]), 0.0625f, __uint_as_float(d[k][2 * j])),
-                                      acc[4 * c + j]);
+                const float v = fmaf(__uint_as_float(d[k][2 * j + 1]), 0.0625f, __uint_as_float(d[k][2 * j]));
+                a4[j] = fmaf(s_r * inv, v, a4[j]);
               }
             }
           }
         }
+        float4& dst = acc4[(c * 2 + h) * kTileRows + row];
+        dst = make_float4(dst.x + a4[0], dst.y + a4[1], dst.z + a4[2], dst.w + a4[3]);
       }
     }
     tc_fence_before();
@@ -944,7 +954,7 @@ struct WConsumer {
   // One segment's partial sums of the CTA: plain stores (read after the next grid barrier), per
   // token of the step. Routed stages: the expert slot's j-th token is tl[u][j]; the down
   // projection's partials carry that token's gate.
-  __device__ __forceinline__ void flush(int kind, const WGeo& g, int seg, int first, int U, const float (&acc)[TPT]) {
+  __device__ __forceinline__ void flush(int kind, const WGeo& g, int seg, int first, int U) {
     if (dead) return;
     const int slot = wcontrib_slot(g, blockIdx.x, first, seg, gridDim.x);
     float* dst = part_of(p, kind) + (size_t)(seg * g.S + slot) * p.MB * kTileRows;
@@ -959,7 +969,7 @@ struct WConsumer {
         const int jl = 8 * (k >> 2) + (k & 3);  // (local token 8c + 4h + j, minus 4h)
         if (jl + 4 * h < n) {
           const int t = tl[jl];
-          float v = acc[k];
+          float v = acc_get(k, h, row);
           if (kind == K_D && u < U) v *= gate_of(t, u);
           dst[(size_t)t * kTileRows + row] = v;
         }
@@ -972,8 +982,14 @@ struct WConsumer {
 #pragma unroll
     for (int k = 0; k < TPT; ++k) {
       const int jl = 8 * (k >> 2) + (k & 3);
-      if (jl < nb) base[jl * kTileRows] = acc[k];
+      if (jl < nb) base[jl * kTileRows] = acc_get(k, h, row);
     }
+  }
+
+  // accumulator k (token 8 (k / 4) + 4 h + k % 4) of the thread (row, half h)
+  __device__ __forceinline__ float acc_get(int k, int h, int row) const {
+    const float4 a = acc4[((k >> 2) * 2 + h) * kTileRows + row];
+    return (k & 3) == 0 ? a.x : (k & 3) == 1 ? a.y : (k & 3) == 2 ? a.z : a.w;
   }
 
   // shared-memory tables of the routing phases (in red): expert marks, the SwiGLU (slot, token)
@@ -1016,24 +1032,26 @@ struct WConsumer {
       __threadfence_block();
       *reinterpret_cast<volatile unsigned*>(&m->stages_begun) = nstage;
     }
-    float acc[TPT];
     int seg_cur = -1, seg_first = 0;
 #pragma unroll 1
     for (int t = t0;;) {
       const int seg = t < t1 ? t / g.kbs : -1;
       if (t == t1 || seg != seg_cur) {
         const unsigned long long cf = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
-        if (seg_cur >= 0) flush(kind, g, seg_cur, seg_first, U, acc);
+        if (seg_cur >= 0) flush(kind, g, seg_cur, seg_first, U);
         if (DEC_TRACE && kind == K_RTGU && tid == 0) tw_flush += gtimer() - cf;
         if (t == t1) break;
         seg_cur = seg;
         seg_first = t;
+        {
+          const int row = 32 * (warp & 3) + lane, h = warp >> 2;
 #pragma unroll
-        for (int j = 0; j < TPT; ++j) acc[j] = 0.f;
+          for (int c = 0; c < NR / 16; ++c) acc4[(c * 2 + h) * kTileRows + row] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
       const GroupShape gsh = group_shape<NR>(p, m, kind, g, t);
       const int n = min(gsh.gt, min(t1, (seg + 1) * g.kbs) - t);
-      epilogue(gseq++, n, gsh.w, kind, g, t, u_lo, acc);
+      epilogue(gseq++, n, gsh.w, kind, g, t, u_lo, 0);
       t += n;
     }
     // the stage's slots (freed by the MMA warp): keep the ring position in step
@@ -1878,7 +1896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     return;
   }
-  WConsumer<NR, HD, G> cons(p, w, ring, full, empty, red, m);
+  WConsumer<NR, HD, G> cons(p, w, ring, full, empty, red, m, reinterpret_cast<float4*>(smem + L.acc_off));
   cons.run();
 }
 
