@@ -48,8 +48,9 @@ WORKLOADS = {
     # batch sweep of the 8-layer stack (each sequence its own seeded 1024-token history)
     "moe8_1k_b2": ("MOE8", 1024, 256, 2),
     "moe8_1k_b4": ("MOE8", 1024, 256, 4),
+    "moe8_1k_b6": ("MOE8", 1024, 256, 6),
     "moe8_1k_b8": ("MOE8", 1024, 256, 8),
-    # batches above 8: the wide kernel (tensor-core GEMMs with the step's tokens as N)
+    # larger batches (the wide kernel, from 5 tokens: tensor-core GEMMs with the step's tokens as N)
     "moe8_1k_b16": ("MOE8", 1024, 128, 16),
     "moe8_1k_b32": ("MOE8", 1024, 128, 32),
     "moe8_1k_b64": ("MOE8", 1024, 128, 64),
@@ -376,9 +377,11 @@ def run_ours(args):
     ranks_barrier()
     torch.cuda.synchronize()
     times = []
+    launches0 = eng.info()["launches"]
     with ClockSampler(local) as clk:
         for _ in range(args.steps):
             times.append(one_step())
+    launches = eng.info()["launches"] - launches0  # the engine's own count of its kernel launches
     torch.cuda.synchronize()
     eng.sync()
     ranks_barrier()
@@ -416,8 +419,7 @@ def run_ours(args):
                     "samples": len(layer_ts),
                     "source": "first CTA's %globaltimer when each layer's input became final, median over "
                               "decode tokens of an untimed replay of the step"}
-    wide = batch >= 8  # the wide kernel (batches of 8 and more): one launch per decode step
-    launches = (n_dec if headless or wide else 1) * args.steps
+    wide = batch >= eng.info()["wide_min_batch"]  # the wide kernel: one launch per decode step
     per_launch_s = total / (args.steps * world) / n_dec
     achieved = bytes_per_step / n_dec / per_launch_s / 1e9
     nominal_hbm = 8000.0

@@ -127,10 +127,10 @@ dec_status dec_validate_cfg(const dec_model_cfg* cfg);
    failure).
    Environment, read here: DEC_TIMEOUT_MS bounds every device-side wait (default 1000);
    DEC_INFLIGHT / DEC_WIDE_INFLIGHT set how many ring slots one CTA keeps in flight (defaults 2
-   and 4; tuning only); DEC_WIDE_MIN_BATCH (2..9, default 8) is the smallest decode batch that
+   and 4; tuning only); DEC_WIDE_MIN_BATCH (2..9, default 5) is the smallest decode batch that
    runs the wide kernel (tuning and tests);
    DEC_TEST_SKIP_ARRIVAL=1 (tests of the failure path only) makes the CTA holding the first
-   q/k/v tile withhold that partial sum's arrival in layer 0 (in a step of 8 tokens or more:
+   q/k/v tile withhold that partial sum's arrival in layer 0 (in a step of 5 tokens or more:
    CTA 0 its arrival at the first grid barrier), so the waits for it run out after
    DEC_TIMEOUT_MS and the step ends with DEC_ERR_TIMEOUT instead of hanging;
    DEC_EPOCH_LIMIT lowers the number of steps after which a step first zeroes the engine's
@@ -196,7 +196,7 @@ dec_status dec_prefill_kv_noalloc(dec_engine* eng, const dec_ctx* ctx);
                                               may be NULL
    batch == 0 is a no-op. Errors: DEC_ERR_ARG, DEC_ERR_CAPACITY (a length would pass max_ctx),
    DEC_ERR_POISONED, DEC_ERR_CUDA (launch failure).
-   Batches of 8 .. 64 (engines built with max_batch >= 8) run the wide kernel: every GEMV on the
+   Batches of 5 .. 64 (engines built with max_batch >= 5) run the wide kernel: every GEMV on the
    tensor cores with all of the step's tokens as the N dimension, tokens grouped per routed expert
    (an expert's products kept for the tokens routed to it), phases separated by grid barriers
    ("vLLM's Kimi K3 Backend Hits 842 Tokens per Second", section "A narrow deployment lane":
@@ -248,7 +248,7 @@ dec_status dec_step(dec_engine* eng, const int32_t* token_ids, int32_t batch, fl
    warps stream the next step's first weights while the LM head finishes. Copies the generated
    tokens back to out_tokens (host int32 [n_steps][batch]) and synchronises. Requires vocab > 0
    and length + n_steps <= max_ctx for every slot (DEC_ERR_CAPACITY otherwise). (A generation of
-   more steps than the engine's epoch period takes one launch per period; batches of 8 and more
+   more steps than the engine's epoch period takes one launch per period; batches of 5 and more
    take one wide-kernel launch per step, the tokens still chained on the device.) */
 dec_status dec_generate(dec_engine* eng, const int32_t* first_tokens, int32_t batch,
                         int32_t n_steps, int32_t* out_tokens, void* stream);
@@ -282,6 +282,8 @@ typedef struct {
   int64_t kv_bytes;       /* KV cache bytes */
   int64_t workspace_bytes;
   int64_t launches;       /* kernel launches issued by this engine so far */
+  int32_t wide_min_batch; /* decode steps of at least this many tokens run the wide kernel
+                             (a value above max_batch: none does) */
 } dec_info;
 dec_status dec_get_info(dec_engine* eng, dec_info* out);
 

@@ -56,7 +56,7 @@ class DecStepArgs(C.Structure):
 class DecInfo(C.Structure):
     _fields_ = [("grid", C.c_int32), ("threads", C.c_int32), ("smem_bytes", C.c_int32), ("ring_slots", C.c_int32),
                 ("stages_per_layer", C.c_int32), ("weight_bytes", C.c_int64), ("kv_bytes", C.c_int64),
-                ("workspace_bytes", C.c_int64), ("launches", C.c_int64)]
+                ("workspace_bytes", C.c_int64), ("launches", C.c_int64), ("wide_min_batch", C.c_int32)]
 
 
 # name -> (restype, argtypes); the exported surface of dec.h

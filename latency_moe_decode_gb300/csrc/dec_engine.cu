@@ -1222,6 +1222,7 @@ dec_status dec_get_info(dec_engine* e, dec_info* o) {
   o->kv_bytes = e->kv_bytes;
   o->workspace_bytes = e->ws_bytes;
   o->launches = e->launches;
+  o->wide_min_batch = e->wide_min;
   return DEC_OK;
 }
 

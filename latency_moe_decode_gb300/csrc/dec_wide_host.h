@@ -17,7 +17,7 @@ int stage_slots(const KParams& p, int kind, int U, int G);
 int stage_tiles(const KParams& p, int kind, int U, int G);
 
 constexpr int kWideTopkHost = 8;  // the wide kernel's experts per token (its routing tables)
-constexpr int kWideMinBatch = 8;  // the smallest decode batch the wide kernel takes by default
+constexpr int kWideMinBatch = 5;  // the smallest decode batch the wide kernel takes by default
 
 }  // namespace wide
 }  // namespace dec

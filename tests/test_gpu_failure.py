@@ -2,7 +2,7 @@
 
 * A wait that runs out: the engine is built with DEC_TEST_SKIP_ARRIVAL=1, so the CTA holding
   the first q/k/v tile withholds that partial sum's arrival in layer 0 (a counter that nothing
-  completes; in a step of 8 tokens or more, the wide kernel, CTA 0 withholds its arrival at
+  completes; in a step of 5 tokens or more, the wide kernel, CTA 0 withholds its arrival at
   the first grid barrier), and with
   DEC_TIMEOUT_MS=20 every wait of the step is bounded by 20 ms. The step must end by itself, the
   next synchronising call must report DEC_ERR_TIMEOUT and poison the engine (later calls give

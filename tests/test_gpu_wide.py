@@ -27,7 +27,7 @@ def _ragged(batch, base=5, step=37, mod=250):
     return [base + (step * b) % mod for b in range(batch)]
 
 
-@pytest.mark.parametrize("batch", [9, 16, 24, 33, 64])
+@pytest.mark.parametrize("batch", [5, 7, 8, 9, 16, 24, 33, 64])
 def test_wide_moe_small_batch_ragged(moe_wide, batch):
     """One step of `batch` sequences with ragged lengths (1 .. 4 KV tiles, several sequences
     sharing an expert, slots beyond 8): logits, argmax, final hidden state, routing and lengths of
