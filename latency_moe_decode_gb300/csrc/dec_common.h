@@ -1,5 +1,7 @@
 // Internal layout shared by the engine's host code and its persistent kernel.
 #pragma once
+#include <cuda.h>  // CUtensorMap
+
 #include <cstdint>
 
 namespace dec {
@@ -148,6 +150,9 @@ struct KParams {
 // byte per token (the pieces encode x * 2^a). The producer copies a tile's block into the ring
 // slot beside the weight tile.
 struct WideParams {
+  // tensor maps of the K and V caches for the attention's tile loads: 3-D (head_dim, position,
+  // (layer, slot, KV head) plane), 64 x 64 boxes of bf16, 128-byte swizzle
+  CUtensorMap kmap, vmap;
   const uint8_t* pb;  // the B operand arena (pbx, pbo, pbh), for the copies' bounds checks
   unsigned long long pb_bytes;
   uint8_t* pbx;       // [kb_d][nr * 128]: the normalised input of a q/k/v, router, gate/up or LM stage

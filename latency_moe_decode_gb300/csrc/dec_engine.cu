@@ -1,6 +1,7 @@
 // Host side of the decode engine: validation, weight repacking into kernel tiles, KV cache and
 // workspace allocation, the per-step cooperative launch and status readback. Implements dec.h.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 
 #include <algorithm>
 #include <cmath>
@@ -168,6 +169,29 @@ struct dec_engine {
 };
 
 namespace {
+
+dec_status fail(dec_engine* e, dec_status s, const std::string& msg);
+
+// Tensor map of one KV cache (kc or vc: [layer][slot][KV head][position][head_dim] bf16) for the
+// wide kernel's tile loads: 3-D (head_dim, position, (layer, slot, KV head) plane), boxes of 64
+// values x 64 positions in the 128-byte swizzled layout, zeros past the cache's end.
+dec_status encode_kv_map(dec_engine* e, CUtensorMap* map, void* base, const dec_model_cfg& c) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  cudaError_t ce = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (ce != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return fail(e, DEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.max_ctx,
+                              (cuuint64_t)c.n_layers * c.max_batch * c.n_kv_heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)c.max_ctx * c.head_dim * 2};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn)(
+      map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(e, DEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return DEC_OK;
+}
 
 dec_status fail(dec_engine* e, dec_status s, const std::string& msg) {
   if (e) e->err = msg;
@@ -791,6 +815,8 @@ dec_status dec_init(const dec_model_cfg* cfg, const dec_weights* W, void* stream
     WZ(wp.attn_part, sizeof(float) * (size_t)w.MB * c.n_kv_heads * e->wnch_max * e->group * (c.head_dim + 2));
     WZ(wp.xbuf, (size_t)w.MB * c.hidden * 2);
     WZ(wp.xmid, (size_t)w.MB * c.hidden * 2);
+    if ((st = encode_kv_map(e, &wp.kmap, p.kc, c)) != DEC_OK) return bail(st);
+    if ((st = encode_kv_map(e, &wp.vmap, p.vc, c)) != DEC_OK) return bail(st);
     // partial sums: [segment][slot][MB][128] fp32 (routed stages: the largest over the expert count)
     const size_t fb = sizeof(float) * (size_t)w.MB * kTileRows;
     auto plain = [&](int kind, int n_rb) {

@@ -223,12 +223,33 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 // Generic-proxy shared-memory writes (st.shared) made visible to the tensor cores' reads.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Shared-memory matrix descriptor of a K-major operand without swizzling: 8-row x 16-byte core
-// matrices, lbo bytes between core matrices adjacent in K, sbo bytes between 8-row groups.
+// Shared-memory matrix descriptor of an operand without swizzling, made of 128-byte core
+// matrices: K-major, 8 rows (M or N) x 16 bytes of K; MN-major, 8 K indices x 16 bytes of M or N.
+// lbo: bytes between core matrices adjacent in K; sbo: between those adjacent in M or N.
 __device__ __forceinline__ uint64_t smem_desc(const void* base, uint32_t lbo, uint32_t sbo) {
   const uint32_t a = smem_u32(base);
   return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
          (1ull << 46);  // descriptor version 1 (tcgen05); base offset 0; no swizzle
+}
+
+// The same for an operand in the 128-byte swizzled layout (atoms of 8 rows x 128 bytes, 1024-byte
+// aligned, 16-byte chunks of row r stored at chunk index c ^ (r % 8)). K-major: sbo = bytes between
+// 8-row groups (lbo unused); MN-major: lbo = bytes between 64-element atoms along M or N, sbo =
+// bytes between groups of 8 K indices.
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* base, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(base, lbo, sbo) | (2ull << 61);
+}
+
+// 3-D tensor tile load (TMA) global -> this CTA's shared memory, completing on an mbarrier, with an
+// L2 eviction-priority hint. The map lives in kernel parameter space; x (the innermost
+// coordinate) times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
 }
 
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (both K-major) and an fp32 D of
@@ -246,6 +267,26 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B and an fp32 D of shape M x N; A either
+// K-major or MN-major (a_mn: the M index contiguous in memory), B K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn) {
+  return (1u << 4)                          // D format: f32
+         | (1u << 7) | (1u << 10)           // A, B format: bf16
+         | ((a_mn ? 1u : 0u) << 15)         // A major-ness (1: MN-major)
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// D[tmem] (+)= A * B^T for one K = 16 slice of bf16 operands.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

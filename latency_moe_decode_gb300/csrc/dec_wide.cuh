@@ -1,4 +1,4 @@
-// The decode step for 8 .. 64 tokens (sequences side by side): the tensor-core expert GEMMs of a
+// The decode step for 5 .. 64 tokens (sequences side by side): the tensor-core expert GEMMs of a
 // batched decode ("vLLM's Kimi K3 Backend Hits 842 Tokens per Second", section "A narrow
 // deployment lane": decode batches up to 64; section "Throughput holds across the tested range").
 //
@@ -14,7 +14,8 @@
 // write one split-K partial per output row block. A routed expert's tiles multiply only its own
 // tokens: after the routing every CTA knows each expert slot's tokens, their B rows are gathered
 // into compact blocks (the slot's j-th token in rows 2j, 2j + 1), and the MMA's N is twice the
-// slot's token count rounded up to 16.
+// slot's token count rounded up to 16. Attention runs on the tensor cores too (bf16 K q^T and
+// V^T P per 64-position KV tile, the tile loaded by tensor-map copies in the layout the MMAs read).
 //
 // Phases of a layer (barrier after each):
 //   q/k/v GEMV | attention (each unit sums its q/k/v partials, applies RoPE, appends its key and
@@ -123,6 +124,10 @@ struct WMisc {
   uint8_t wsel[kWideMax][kWideTopk];          // expert slot of each token's selections
   float wgate[kWideMax][kWideTopk];           // and their gates
   float rsum[kConsumerWarps];
+  // attention on the tensor cores: the consumers' own MMA completions, and per tile the two
+  // position warps' score maxima, the rescale factors and, per unit, the softmax state per head
+  uint64_t sbar, obar;  // S^T and O^T products done (one commit per tile each)
+  float amx[2][8], acr[8], alw[2][8], amr[8];
   alignas(16) int8_t ex[kMaxKb * kWideMax];  // exponents of the running GEMV stage's B blocks [row][token]
 };
 
@@ -173,6 +178,18 @@ __device__ __forceinline__ void wsplit(WGeo& g, const M* m, const KParams& p, in
 struct WLayout {
   int ring_off, full_off, empty_off, mempty_off, red_off, acc_off, misc_off, total;
 };
+// Attention operands staged by the consumers (att_* offsets, whole 128-byte core matrices): the
+// probabilities P as [position block][column][8 positions] (16 columns) and the group's query
+// heads as [d chunk][head row][8 values] (16 rows). K and V stay in their ring slot.
+__host__ __device__ constexpr int att_p(int) { return 0; }
+__host__ __device__ constexpr int att_q(int) { return kKvTilePos * 16 * 2; }
+__host__ __device__ constexpr int att_bytes(int hd) { return att_q(hd) + 16 * hd * 2; }
+
+// A KV tile in a ring slot: from the first 1024-byte boundary, K then V, each as head_dim / 64
+// boxes of 64 positions x 128 bytes in the 128-byte swizzled layout (box b: d = 64 b .. 64 b + 63)
+__device__ __forceinline__ uint8_t* kv_area(uint8_t* slot) {
+  return slot + ((1024u - (smem_u32(slot) & 1023u)) & 1023u);
+}
 // The GEMV accumulators live in shared memory, not registers: nr / 4 per consumer thread (up to
 // 32) did not fit beside the rest of the kernel's live state at the 168-register cap, and the
 // spills cost more than the shared-memory round trips (measured: 64 tokens 13761 vs 11452
@@ -190,8 +207,10 @@ __host__ __device__ inline WLayout wlayout(int ring, int nr, int hd, int group) 
   const int pairs = (kMaxExperts + kWideMax * 17) * 4 + (kMaxExperts + 1) * kWideMax;
   red = red > pairs ? red : pairs;
   s.acc_off = align_up(s.red_off + red, 128);
-  // one float4 per (token chunk, warp half, weight row): thread (row, half) owns its entries
-  const int acc = kTileRows * (nr / 2) * 4;
+  // one float4 per (token chunk, warp half, weight row): thread (row, half) owns its entries; the
+  // attention's staging shares the area (no GEMV runs meanwhile)
+  int acc = kTileRows * (nr / 2) * 4;
+  acc = acc > att_bytes(hd) ? acc : att_bytes(hd);
   s.misc_off = align_up(s.acc_off + acc, 128);
   s.total = align_up(s.misc_off + (int)sizeof(WMisc), 128);
   return s;
@@ -469,26 +488,28 @@ struct WProducer {
   __device__ void issue_attn(int l) {
     if (dead) return;
     const int NU = p.B * p.hkv * w.nch;
-    const unsigned row_bytes = HD * 2;
+    const int planes = p.L * p.slots * p.hkv;
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
       const WUnit a = wunit(p, w, m, u);
+      const int z = (l * p.slots + p.seq0 + a.b) * p.hkv + a.g;  // (the rows of kv_row)
       for (int t = a.tile0; t < a.tile1; ++t) {
         int slot;
         if (!claim(slot, false)) return;
         const int p0 = t * kKvTilePos;
-        const int n = min(kKvTilePos, a.T - p0);
-        uint8_t* dst = ring + (size_t)slot * SB;
-        const size_t r0 = kv_row(p, l, a.b, a.g, p0);
-        if (n < 1 || n > kKvTilePos || !within(p.kc + r0, n * row_bytes, p.kc, p.kv_bytes) ||
-            !within(p.vc + r0, n * row_bytes, p.vc, p.kv_bytes)) {
+        uint8_t* dst = kv_area(ring + (size_t)slot * SB);
+        if (a.T - p0 < 1 || a.T > p.max_ctx || z < 0 || z >= planes) {
           raise_err(p, kDevBadArg, 46);
           mbar_arrive(&full[slot]);
           advance();
           continue;
         }
-        mbar_arrive_expect_tx(&full[slot], 2u * n * row_bytes);
-        bulk_g2s_hint(dst, p.kc + r0, n * row_bytes, &full[slot], pol_near);
-        bulk_g2s_hint(dst + kKvTilePos * row_bytes, p.vc + r0, n * row_bytes, &full[slot], pol_near);
+        // whole boxes (rows past the cache's end read as zeros)
+        mbar_arrive_expect_tx(&full[slot], 2u * kKvTilePos * HD * 2);
+#pragma unroll
+        for (int hb = 0; hb < HD / 64; ++hb) {
+          tma_load_3d(dst + hb * 8192, &w.kmap, hb * 64, p0, z, &full[slot], pol_near);
+          tma_load_3d(dst + HD * kKvTilePos * 2 + hb * 8192, &w.vmap, hb * 64, p0, z, &full[slot], pol_near);
+        }
         advance();
       }
     }
@@ -725,7 +746,9 @@ struct WConsumer {
   unsigned nstage = 0;  // GEMV stages begun (thread 0)
   unsigned long long tw_prod = 0, tw_stage = 0, tw_ld = 0, tw_flush = 0;  // diagnostics (thread 0): routed gate/up
   int rtgu_seen = 0;
+  unsigned sph = 0, oph = 0;  // attention MMA completions waited for (phases of sbar, obar)
   unsigned long long tw_kv = 0, tw_attn = 0, tw_pro = 0, tw_post = 0;  // diagnostics: attention
+  unsigned long long tw_a[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // diagnostics: attention tile steps
   uint32_t tmem = 0;
 
   __device__ WConsumer(const KParams& p_, const WideParams& w_, uint8_t* r, uint64_t* f, uint64_t* e, float* rd,
@@ -1121,40 +1144,106 @@ struct WConsumer {
     cons_sync();
   }
 
-  template <int NV>
-  __device__ __forceinline__ float warp_transpose_reduce(float (&v)[NV]) {
+  // eight bf16 values (given as floats that bf16 holds exactly) as one 16-byte chunk
+  __device__ __forceinline__ static uint4 bf16x8(const float* f) {
+    uint32_t u[4];
 #pragma unroll
-    for (int off = 16, n = NV; n > 1; off >>= 1, n >>= 1) {
-      const bool upper = (lane & off) != 0;
-#pragma unroll
-      for (int i = 0; i < n / 2; ++i) {
-        float send = upper ? v[i] : v[i + n / 2];
-        float keep = upper ? v[i + n / 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-      }
+    for (int i = 0; i < 4; ++i) u[i] = (uint32_t)f2bf(f[2 * i]) | ((uint32_t)f2bf(f[2 * i + 1]) << 16);
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+
+  // Split-context GQA decode on the tensor cores: unit (token b, KV head g, chunk c) over the KV
+  // tiles of its chunk, one online softmax per unit. The producer loads each 64-position tile's K
+  // and V into a ring slot with tensor-map copies in the 128-byte swizzled layout the MMAs read;
+  // the consumers only write in the new position's key and value (and zero the value rows past
+  // the context). One thread issues S^T = K q^T (M = 128 rows: the tile's positions, then 64
+  // unused; N = 16 columns: the group's heads, then zeros; bf16 operands, fp32 in TMEM columns
+  // 0..15). The warps holding the tile's positions take each head's maximum, form p = 2^(s - m)
+  // and split it into three bf16 pieces, p = p1 + p2 + p3 within 2^-27 p (two pieces, within
+  // 2^-17 p, flipped the bf16 rounding of about one output in a thousand against fp32
+  // arithmetic); one thread issues O^T = V^T [p1 p2 p3] (M = head_dim rows, V read MN-major;
+  // TMEM columns 16..31) and each output row's thread rescales its running sum and adds the
+  // pieces' products. Software pipeline over the tiles: S^T of tile t + 1 runs during tile t's
+  // softmax, O^T of tile t during the next tile's score load (two consumer barriers per tile).
+  // One chunk: the normalised outputs go straight to the B blocks of the projection; otherwise
+  // the chunk's state is published for the merge phase.
+  static constexpr int NCH = HD / 8;           // 16-byte chunks of a K or V row
+  static constexpr int NT = kConsumerWarps * 32;
+
+  // the ring item after the current one (the current one still held)
+  __device__ const uint8_t* wait_next_item() {
+    int s = rslot + 1;
+    unsigned par = rpar;
+    if (s == p.ring) {
+      s = 0;
+      par ^= 1;
     }
-    float r = v[0];
-    constexpr int lanes_per = 32 / NV;
-#pragma unroll
-    for (int off = lanes_per / 2; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    if (!dead && !mbar_wait(&full[s], par, p, 52)) dead = true;
+    return ring + (size_t)s * SB;
+  }
+
+  __device__ __forceinline__ static float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
   }
 
-  // Split-context GQA decode: unit (token b, KV head g, chunk c) over the KV tiles of its chunk
-  // (each tile shared by the eight warps, 8 positions per warp, online softmax per warp, merged
-  // per unit). One chunk: the normalised outputs go straight to the B blocks of the projection;
-  // otherwise the chunk's state is published for the merge phase.
+  // O^T of the tile just finished (TMEM columns 16..): this output row's running sums rescaled by
+  // the tile's factors, then the three pieces' products added
+  __device__ __forceinline__ void add_o(float (&acc)[G / 2], int h0) {
+    const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16u;
+    float o[16];
+    if constexpr (3 * G > 8) {
+      tmem_ld16(ta, o);
+    } else {
+      float o8[8];
+      tmem_ld<8>(ta, o8);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = i < 8 ? o8[i] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < G / 2; ++j) {
+      const int h = h0 + j;
+      acc[j] = acc[j] * m->acr[h] + (o[h] + (o[G + h] + o[2 * G + h]));
+    }
+  }
+
   __device__ void attention(int l) {
-    constexpr int DPL = HD / 32;
-    constexpr int PPW = kKvTilePos / kConsumerWarps;
-    constexpr int NV = PPW * G;
-    static_assert(NV <= 32 && (NV & (NV - 1)) == 0, "scores per warp must be a power of two <= 32");
-    constexpr int LPV = 32 / NV;
-    static_assert(DPL == 2 || DPL == 4, "head_dim 64 or 128");
-    static_assert((G * HD) % kTileK == 0, "a KV group's heads must fill whole k blocks");
+    static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+    static_assert(G % 2 == 0 && 3 * G <= 16, "two head groups; the three p pieces within 16 columns");
+    constexpr int GH = G / 2;                     // heads per warp group
+    constexpr int HB = HD / 64;                   // 64-wide d boxes of a K or V tile
+    constexpr int VOFF = HD * kKvTilePos * 2;     // V after K in the slot's KV area
+    uint8_t* st = reinterpret_cast<uint8_t*>(acc4);
+    uint8_t* ps = st + att_p(HD);
+    uint8_t* qs = st + att_q(HD);
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-    const unsigned row_bytes = HD * 2;
     const int NU = p.B * p.hkv * w.nch;
+    const int q4 = warp & 3, h0 = (warp >> 2) * GH;  // TMEM lane quadrant; the warp's heads
+    const bool pos_warp = q4 < 2;        // TMEM lanes 0..63: the tile's positions
+    const bool out_warp = 32 * q4 < HD;  // TMEM lanes 0..HD-1: output rows d
+    const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 16, false), kIdO = idesc_bf16_f32(128, 16, true);
+    // S^T = K q^T. A = K, K-major 128-byte swizzled (8-row groups 1024 B apart; K = 16 steps of 32
+    // bytes inside a box, then the next box); B = q ([d chunk][row][8 values]: rows 8 apart 128 B,
+    // d chunks 256 B).
+    auto issue_s = [&](const uint8_t* kv) {
+      const uint64_t bd = smem_desc(qs, 256, 128);
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k)
+        mma_bf16(tmem, smem_desc_sw128(kv + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), bd + (uint64_t)(k * 32),
+                 kIdS, k > 0 ? 1u : 0u);
+    };
+    // O^T = V^T P. A = V^T, MN-major 128-byte swizzled (64-row atoms of d one box apart, groups of
+    // 8 positions 1024 B); B = P ([position block][column][8 positions]: columns 8 apart 128 B,
+    // position blocks 256 B).
+    auto issue_o = [&](const uint8_t* kv) {
+      const uint64_t bd = smem_desc(ps, 256, 128);
+#pragma unroll
+      for (int k = 0; k < kKvTilePos / 16; ++k)
+        mma_bf16(tmem + 16, smem_desc_sw128(kv + VOFF + k * 2048, 8192, 1024), bd + (uint64_t)(k * 32), kIdO,
+                 k > 0 ? 1u : 0u);
+    };
     const unsigned long long ca = DEC_TRACE ? gtimer() : 0;
 #pragma unroll 1
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
@@ -1163,177 +1252,174 @@ struct WConsumer {
       const unsigned long long cp = DEC_TRACE ? gtimer() : 0;
       if (a.tile1 > a.tile0) prologue(l, a, qkvn);  // (CTA barriers inside: no branch on `dead`)
       if (DEC_TRACE && tid == 0) tw_pro += gtimer() - cp;
-      float q[G][DPL];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) q[h][j] = qkvn[h * HD + lane * DPL + j] * qscale;
-      float kn[DPL], vn[DPL];  // (the new key and value, patched into the tile that holds them)
-      float mrun[G], lrun[G], acc[G][DPL];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        mrun[h] = -INFINITY;
-        lrun[h] = 0.f;
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) acc[h][j] = 0.f;
+      // the group's query heads in rows 0..G-1 of q's staging, zero rows after; P zeroed
+      for (int i = tid; i < NCH * 16; i += NT) {
+        const int dc = i >> 4, n = i & 15;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n < G && a.tile1 > a.tile0) v = bf16x8(qkvn + n * HD + dc * 8);
+        *reinterpret_cast<uint4*>(qs + dc * 256 + n * 16) = v;
       }
-      (void)kn;
-      (void)vn;
+      for (int i = tid; i < kKvTilePos * 2; i += NT) reinterpret_cast<uint4*>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
+      float acc[GH], mrun[GH], lw[GH];  // lw: this lane's position's share of the sums
+#pragma unroll
+      for (int j = 0; j < GH; ++j) {
+        acc[j] = 0.f;
+        mrun[j] = -INFINITY;
+        lw[j] = 0.f;
+      }
       const int newpos = a.T - 1;
-      const int vidx = lane / LPV;
-      const int my_i = vidx / G, my_h = vidx % G;
+      // The tile that holds the new position: its key and value rows written in (the cache copy
+      // may predate the prologue's append), value rows after it zeroed (the cache there may hold
+      // anything; P is 0 there, but 0 x NaN would not be). After the tile has landed.
+      auto patch = [&](uint8_t* kv, int jn) {
+        const int nk = HB * 8, nv = (kKvTilePos - jn) * HB * 8;
+        for (int i = tid; i < nk + nv; i += NT) {
+          const bool isk = i < nk;
+          const int ii = isk ? i : i - nk;
+          const int c = ii & 7, hb = (ii >> 3) % HB, r = isk ? jn : jn + (ii >> 3) / HB;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (isk) v = bf16x8(qkvn + G * HD + hb * 64 + c * 8);
+          else if (r == jn) v = bf16x8(qkvn + (G + 1) * HD + hb * 64 + c * 8);
+          *reinterpret_cast<uint4*>(kv + (isk ? 0 : VOFF) + hb * 8192 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        }
+      };
+      uint8_t* kvc = nullptr;
+      if (a.tile1 > a.tile0) {  // first tile: patched if needed, S^T issued
+        kvc = kv_area(const_cast<uint8_t*>(wait_item()));
+        const int jn = newpos - a.tile0 * kKvTilePos;
+        if (jn < kKvTilePos && !dead) patch(kvc, jn);
+        fence_proxy_async_smem();  // (also the q and P staging above)
+        cons_sync();
+        if (tid == 0) {
+          tc_fence_after();
+          if (!dead) issue_s(kvc);
+          mma_commit(&m->sbar);
+        }
+      }
 #pragma unroll 1
       for (int t = a.tile0; t < a.tile1; ++t) {
-        const uint8_t* slot = wait_item();
-        const int jn = newpos - t * kKvTilePos;
-        if (jn >= 0 && jn < kKvTilePos) {  // (the same for all warps)
-          uint16_t* kr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + jn * row_bytes);
-          uint16_t* vr = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(slot) + (kKvTilePos + jn) * row_bytes);
-          if (!dead)
-            for (int d = tid; d < HD; d += kConsumerWarps * 32) {
-              kr[d] = f2bf(qkvn[G * HD + d]);
-              vr[d] = f2bf(qkvn[(G + 1) * HD + d]);
-            }
-          cons_sync();
-        }
-        if (!dead) {
-          const int p0 = t * kKvTilePos;
-          const int npos = min(kKvTilePos, a.T - p0);
-          float s[NV];
+        const int p0 = t * kKvTilePos;
+        const int npos = min(kKvTilePos, a.T - p0);
+        const bool more = t + 1 < a.tile1;
+        // scores of tile t, each head's tile maximum
+        unsigned long long c0 = DEC_TRACE ? gtimer() : 0, c1 = 0;
+#define ATT_T(i) if (DEC_TRACE && tid == 0) { c1 = gtimer(); tw_a[i] += c1 - c0; c0 = c1; }
+        if (!dead && !mbar_wait(&m->sbar, sph & 1u, p, 57)) dead = true;
+        ATT_T(0)
+        ++sph;
+        tc_fence_after();
+        float sv[GH];
+        if (pos_warp) {
+          float s8[8];
+          tmem_ld<G>(tl, s8);
+          const int pos = 32 * q4 + lane;
 #pragma unroll
-          for (int i = 0; i < PPW; ++i) {
-            const int j = warp * PPW + i;
-            float kf[DPL];
-            if (j < npos) {
-              const uint16_t* src = reinterpret_cast<const uint16_t*>(slot + j * row_bytes) + lane * DPL;
-              if (DPL == 4) {
-                const uint2 v = *reinterpret_cast<const uint2*>(src);
-                kf[0] = bf16lo(v.x);
-                kf[1] = bf16hi(v.x);
-                kf[2 % DPL] = bf16lo(v.y);
-                kf[3 % DPL] = bf16hi(v.y);
-              } else {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-                kf[0] = bf16lo(v);
-                kf[1 % DPL] = bf16hi(v);
-              }
-            } else {
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) kf[d] = 0.f;
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float acc_s = 0.f;
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) acc_s = fmaf(q[h][d], kf[d], acc_s);
-              s[i * G + h] = acc_s;
-            }
-          }
-          float sc_own = warp_transpose_reduce<NV>(s);
-          if (warp * PPW + my_i >= npos) sc_own = -INFINITY;
-          float bm = sc_own;
-#pragma unroll
-          for (int off = LPV * G; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-          float mnew[G], corr[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float bmh = __shfl_sync(0xffffffffu, bm, h * LPV);
-            mnew[h] = fmaxf(mrun[h], bmh);
-            corr[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(mrun[h] - mnew[h]);
-          }
-          float mn_own = mnew[0];
-#pragma unroll
-          for (int h = 1; h < G; ++h)
-            if (my_h == h) mn_own = mnew[h];
-          const float pown = (sc_own == -INFINITY) ? 0.f : exp2f(sc_own - mn_own);
-          float pv[NV];
-#pragma unroll
-          for (int v = 0; v < NV; ++v) pv[v] = __shfl_sync(0xffffffffu, pown, v * LPV);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float ls = 0.f;
-#pragma unroll
-            for (int i = 0; i < PPW; ++i) ls += pv[i * G + h];
-            lrun[h] = lrun[h] * corr[h] + ls;
-            mrun[h] = mnew[h];
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) acc[h][d] *= corr[h];
-          }
-#pragma unroll
-          for (int i = 0; i < PPW; ++i) {
-            const int j = warp * PPW + i;
-            if (j < npos) {
-              const uint16_t* src = reinterpret_cast<const uint16_t*>(slot + (kKvTilePos + j) * row_bytes) + lane * DPL;
-              float vf[DPL];
-              if (DPL == 4) {
-                const uint2 v = *reinterpret_cast<const uint2*>(src);
-                vf[0] = bf16lo(v.x);
-                vf[1] = bf16hi(v.x);
-                vf[2 % DPL] = bf16lo(v.y);
-                vf[3 % DPL] = bf16hi(v.y);
-              } else {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-                vf[0] = bf16lo(v);
-                vf[1 % DPL] = bf16hi(v);
-              }
-#pragma unroll
-              for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(pv[i * G + h], vf[d], acc[h][d]);
-            }
+          for (int j = 0; j < GH; ++j) {
+            sv[j] = pos < npos ? s8[h0 + j] * qscale : -INFINITY;
+            const float mx = warp_max(sv[j]);
+            if (lane == 0) m->amx[q4][h0 + j] = mx;
           }
         }
+        ATT_T(1)
+        // O^T of tile t - 1 into the running sums; its slot released
+        if (t > a.tile0) {
+          if (!dead && !mbar_wait(&m->obar, oph & 1u, p, 58)) dead = true;
+          ATT_T(2)
+          ++oph;
+          tc_fence_after();
+          if (out_warp) add_o(acc, h0);
+          release_item();
+          ATT_T(3)
+        }
+        // tile t + 1 landed (and patched)
+        uint8_t* kvn = nullptr;
+        bool patched = false;
+        if (more) {
+          kvn = kv_area(const_cast<uint8_t*>(wait_next_item()));
+          const int jn = newpos - p0 - kKvTilePos;
+          if (jn < kKvTilePos) {
+            patched = true;
+            if (!dead) patch(kvn, jn);
+          }
+        }
+        if (patched) fence_proxy_async_smem();
+        ATT_T(4)
+        tc_fence_before();
+        cons_sync();
+        if (tid == 0 && more) {
+          tc_fence_after();
+          if (!dead) issue_s(kvn);
+          mma_commit(&m->sbar);
+        }
+        ATT_T(5)
+        // softmax of tile t: P's three pieces, the rescale factors
+        if (pos_warp) {
+          const int pos = 32 * q4 + lane;
+          uint8_t* pr = ps + (pos >> 3) * 256 + (pos & 7) * 2;  // [position block][column][8 positions]
+#pragma unroll
+          for (int j = 0; j < GH; ++j) {
+            const int h = h0 + j;
+            const float mnew = fmaxf(mrun[j], fmaxf(m->amx[0][h], m->amx[1][h]));
+            const float corr = mrun[j] == -INFINITY ? 0.f : exp2f(mrun[j] - mnew);
+            const float pe = sv[j] == -INFINITY ? 0.f : exp2f(sv[j] - mnew);
+            const uint16_t p1 = f2bf(pe);
+            const float r1 = pe - bf16f(p1);  // (exact, and r1 - bf16(r1) too)
+            const uint16_t p2 = f2bf(r1);
+            *reinterpret_cast<uint16_t*>(pr + h * 16) = p1;
+            *reinterpret_cast<uint16_t*>(pr + (G + h) * 16) = p2;
+            *reinterpret_cast<uint16_t*>(pr + (2 * G + h) * 16) = f2bf(r1 - bf16f(p2));
+            lw[j] = lw[j] * corr + pe;
+            mrun[j] = mnew;
+            if (q4 == 0 && lane == 0) m->acr[h] = corr;
+          }
+          fence_proxy_async_smem();
+        }
+        ATT_T(6)
+        cons_sync();
+        if (tid == 0) {
+          tc_fence_after();
+          if (!dead) issue_o(kvc);
+          mma_commit(&m->obar);
+        }
+        ATT_T(7)
+#undef ATT_T
+        kvc = kvn;
+      }
+      if (a.tile1 > a.tile0) {  // the last tile's O^T
+        if (!dead && !mbar_wait(&m->obar, oph & 1u, p, 58)) dead = true;
+        ++oph;
+        tc_fence_after();
+        if (out_warp) add_o(acc, h0);
+        tc_fence_before();
         release_item();
+      }
+      // the unit's state per head: m (the same in both position warps), l = the sum over lanes
+      // and position warps
+      if (pos_warp) {
+#pragma unroll
+        for (int j = 0; j < GH; ++j) {
+          float s = lw[j];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+          if (lane == 0) {
+            m->alw[q4][h0 + j] = s;
+            if (q4 == 0) m->amr[h0 + j] = mrun[j];
+          }
+        }
       }
       dead = cons_any(dead);  // (one verdict: the packing below is warp-collective)
       const unsigned long long cq = DEC_TRACE ? gtimer() : 0;
-      // the warps' states -> the unit's (max, sum, unnormalised output) per head
-      float* wst = red;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float* r = wst + ((size_t)warp * G + h) * (HD + 2);
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) r[lane * DPL + d] = acc[h][d];
-        if (lane == 0) {
-          r[HD] = mrun[h];
-          r[HD + 1] = lrun[h];
-        }
-      }
-      cons_sync();
-      constexpr int NPT = (G * HD + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
-      float ov[NPT], mv[NPT], lv[NPT];
-#pragma unroll
-      for (int i = 0; i < NPT; ++i) {
-        const int idx = tid + i * kConsumerWarps * 32;
-        ov[i] = mv[i] = lv[i] = 0.f;
-        if (idx < G * HD) {
-          const int h = idx / HD, d = idx % HD;
-          float M = -INFINITY;
-          for (int wi = 0; wi < kConsumerWarps; ++wi) M = fmaxf(M, wst[((size_t)wi * G + h) * (HD + 2) + HD]);
-          float A = 0.f, Lsum = 0.f;
-          if (M != -INFINITY) {
-            for (int wi = 0; wi < kConsumerWarps; ++wi) {
-              const float* r = wst + ((size_t)wi * G + h) * (HD + 2);
-              const float e = exp2f(r[HD] - M);
-              A = fmaf(e, r[d], A);
-              Lsum = fmaf(e, r[HD + 1], Lsum);
-            }
-          }
-          ov[i] = A;
-          mv[i] = M;
-          lv[i] = Lsum;
-        }
-      }
-      cons_sync();  // (wst is overwritten below)
       if (w.nch == 1) {
         // the normalised output (bf16) of the group's heads, then their B blocks
         float* ob = red;
+        if (out_warp) {
+          const int d = 32 * q4 + lane;
 #pragma unroll
-        for (int i = 0; i < NPT; ++i) {
-          const int idx = tid + i * kConsumerWarps * 32;
-          if (idx < G * HD) {
-            const float wgt = (mv[i] == -INFINITY || !(lv[i] > 0.f)) ? 0.f : 1.f / lv[i];
-            ob[idx] = bf16f(f2bf(wgt * ov[i]));
+          for (int j = 0; j < GH; ++j) {
+            const int h = h0 + j;
+            const float L = m->alw[0][h] + m->alw[1][h];
+            const float wgt = (m->amr[h] == -INFINITY || !(L > 0.f)) ? 0.f : 1.f / L;
+            ob[h * HD + d] = bf16f(f2bf(wgt * acc[j]));
           }
         }
         cons_sync();
@@ -1344,18 +1430,16 @@ struct WConsumer {
           for (int i = 0; i < 4; ++i) f[i] = ob[warp * kTileK + lane * 4 + i];
           pack4(w.pbo + (size_t)kb * PBS, w.exo + (size_t)kb * kWideMax + a.b, a.b, lane * 4, f);
         }
-      } else if (!dead) {
+      } else if (!dead && out_warp) {
         float* dst = w.attn_part + ((((size_t)a.b * p.hkv + a.g) * w.nch + a.c) * G) * (HD + 2);
+        const int d = 32 * q4 + lane;
 #pragma unroll
-        for (int i = 0; i < NPT; ++i) {
-          const int idx = tid + i * kConsumerWarps * 32;
-          if (idx < G * HD) {
-            const int h = idx / HD, d = idx % HD;
-            dst[(size_t)h * (HD + 2) + d] = ov[i];
-            if (d == 0) {
-              dst[(size_t)h * (HD + 2) + HD] = mv[i];
-              dst[(size_t)h * (HD + 2) + HD + 1] = lv[i];
-            }
+        for (int j = 0; j < GH; ++j) {
+          const int h = h0 + j;
+          dst[(size_t)h * (HD + 2) + d] = acc[j];
+          if (d == 0) {
+            dst[(size_t)h * (HD + 2) + HD] = m->amr[h];
+            dst[(size_t)h * (HD + 2) + HD + 1] = m->alw[0][h] + m->alw[1][h];
           }
         }
       }
@@ -1821,6 +1905,7 @@ struct WConsumer {
       p.trace[kWaitTrace + 9] = tw_attn;
       p.trace[kWaitTrace + 10] = tw_pro;
       p.trace[kWaitTrace + 11] = tw_post;
+      for (int i = 0; i < 8; ++i) p.trace[kWaitTrace + 12 + i] = tw_a[i];
     }
     // TMEM is freed once the MMA warp has finished (bounded wait)
     if (warp == 0) {
@@ -1859,6 +1944,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&m->rt_bar, 1);
     mbar_init(&m->mma_done, 1);
     mbar_init(&m->tm_ready, 1);
+    mbar_init(&m->sbar, 1);
+    mbar_init(&m->obar, 1);
     m->stages_begun = 0;
     for (int i = 0; i < kNGW; ++i) {
       mbar_init(&m->tfull[i], 2);  // MMA commit + the MMA thread's release of the block scales
