@@ -126,8 +126,8 @@ struct WMisc {
   float rsum[kConsumerWarps];
   // attention on the tensor cores: the consumers' own MMA completions, and per tile the two
   // position warps' score maxima, the rescale factors and, per unit, the softmax state per head
-  uint64_t sbar, obar;  // S^T and O^T products done (one commit per tile each)
-  float amx[2][8], acr[8], alw[2][8], amr[8];
+  uint64_t sbar, obar;  // a round's S^T and O^T products done
+  float amx[4][8], acr[8], alw[4][8], amr[8];
   alignas(16) int8_t ex[kMaxKb * kWideMax];  // exponents of the running GEMV stage's B blocks [row][token]
 };
 
@@ -182,11 +182,12 @@ struct WLayout {
 // probabilities P as [position block][column][8 positions] (16 columns) and the group's query
 // heads as [d chunk][head row][8 values] (16 rows). K and V stay in their ring slot.
 __host__ __device__ constexpr int att_p(int) { return 0; }
-__host__ __device__ constexpr int att_q(int) { return kKvTilePos * 16 * 2; }
+__host__ __device__ constexpr int att_q(int) { return 2 * kKvTilePos * 16 * 2; }  // (P: two tiles)
 __host__ __device__ constexpr int att_bytes(int hd) { return att_q(hd) + 16 * hd * 2; }
 
-// A KV tile in a ring slot: from the first 1024-byte boundary, K then V, each as head_dim / 64
-// boxes of 64 positions x 128 bytes in the 128-byte swizzled layout (box b: d = 64 b .. 64 b + 63)
+// The K (or V) of a round of two KV tiles in a ring slot: from the first 1024-byte boundary,
+// head_dim / 64 parts of 128 positions x 128 bytes in the 128-byte swizzled layout (part b: d =
+// 64 b .. 64 b + 63), each filled by two 64 x 64 boxes
 __device__ __forceinline__ uint8_t* kv_area(uint8_t* slot) {
   return slot + ((1024u - (smem_u32(slot) & 1023u)) & 1023u);
 }
@@ -492,25 +493,29 @@ struct WProducer {
     for (int u = blockIdx.x; u < NU; u += gridDim.x) {
       const WUnit a = wunit(p, w, m, u);
       const int z = (l * p.slots + p.seq0 + a.b) * p.hkv + a.g;  // (the rows of kv_row)
-      for (int t = a.tile0; t < a.tile1; ++t) {
-        int slot;
-        if (!claim(slot, false)) return;
+      for (int t = a.tile0; t < a.tile1; t += 2) {  // a round: its K, then its V
         const int p0 = t * kKvTilePos;
-        uint8_t* dst = kv_area(ring + (size_t)slot * SB);
-        if (a.T - p0 < 1 || a.T > p.max_ctx || z < 0 || z >= planes) {
-          raise_err(p, kDevBadArg, 46);
-          mbar_arrive(&full[slot]);
-          advance();
-          continue;
-        }
-        // whole boxes (rows past the cache's end read as zeros)
-        mbar_arrive_expect_tx(&full[slot], 2u * kKvTilePos * HD * 2);
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv) {
+          int slot;
+          if (!claim(slot, false)) return;
+          uint8_t* dst = kv_area(ring + (size_t)slot * SB);
+          if (a.T - p0 < 1 || a.T > p.max_ctx || z < 0 || z >= planes) {
+            raise_err(p, kDevBadArg, 46);
+            mbar_arrive(&full[slot]);
+            advance();
+            continue;
+          }
+          // whole boxes of both tiles (rows past the cache's end read as zeros)
+          mbar_arrive_expect_tx(&full[slot], 2u * kKvTilePos * HD * 2);
 #pragma unroll
-        for (int hb = 0; hb < HD / 64; ++hb) {
-          tma_load_3d(dst + hb * 8192, &w.kmap, hb * 64, p0, z, &full[slot], pol_near);
-          tma_load_3d(dst + HD * kKvTilePos * 2 + hb * 8192, &w.vmap, hb * 64, p0, z, &full[slot], pol_near);
+          for (int hb = 0; hb < HD / 64; ++hb)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              tma_load_3d(dst + hb * 16384 + i * 8192, kv ? &w.vmap : &w.kmap, hb * 64, p0 + i * kKvTilePos, z,
+                          &full[slot], pol_near);
+          advance();
         }
-        advance();
       }
     }
   }
@@ -690,7 +695,7 @@ struct WMma {
       int items = 0;
       for (int u = blockIdx.x; u < p.B * p.hkv * w.nch; u += gridDim.x) {
         const WUnit a = wunit(p, w, m, u);
-        items += a.tile1 - a.tile0;
+        items += 2 * ((a.tile1 - a.tile0 + 1) / 2);  // (a K and a V item per round of two tiles)
       }
       skip(items);
       gemv(K_O, 0);
@@ -748,7 +753,7 @@ struct WConsumer {
   int rtgu_seen = 0;
   unsigned sph = 0, oph = 0;  // attention MMA completions waited for (phases of sbar, obar)
   unsigned long long tw_kv = 0, tw_attn = 0, tw_pro = 0, tw_post = 0;  // diagnostics: attention
-  unsigned long long tw_a[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // diagnostics: attention tile steps
+  unsigned long long tw_a[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // diagnostics: attention round steps
   uint32_t tmem = 0;
 
   __device__ WConsumer(const KParams& p_, const WideParams& w_, uint8_t* r, uint64_t* f, uint64_t* e, float* rd,
@@ -1153,20 +1158,20 @@ struct WConsumer {
   }
 
   // Split-context GQA decode on the tensor cores: unit (token b, KV head g, chunk c) over the KV
-  // tiles of its chunk, one online softmax per unit. The producer loads each 64-position tile's K
-  // and V into a ring slot with tensor-map copies in the 128-byte swizzled layout the MMAs read;
-  // the consumers only write in the new position's key and value (and zero the value rows past
-  // the context). One thread issues S^T = K q^T (M = 128 rows: the tile's positions, then 64
-  // unused; N = 16 columns: the group's heads, then zeros; bf16 operands, fp32 in TMEM columns
-  // 0..15). The warps holding the tile's positions take each head's maximum, form p = 2^(s - m)
-  // and split it into three bf16 pieces, p = p1 + p2 + p3 within 2^-27 p (two pieces, within
-  // 2^-17 p, flipped the bf16 rounding of about one output in a thousand against fp32
-  // arithmetic); one thread issues O^T = V^T [p1 p2 p3] (M = head_dim rows, V read MN-major;
-  // TMEM columns 16..31) and each output row's thread rescales its running sum and adds the
-  // pieces' products. Software pipeline over the tiles: S^T of tile t + 1 runs during tile t's
-  // softmax, O^T of tile t during the next tile's score load (two consumer barriers per tile).
-  // One chunk: the normalised outputs go straight to the B blocks of the projection; otherwise
-  // the chunk's state is published for the merge phase.
+  // tiles of its chunk in rounds of two 64-position tiles, one online softmax per unit. For a
+  // round the producer loads K into one ring slot and V into the next with tensor-map copies, in
+  // the 128-byte swizzled layout the MMAs read (128 positions of both tiles in a row); the
+  // consumers only write in the new position's key and value (and zero the value rows past it).
+  // One thread issues S^T = K q^T (M = the round's 128 positions, N = 16 columns: the group's
+  // heads, then zeros; bf16 operands, fp32 in TMEM columns 0..15). Each thread takes its
+  // position's scores, each head's maximum over the round, forms p = 2^(s - m) and splits it into
+  // three bf16 pieces, p = p1 + p2 + p3 within 2^-27 p (two pieces, within 2^-17 p, flipped the
+  // bf16 rounding of about one output in a thousand against fp32 arithmetic); one thread issues
+  // O^T = V^T [p1 p2 p3] (M = head_dim rows, V read MN-major; TMEM columns 16..31) and each
+  // output row's thread rescales its running sum and adds the pieces' products. An MMA of these
+  // shapes costs tens of nanoseconds whatever its N, so a round takes 2 x head_dim / 16 of them
+  // for 128 positions. One chunk: the normalised outputs go straight to the B blocks of the
+  // projection; otherwise the chunk's state is published for the merge phase.
   static constexpr int NCH = HD / 8;           // 16-byte chunks of a K or V row
   static constexpr int NT = kConsumerWarps * 32;
 
@@ -1188,8 +1193,8 @@ struct WConsumer {
     return r;
   }
 
-  // O^T of the tile just finished (TMEM columns 16..): this output row's running sums rescaled by
-  // the tile's factors, then the three pieces' products added
+  // O^T of the round just finished (TMEM columns 16..): this output row's running sums rescaled
+  // by the round's factors, then the three pieces' products added
   __device__ __forceinline__ void add_o(float (&acc)[G / 2], int h0) {
     const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16u;
     float o[16];
@@ -1212,36 +1217,34 @@ struct WConsumer {
     static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
     static_assert(G % 2 == 0 && 3 * G <= 16, "two head groups; the three p pieces within 16 columns");
     constexpr int GH = G / 2;                     // heads per warp group
-    constexpr int HB = HD / 64;                   // 64-wide d boxes of a K or V tile
-    constexpr int VOFF = HD * kKvTilePos * 2;     // V after K in the slot's KV area
+    constexpr int HB = HD / 64;                   // 64-wide d parts of a round's K or V
     uint8_t* st = reinterpret_cast<uint8_t*>(acc4);
     uint8_t* ps = st + att_p(HD);
     uint8_t* qs = st + att_q(HD);
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);
     const int NU = p.B * p.hkv * w.nch;
     const int q4 = warp & 3, h0 = (warp >> 2) * GH;  // TMEM lane quadrant; the warp's heads
-    const bool pos_warp = q4 < 2;        // TMEM lanes 0..63: the tile's positions
     const bool out_warp = 32 * q4 < HD;  // TMEM lanes 0..HD-1: output rows d
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 16, false), kIdO = idesc_bf16_f32(128, 16, true);
     // S^T = K q^T. A = K, K-major 128-byte swizzled (8-row groups 1024 B apart; K = 16 steps of 32
-    // bytes inside a box, then the next box); B = q ([d chunk][row][8 values]: rows 8 apart 128 B,
+    // bytes inside a 64-wide d part, then the next part); B = q ([d chunk][row][8 values]: rows 8 apart 128 B,
     // d chunks 256 B).
-    auto issue_s = [&](const uint8_t* kv) {
+    auto issue_s = [&](const uint8_t* kk) {
       const uint64_t bd = smem_desc(qs, 256, 128);
 #pragma unroll
       for (int k = 0; k < HD / 16; ++k)
-        mma_bf16(tmem, smem_desc_sw128(kv + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), bd + (uint64_t)(k * 32),
-                 kIdS, k > 0 ? 1u : 0u);
+        mma_bf16(tmem, smem_desc_sw128(kk + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024), bd + (uint64_t)(k * 32), kIdS,
+                 k > 0 ? 1u : 0u);
     };
-    // O^T = V^T P. A = V^T, MN-major 128-byte swizzled (64-row atoms of d one box apart, groups of
-    // 8 positions 1024 B); B = P ([position block][column][8 positions]: columns 8 apart 128 B,
+    // O^T = V^T P. A = V^T, MN-major 128-byte swizzled (64-row atoms of d one part apart, groups
+    // of 8 positions 1024 B); B = P ([position block][column][8 positions]: columns 8 apart 128 B,
     // position blocks 256 B).
-    auto issue_o = [&](const uint8_t* kv) {
+    auto issue_o = [&](const uint8_t* vv) {
       const uint64_t bd = smem_desc(ps, 256, 128);
 #pragma unroll
-      for (int k = 0; k < kKvTilePos / 16; ++k)
-        mma_bf16(tmem + 16, smem_desc_sw128(kv + VOFF + k * 2048, 8192, 1024), bd + (uint64_t)(k * 32), kIdO,
+      for (int k = 0; k < 2 * kKvTilePos / 16; ++k)
+        mma_bf16(tmem + 16, smem_desc_sw128(vv + k * 2048, 16384, 1024), bd + (uint64_t)(k * 32), kIdO,
                  k > 0 ? 1u : 0u);
     };
     const unsigned long long ca = DEC_TRACE ? gtimer() : 0;
@@ -1259,7 +1262,7 @@ struct WConsumer {
         if (n < G && a.tile1 > a.tile0) v = bf16x8(qkvn + n * HD + dc * 8);
         *reinterpret_cast<uint4*>(qs + dc * 256 + n * 16) = v;
       }
-      for (int i = tid; i < kKvTilePos * 2; i += NT) reinterpret_cast<uint4*>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = tid; i < kKvTilePos * 4; i += NT) reinterpret_cast<uint4*>(ps)[i] = make_uint4(0u, 0u, 0u, 0u);
       float acc[GH], mrun[GH], lw[GH];  // lw: this lane's position's share of the sums
 #pragma unroll
       for (int j = 0; j < GH; ++j) {
@@ -1271,8 +1274,8 @@ struct WConsumer {
       // The tile that holds the new position: its key and value rows written in (the cache copy
       // may predate the prologue's append), value rows after it zeroed (the cache there may hold
       // anything; P is 0 there, but 0 x NaN would not be). After the tile has landed.
-      auto patch = [&](uint8_t* kv, int jn) {
-        const int nk = HB * 8, nv = (kKvTilePos - jn) * HB * 8;
+      auto patch = [&](uint8_t* kk, uint8_t* vv, int jn) {  // (jn: the row in the round, < 128)
+        const int nk = HB * 8, nv = (2 * kKvTilePos - jn) * HB * 8;
         for (int i = tid; i < nk + nv; i += NT) {
           const bool isk = i < nk;
           const int ii = isk ? i : i - nk;
@@ -1280,86 +1283,61 @@ struct WConsumer {
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (isk) v = bf16x8(qkvn + G * HD + hb * 64 + c * 8);
           else if (r == jn) v = bf16x8(qkvn + (G + 1) * HD + hb * 64 + c * 8);
-          *reinterpret_cast<uint4*>(kv + (isk ? 0 : VOFF) + hb * 8192 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>((isk ? kk : vv) + hb * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = v;
         }
       };
-      uint8_t* kvc = nullptr;
-      if (a.tile1 > a.tile0) {  // first tile: patched if needed, S^T issued
-        kvc = kv_area(const_cast<uint8_t*>(wait_item()));
-        const int jn = newpos - a.tile0 * kKvTilePos;
-        if (jn < kKvTilePos && !dead) patch(kvc, jn);
-        fence_proxy_async_smem();  // (also the q and P staging above)
+      // rounds of two tiles (the second may lie past the chunk or the context: masked): S^T of
+      // both in one M = 128 product, one softmax over their 128 positions, O^T over both
+      const int pend = min(a.T, a.tile1 * kKvTilePos);  // this unit's positions end here
+#pragma unroll 1
+      for (int t = a.tile0; t < a.tile1; t += 2) {
+        unsigned long long c0 = DEC_TRACE ? gtimer() : 0, c1 = 0;
+#define ATT_T(i) if (DEC_TRACE && tid == 0) { c1 = gtimer(); tw_a[i] += c1 - c0; c0 = c1; }
+        uint8_t* kk = kv_area(const_cast<uint8_t*>(wait_item()));
+        uint8_t* vv = kv_area(const_cast<uint8_t*>(wait_next_item()));
+        const int p0 = t * kKvTilePos;
+        const int jn = newpos - p0;  // (the new position is in this round if jn < 128)
+        const bool patched = jn < 2 * kKvTilePos;
+        if (patched && !dead) patch(kk, vv, jn);
+        if (patched || t == a.tile0) fence_proxy_async_smem();  // (the first round: q and P staging too)
+        ATT_T(0)
+        tc_fence_before();
         cons_sync();
         if (tid == 0) {
           tc_fence_after();
-          if (!dead) issue_s(kvc);
+          if (!dead) issue_s(kk);
           mma_commit(&m->sbar);
         }
-      }
-#pragma unroll 1
-      for (int t = a.tile0; t < a.tile1; ++t) {
-        const int p0 = t * kKvTilePos;
-        const int npos = min(kKvTilePos, a.T - p0);
-        const bool more = t + 1 < a.tile1;
-        // scores of tile t, each head's tile maximum
-        unsigned long long c0 = DEC_TRACE ? gtimer() : 0, c1 = 0;
-#define ATT_T(i) if (DEC_TRACE && tid == 0) { c1 = gtimer(); tw_a[i] += c1 - c0; c0 = c1; }
+        ATT_T(1)
         if (!dead && !mbar_wait(&m->sbar, sph & 1u, p, 57)) dead = true;
-        ATT_T(0)
+        ATT_T(2)
         ++sph;
         tc_fence_after();
+        release_item();  // (the K slot: its product is done; the producer may refill it now)
+        // scores: this lane's position (TMEM lane) of the round; each head's maximum
+        const int pos = 32 * q4 + lane;
         float sv[GH];
-        if (pos_warp) {
+        {
           float s8[8];
           tmem_ld<G>(tl, s8);
-          const int pos = 32 * q4 + lane;
 #pragma unroll
           for (int j = 0; j < GH; ++j) {
-            sv[j] = pos < npos ? s8[h0 + j] * qscale : -INFINITY;
+            sv[j] = p0 + pos < pend ? s8[h0 + j] * qscale : -INFINITY;
             const float mx = warp_max(sv[j]);
             if (lane == 0) m->amx[q4][h0 + j] = mx;
           }
         }
-        ATT_T(1)
-        // O^T of tile t - 1 into the running sums; its slot released
-        if (t > a.tile0) {
-          if (!dead && !mbar_wait(&m->obar, oph & 1u, p, 58)) dead = true;
-          ATT_T(2)
-          ++oph;
-          tc_fence_after();
-          if (out_warp) add_o(acc, h0);
-          release_item();
-          ATT_T(3)
-        }
-        // tile t + 1 landed (and patched)
-        uint8_t* kvn = nullptr;
-        bool patched = false;
-        if (more) {
-          kvn = kv_area(const_cast<uint8_t*>(wait_next_item()));
-          const int jn = newpos - p0 - kKvTilePos;
-          if (jn < kKvTilePos) {
-            patched = true;
-            if (!dead) patch(kvn, jn);
-          }
-        }
-        if (patched) fence_proxy_async_smem();
-        ATT_T(4)
         tc_fence_before();
         cons_sync();
-        if (tid == 0 && more) {
-          tc_fence_after();
-          if (!dead) issue_s(kvn);
-          mma_commit(&m->sbar);
-        }
-        ATT_T(5)
-        // softmax of tile t: P's three pieces, the rescale factors
-        if (pos_warp) {
-          const int pos = 32 * q4 + lane;
+        ATT_T(3)
+        // softmax of the round: P's three pieces, the rescale factors
+        {
           uint8_t* pr = ps + (pos >> 3) * 256 + (pos & 7) * 2;  // [position block][column][8 positions]
 #pragma unroll
           for (int j = 0; j < GH; ++j) {
             const int h = h0 + j;
-            const float mnew = fmaxf(mrun[j], fmaxf(m->amx[0][h], m->amx[1][h]));
+            const float mr = fmaxf(fmaxf(m->amx[0][h], m->amx[1][h]), fmaxf(m->amx[2][h], m->amx[3][h]));
+            const float mnew = fmaxf(mrun[j], mr);
             const float corr = mrun[j] == -INFINITY ? 0.f : exp2f(mrun[j] - mnew);
             const float pe = sv[j] == -INFINITY ? 0.f : exp2f(sv[j] - mnew);
             const uint16_t p1 = f2bf(pe);
@@ -1374,37 +1352,34 @@ struct WConsumer {
           }
           fence_proxy_async_smem();
         }
-        ATT_T(6)
         cons_sync();
+        ATT_T(4)
         if (tid == 0) {
           tc_fence_after();
-          if (!dead) issue_o(kvc);
+          if (!dead) issue_o(vv);
           mma_commit(&m->obar);
         }
-        ATT_T(7)
-#undef ATT_T
-        kvc = kvn;
-      }
-      if (a.tile1 > a.tile0) {  // the last tile's O^T
+        ATT_T(5)
         if (!dead && !mbar_wait(&m->obar, oph & 1u, p, 58)) dead = true;
+        ATT_T(6)
         ++oph;
         tc_fence_after();
         if (out_warp) add_o(acc, h0);
         tc_fence_before();
-        release_item();
+        release_item();  // (the V slot)
+        ATT_T(7)
+#undef ATT_T
       }
-      // the unit's state per head: m (the same in both position warps), l = the sum over lanes
-      // and position warps
-      if (pos_warp) {
+      // the unit's state per head: m (the same in every warp of a head group), l = the sum over
+      // lanes and lane quadrants
 #pragma unroll
-        for (int j = 0; j < GH; ++j) {
-          float s = lw[j];
+      for (int j = 0; j < GH; ++j) {
+        float s = lw[j];
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-          if (lane == 0) {
-            m->alw[q4][h0 + j] = s;
-            if (q4 == 0) m->amr[h0 + j] = mrun[j];
-          }
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) {
+          m->alw[q4][h0 + j] = s;
+          if (q4 == 0) m->amr[h0 + j] = mrun[j];
         }
       }
       dead = cons_any(dead);  // (one verdict: the packing below is warp-collective)
@@ -1417,7 +1392,7 @@ struct WConsumer {
 #pragma unroll
           for (int j = 0; j < GH; ++j) {
             const int h = h0 + j;
-            const float L = m->alw[0][h] + m->alw[1][h];
+            const float L = (m->alw[0][h] + m->alw[1][h]) + (m->alw[2][h] + m->alw[3][h]);
             const float wgt = (m->amr[h] == -INFINITY || !(L > 0.f)) ? 0.f : 1.f / L;
             ob[h * HD + d] = bf16f(f2bf(wgt * acc[j]));
           }
@@ -1439,7 +1414,7 @@ struct WConsumer {
           dst[(size_t)h * (HD + 2) + d] = acc[j];
           if (d == 0) {
             dst[(size_t)h * (HD + 2) + HD] = m->amr[h];
-            dst[(size_t)h * (HD + 2) + HD + 1] = m->alw[0][h] + m->alw[1][h];
+            dst[(size_t)h * (HD + 2) + HD + 1] = (m->alw[0][h] + m->alw[1][h]) + (m->alw[2][h] + m->alw[3][h]);
           }
         }
       }
