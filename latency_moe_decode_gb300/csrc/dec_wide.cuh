@@ -288,11 +288,14 @@ __device__ int range_slots(const KParams& p, const WMisc* m, int kind, const WGe
 template <int NR>
 __device__ __forceinline__ int b_off(int n, int j) { return n == 2 ? 2 * kTileBytes + j * (b_area(NR) / 2) : kTileBytes; }
 
+// min(8, kGC / w) for B rows w = 16, 32, .., 128 (without a division)
+static_assert(kGC == 256, "group_tiles assumes 256 columns per group");
+__device__ __forceinline__ int group_tiles(int w) { return w <= 32 ? 8 : w == 48 ? 5 : w == 64 ? 4 : w == 80 ? 3 : 2; }
 template <int NR>
 __device__ __forceinline__ GroupShape group_shape(const KParams& p, const WMisc* m, int kind, const WGeo& g, int t) {
   GroupShape s;
   s.w = min(NR, brows(tile_tokens(p, m, kind, g, t)));
-  s.gt = min(8, kGC / s.w);
+  s.gt = group_tiles(s.w);
   return s;
 }
 
@@ -446,10 +449,53 @@ struct WProducer {
     wsplit(g, m, p, kind, U, gridDim.x);
     const int t0 = wstart(g, blockIdx.x, gridDim.x), t1 = wstart(g, blockIdx.x + 1, gridDim.x);
     const LayerDev& Ld = p.layers[l < p.L ? l : 0];
+    // Tile sources walked incrementally (the same as tile_src / b_src / slot_take give, without
+    // a division or popcount per tile): the segment start (k block kb = t - seg0), the expert
+    // slot u of tile t with its first tile, weights and B rows.
+    const bool ex = kind == K_RTGU || kind == K_D;
+    int seg0 = (t0 / g.kbs) * g.kbs;
+    int u = ex ? t0 / g.tpe : 0;
+    int u0 = ex ? u * g.tpe : 0, u1 = ex ? u0 + g.tpe : t1;
+    auto rows_of = [&](int uu) { return min(NR, brows(ex ? __popcll(m->umask[uu]) : p.B)); };
+    auto wbase = [&](int uu) -> const uint8_t* {
+      switch (kind) {
+        case K_QKV: return Ld.qkv;
+        case K_O: return Ld.o;
+        case K_ROUTER: return Ld.router;
+        case K_SHGU: return Ld.sh_gu;
+        case K_RTGU: return Ld.e_gu + (size_t)elist[uu] * p.e_gu_stride;
+        case K_D: return uu < U ? Ld.e_d + (size_t)elist[uu] * p.e_d_stride : Ld.sh_d;
+        default: return p.lm;
+      }
+    };
+    auto bbase = [&](int uu) -> const uint8_t* {
+      switch (kind) {
+        case K_O: return w.pbo;
+        case K_D: return w.pbh + (size_t)uu * p.kb_i * PBS;
+        case K_RTGU: return w.pbg + (size_t)uu * p.kb_d * PBS;
+        default: return w.pbx;
+      }
+    };
+    int rows_u = t0 < t1 ? rows_of(u) : 0;
+    const uint8_t* wb = t0 < t1 ? wbase(u) : nullptr;
+    const uint8_t* bbs = t0 < t1 ? bbase(u) : nullptr;
+    auto advance_to = [&](int t) {
+      while (t >= seg0 + g.kbs) seg0 += g.kbs;
+      while (t >= u1) {
+        ++u;
+        u0 = u1;
+        u1 += g.tpe;
+        rows_u = rows_of(u);
+        wb = wbase(u);
+        bbs = bbase(u);
+      }
+    };
     for (int t = t0; t < t1;) {
       int slot;
       if (!claim(slot, true)) return;
-      const int n = slot_take<NR>(p, m, kind, g, t, t1);
+      advance_to(t);
+      const int r1 = t + 1 < u1 ? rows_u : (t + 1 < t1 ? rows_of(u + 1) : 0);
+      const int n = (t + 1 < t1 && rows_u <= pair_rows(NR) && r1 <= pair_rows(NR)) ? 2 : 1;  // (slot_take)
       const uint8_t* a[2];
       const uint8_t* b[2];
       unsigned bb[2];  // B bytes of each tile: its tokens' rows
@@ -458,9 +504,10 @@ struct WProducer {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         if (j < n) {
-          a[j] = tile_src(kind, Ld, g, t + j, U, elist);
-          b[j] = b_src(kind, g, t + j);
-          bb[j] = (unsigned)tile_rows<NR>(p, m, kind, g, t + j) * 128u;
+          if (j) advance_to(t + 1);
+          a[j] = wb + (size_t)(t + j - u0) * kTileBytes;
+          b[j] = bbs + (size_t)(t + j - seg0) * PBS;
+          bb[j] = (unsigned)rows_u * 128u;
           tx += kTileBytes + bb[j];
           ok = ok && within(a[j], kTileBytes, p.warena, p.warena_bytes) && within(b[j], bb[j], w.pb, w.pb_bytes);
         }
@@ -599,6 +646,8 @@ struct WMma {
   unsigned gseq = 0;
   unsigned stage = 0;  // GEMV stages reached
   unsigned long long tw_full = 0, tw_tmem = 0;  // diagnostics: wait totals in routed gate/up stages
+  // diagnostics: its stage time, MMA issue time and tiles in the routed gate/up and down stages
+  unsigned long long tw_mstage[2] = {0, 0}, tw_miss[2] = {0, 0}, tw_mtiles[2] = {0, 0};
   bool dead = false;
   uint32_t tmem = 0;
   unsigned lay = 0;
@@ -637,15 +686,33 @@ struct WMma {
   __device__ void gemv(int kind, int U) {
     ++stage;
     wait_stage();
+    const int dk = kind == K_D ? 1 : 0;
+    const bool twx = DEC_TRACE && (kind == K_RTGU || kind == K_D);
+    const unsigned long long cs = twx ? gtimer() : 0;
     WGeo g = wgeo(p, kind, U, gridDim.x);
     wsplit(g, m, p, kind, U, gridDim.x);
     const int t0 = wstart(g, blockIdx.x, gridDim.x), t1 = wstart(g, blockIdx.x + 1, gridDim.x);
     int j = 0, ns = 0;  // tile j of the current slot of ns tiles
+    // The same tile, slot and group sequence as slot_take / group_shape give, walked
+    // incrementally (this warp's bookkeeping paces the expert stages at large batches: integer
+    // divisions and popcounts per tile cost more than the tile's MMAs): the segment's end, the
+    // expert slot's end and its B rows follow t.
+    const bool ex = kind == K_RTGU || kind == K_D;
+    int seg_end = (t0 / g.kbs + 1) * g.kbs;
+    int u = ex ? t0 / g.tpe : 0;
+    int u_end = ex ? (u + 1) * g.tpe : t1;
+    auto rows_of = [&](int uu) { return min(NR, brows(ex ? __popcll(m->umask[uu]) : p.B)); };
+    int rows_u = t0 < t1 ? rows_of(u) : 0;
 #pragma unroll 1
     for (int t = t0; t < t1;) {
-      const int seg = t / g.kbs;
-      const GroupShape gs = group_shape<NR>(p, m, kind, g, t);
-      const int n = min(gs.gt, min(t1, (seg + 1) * g.kbs) - t);
+      while (t >= seg_end) seg_end += g.kbs;
+      while (t >= u_end) {
+        ++u;
+        u_end += g.tpe;
+        rows_u = rows_of(u);
+      }
+      const GroupShape gs{rows_u, group_tiles(rows_u)};
+      const int n = min(gs.gt, min(t1, seg_end) - t);
       const int gsl = gseq % kNGW;
       const bool tw = DEC_TRACE && kind == K_RTGU;
       unsigned long long c0 = tw ? gtimer() : 0;
@@ -653,14 +720,16 @@ struct WMma {
       if (tw) tw_tmem += gtimer() - c0;
 #pragma unroll 1
       for (int i = 0; i < n; ++i, ++t) {
-        if (j == 0) {
-          ns = slot_take<NR>(p, m, kind, g, t, t1);
+        if (j == 0) {  // (slot_take)
+          const int r1 = t + 1 < u_end ? rows_u : (t + 1 < t1 ? rows_of(u + 1) : 0);
+          ns = (t + 1 < t1 && rows_u <= pair_rows(NR) && r1 <= pair_rows(NR)) ? 2 : 1;
           if (tw) c0 = gtimer();
           if (!dead && !mbar_wait(&full[slot], lap & 1, p, 49)) dead = true;
           if (tw) tw_full += gtimer() - c0;
         }
         const uint8_t* a = ring + (size_t)slot * SB + (size_t)j * kTileBytes;
         const uint8_t* b = ring + (size_t)slot * SB + b_off<NR>(ns, j);
+        const unsigned long long ci = twx ? gtimer() : 0;
         if (!dead) {
           tc_fence_after();
           m->hdr[gsl][i] = *reinterpret_cast<const float2*>(a + kTileData);
@@ -670,6 +739,10 @@ struct WMma {
 #pragma unroll
           for (int k = 0; k < kTileK / 32; ++k)
             mma_e4m3(d, ad + (uint64_t)(k * 16), bd + (uint64_t)(k * 16), idesc, k > 0 ? 1u : 0u);
+        }
+        if (twx) {
+          tw_miss[dk] += gtimer() - ci;
+          ++tw_mtiles[dk];
         }
         if (++j == ns) {
           if (!dead) mma_commit(&mempty[slot]);
@@ -683,6 +756,7 @@ struct WMma {
       }
       ++gseq;
     }
+    if (twx) tw_mstage[dk] += gtimer() - cs;
   }
 
   __device__ void run() {
@@ -720,6 +794,11 @@ struct WMma {
     if (DEC_TRACE && blockIdx.x == 0) {
       p.trace[kWaitTrace + 2] = tw_full;
       p.trace[kWaitTrace + 3] = tw_tmem;
+      for (int i = 0; i < 2; ++i) {
+        p.trace[kWaitTrace + 20 + 3 * i] = tw_mstage[i];
+        p.trace[kWaitTrace + 21 + 3 * i] = tw_miss[i];
+        p.trace[kWaitTrace + 22 + 3 * i] = tw_mtiles[i];
+      }
     }
     mbar_arrive(&m->mma_done);
   }
