@@ -121,7 +121,7 @@ struct WMisc {
   unsigned long long umask[kMaxExperts + 1];  // tokens routed to expert slot u (slot U: shared)
   int pw[kMaxExperts + 2];                    // prefix sums of the slots' tile weights (wsplit)
   int wmax;                                   // the heaviest slot's weight
-  uint8_t wsel[kWideMax][kWideTopk];          // expert slot of each token's selections
+  alignas(8) uint8_t wsel[kWideMax][kWideTopk];  // expert slot of each token's selections
   float wgate[kWideMax][kWideTopk];           // and their gates
   float rsum[kConsumerWarps];
   // attention on the tensor cores: the consumers' own MMA completions, and per tile the two
@@ -829,6 +829,7 @@ struct WConsumer {
   unsigned nbar = 0;  // grid barriers passed
   unsigned nstage = 0;  // GEMV stages begun (thread 0)
   unsigned long long tw_prod = 0, tw_stage = 0, tw_ld = 0, tw_flush = 0;  // diagnostics (thread 0): routed gate/up
+  unsigned long long tw_dprod = 0, tw_dstage = 0, tw_dflush = 0;  // the same in the down projection
   int rtgu_seen = 0;
   unsigned sph = 0, oph = 0;  // attention MMA completions waited for (phases of sbar, obar)
   unsigned long long tw_kv = 0, tw_attn = 0, tw_pro = 0, tw_post = 0;  // diagnostics: attention
@@ -1002,9 +1003,10 @@ struct WConsumer {
   __device__ __forceinline__ void epilogue(unsigned gs, int n, int sw, int kind, const WGeo& g, int t, int u_lo,
                                           int) {
     const int gsl = gs % kNGW;
-    const unsigned long long c0 = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
+    const unsigned long long c0 = (DEC_TRACE && (kind == K_RTGU || kind == K_D)) ? gtimer() : 0;
     if (!dead && !mbar_wait(&m->tfull[gsl], (gs / kNGW) & 1, p, 54)) dead = true;
     if (DEC_TRACE && kind == K_RTGU && tid == 0) tw_prod += gtimer() - c0;
+    if (DEC_TRACE && kind == K_D && tid == 0) tw_dprod += gtimer() - c0;
     dead = __any_sync(0xffffffffu, dead);  // (the TMEM loads below are warp-collective)
     const int q = warp & 3, h = warp >> 2, row = 32 * q + lane;
     const int seg = t / g.kbs, kb0 = t - seg * g.kbs;
@@ -1052,10 +1054,16 @@ struct WConsumer {
     if (lane == 0) mbar_arrive(&m->tempty[gsl]);
   }
 
+  // token t's gate for expert slot u: its selections' slots as one 8-byte word, the matching
+  // byte found without a loop (a token selects a slot at most once)
   __device__ float gate_of(int t, int u) const {
-    for (int k = 0; k < p.topk; ++k)
-      if (m->wsel[t][k] == u) return m->wgate[t][k];
-    return 0.f;
+    static_assert(kWideTopk == 8, "one 8-byte word of selections per token");
+    const unsigned long long x =
+        *reinterpret_cast<const unsigned long long*>(m->wsel[t]) ^ (0x0101010101010101ull * (unsigned)u);
+    const unsigned long long z = (x - 0x0101010101010101ull) & ~x & 0x8080808080808080ull;  // zero bytes
+    if (z == 0ull) return 0.f;
+    const int k = (__ffsll((long long)z) - 1) >> 3;  // (the lowest zero byte is found exactly)
+    return k < p.topk ? m->wgate[t][k] : 0.f;
   }
 
   // One segment's partial sums of the CTA: plain stores (read after the next grid barrier), per
@@ -1108,7 +1116,7 @@ struct WConsumer {
   }
 
   __device__ void gemv(int kind, int U) {
-    const unsigned long long cs = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
+    const unsigned long long cs = (DEC_TRACE && (kind == K_RTGU || kind == K_D)) ? gtimer() : 0;
     WGeo g = wgeo(p, kind, U, gridDim.x);
     wsplit(g, m, p, kind, U, gridDim.x);
     const int t0 = wstart(g, blockIdx.x, gridDim.x), t1 = wstart(g, blockIdx.x + 1, gridDim.x);
@@ -1144,9 +1152,10 @@ struct WConsumer {
     for (int t = t0;;) {
       const int seg = t < t1 ? t / g.kbs : -1;
       if (t == t1 || seg != seg_cur) {
-        const unsigned long long cf = (DEC_TRACE && kind == K_RTGU) ? gtimer() : 0;
+        const unsigned long long cf = (DEC_TRACE && (kind == K_RTGU || kind == K_D)) ? gtimer() : 0;
         if (seg_cur >= 0) flush(kind, g, seg_cur, seg_first, U);
         if (DEC_TRACE && kind == K_RTGU && tid == 0) tw_flush += gtimer() - cf;
+        if (DEC_TRACE && kind == K_D && tid == 0) tw_dflush += gtimer() - cf;
         if (t == t1) break;
         seg_cur = seg;
         seg_first = t;
@@ -1164,6 +1173,7 @@ struct WConsumer {
     // the stage's slots (freed by the MMA warp): keep the ring position in step
     ring_skip(range_slots<NR>(p, m, kind, g, t0, t1));
     dead = cons_any(dead);
+    if (DEC_TRACE && kind == K_D && tid == 0) tw_dstage += gtimer() - cs;
     if (DEC_TRACE && kind == K_RTGU && tid == 0) {
       const unsigned long long dt = gtimer() - cs;
       tw_stage += dt;
@@ -1955,6 +1965,9 @@ struct WConsumer {
       p.trace[kWaitTrace + 5] = tw_stage;
       p.trace[kWaitTrace + 6] = tw_ld;
       p.trace[kWaitTrace + 7] = tw_flush;
+      p.trace[kWaitTrace + 26] = tw_dprod;
+      p.trace[kWaitTrace + 27] = tw_dstage;
+      p.trace[kWaitTrace + 28] = tw_dflush;
       p.trace[kWaitTrace + 8] = tw_kv;
       p.trace[kWaitTrace + 9] = tw_attn;
       p.trace[kWaitTrace + 10] = tw_pro;
