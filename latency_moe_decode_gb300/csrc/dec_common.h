@@ -25,7 +25,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + the producer warp and the MMA warp
 constexpr int kKvTilePos = 64;                       // KV positions per ring slot
 constexpr int kMaxBatch = 8;                         // tokens of one step of decode_step_kernel
-constexpr int kWideMax = 64;                         // tokens of one step of the wide kernel (8 .. 64)
+constexpr int kWideMax = 64;                         // tokens of one step of the wide kernel (5 .. 64)
 constexpr int kMaxHidden = 4096;                     // hidden sizes the kernel handles
 constexpr int kTraceSlots = 512;                     // CTA-0 / producer trace words per step
 #ifndef DEC_STAMPS
@@ -143,7 +143,7 @@ struct KParams {
   unsigned long long timeout_ns;
 };
 
-// The wide kernel's own buffers (steps of 8 .. 64 tokens). Every GEMV stage input is kept in
+// The wide kernel's own buffers (steps of 5 .. 64 tokens). Every GEMV stage input is kept in
 // global memory as the tensor cores' B operand: per k block of 128 activations one block of
 // nr rows x 128 bytes (token t's two E4M3 pieces in rows 2t and 2t + 1, canonical K-major layout
 // of 8-row x 16-byte core matrices; nr = the kernel's row count, 32, 64 or 128) and one exponent

@@ -1,4 +1,4 @@
-// The wide decode kernels (steps of 8 .. 64 tokens), compiled in their own translation unit.
+// The wide decode kernels (steps of 5 .. 64 tokens), compiled in their own translation unit.
 #include "dec_wide.cuh"
 #include "dec_wide_host.h"
 

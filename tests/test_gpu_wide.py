@@ -1,4 +1,4 @@
-"""GPU parity of the wide kernel (decode steps of 8 .. 64 sequences: every GEMV on the tensor cores
+"""GPU parity of the wide kernel (decode steps of 5 .. 64 sequences: every GEMV on the tensor cores
 with the step's tokens as N, tokens grouped per routed expert) against the CPU oracle, through
 the C ABI. Each sequence has its own seeded KV history and is compared with the oracle's decode
 of that sequence alone.
