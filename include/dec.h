@@ -122,9 +122,11 @@ dec_status dec_validate_cfg(const dec_model_cfg* cfg);
    library-owned memory (repacked into the kernel's tile order; the caller may free its buffers
    once the call returns), builds the RoPE table (angles in double on the host), allocates the
    KV cache [n_layers][max_batch][n_kv_heads][max_ctx][head_dim] bf16 x2 and the workspace, and
-   checks that one CTA per SM can be co-resident. All sequence lengths start at 0. Work is
-   queued on `stream` and synchronised before return. *out receives the engine (NULL on
-   failure).
+   checks that one CTA per SM can be co-resident. An engine of max_batch >= 5 also builds the
+   wide kernel's buffers and two tensor maps over the K and V caches (the driver's
+   cuTensorMapEncodeTiled, reached through the runtime; DEC_ERR_CUDA if it is missing). All
+   sequence lengths start at 0. Work is queued on `stream` and synchronised before return. *out
+   receives the engine (NULL on failure).
    Environment, read here: DEC_TIMEOUT_MS bounds every device-side wait (default 1000);
    DEC_INFLIGHT / DEC_WIDE_INFLIGHT set how many ring slots one CTA keeps in flight (defaults 2
    and 4; tuning only); DEC_WIDE_MIN_BATCH (2..9, default 5) is the smallest decode batch that
@@ -198,7 +200,8 @@ dec_status dec_prefill_kv_noalloc(dec_engine* eng, const dec_ctx* ctx);
    DEC_ERR_POISONED, DEC_ERR_CUDA (launch failure).
    Batches of 5 .. 64 (engines built with max_batch >= 5) run the wide kernel: every GEMV on the
    tensor cores with all of the step's tokens as the N dimension, tokens grouped per routed expert
-   (an expert's products kept for the tokens routed to it), phases separated by grid barriers
+   (an expert's products kept for the tokens routed to it), attention as bf16 tensor-core products
+   on KV tiles loaded by tensor-map copies, phases separated by grid barriers
    ("vLLM's Kimi K3 Backend Hits 842 Tokens per Second", section "A narrow deployment lane":
    decode batches up to 64). Same arguments, results and errors. */
 typedef struct {
